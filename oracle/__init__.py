@@ -1,0 +1,171 @@
+"""TEST INFRASTRUCTURE: the fp64 CPU oracle for MLA paged-KV decode.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py`` (its cpu
+baseline and ``--impl reference`` arm) may import this package.  The product
+path (``mla_paged_kv_decode_gb300``) never does, and shares no code with it.
+
+Two independent implementations live here:
+  * ``mla_decode`` / ``mla_decode_range`` / ``merge`` / ``e4m3_*``: plain C in
+    fp64 (``mla_oracle.c``), the definition written out loop by loop;
+  * ``brute.brute_force``: torch fp64, materialising K and V by Python
+    indexing and calling ``torch.softmax`` / ``torch.logsumexp``, used to pin
+    the C oracle on small shapes.
+See ``mla_oracle.c`` for the definition and the pages it follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mla_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(out_path: str = _LIB_PATH, plant: int = 0) -> str:
+    """Compile the oracle (gcc, -O2, OpenMP).  ``plant`` != 0 builds a copy with a
+    deliberate mistake, used only by the test that proves the pins catch it."""
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-shared", "-fPIC", f"-DORACLE_PLANT={int(plant)}",
+           _SRC, "-o", out_path, "-lm"]
+    subprocess.run(cmd, check=True)
+    return out_path
+
+
+def _bind(lib):
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    lib.oracle_mla_decode.restype = ctypes.c_int
+    lib.oracle_mla_decode.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                      ctypes.c_void_p, ctypes.c_void_p, i32p, i32p, i32p,
+                                      ctypes.c_double, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+    lib.oracle_mla_decode_range.restype = ctypes.c_int
+    lib.oracle_mla_decode_range.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                            ctypes.c_void_p, ctypes.c_void_p, i32p, i32p,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                            ctypes.c_void_p, ctypes.c_void_p]
+    lib.oracle_merge.restype = None
+    lib.oracle_merge.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    lib.oracle_e4m3_decode.restype = ctypes.c_double
+    lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+    lib.oracle_e4m3_encode.argtypes = [ctypes.c_double]
+    return lib
+
+
+def load(path: Optional[str] = None):
+    """Load (building first if needed) the oracle library."""
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+            build()
+        _lib = _bind(ctypes.CDLL(_LIB_PATH))
+    return _lib
+
+
+def _u16(t: torch.Tensor) -> np.ndarray:
+    assert t.dtype == torch.bfloat16
+    return np.ascontiguousarray(t.contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def _i32(t) -> np.ndarray:
+    return np.ascontiguousarray(torch.as_tensor(t).to(torch.int32).numpy())
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _ip(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+def _cache_arrays(ckv, ckv_scale):
+    if ckv.dtype == torch.uint8:
+        assert ckv_scale is not None, "8-bit cache needs its per-token scales"
+        return np.ascontiguousarray(ckv.contiguous().numpy()), 1, \
+            np.ascontiguousarray(ckv_scale.contiguous().to(torch.float32).numpy())
+    return _u16(ckv), 0, None
+
+
+def mla_decode(q_nope, q_pe, ckv, kpe, kv_indices, kv_indptr, kv_last_page_len, sm_scale,
+               ckv_scale=None, threads: int = 0, lib=None):
+    """fp64 oracle.  CPU tensors in the library's layout; returns (out [B,H,512], lse [B,H])
+    as float64 torch tensors."""
+    lib = lib or load()
+    B, H, _ = q_nope.shape
+    P = ckv.shape[1]
+    qn, qp, kp = _u16(q_nope), _u16(q_pe), _u16(kpe)
+    ck, is8, sc = _cache_arrays(ckv, ckv_scale)
+    ind, iptr, last = _i32(kv_indices), _i32(kv_indptr), _i32(kv_last_page_len)
+    out = np.zeros((B, H, 512), dtype=np.float64)
+    lse = np.zeros((B, H), dtype=np.float64)
+    rc = lib.oracle_mla_decode(B, H, P, _ptr(qn), _ptr(qp), _ptr(ck), is8,
+                               _ptr(sc) if sc is not None else None, _ptr(kp),
+                               _ip(ind), _ip(iptr), _ip(last), float(sm_scale),
+                               _ptr(out), _ptr(lse), int(threads))
+    if rc != 0:
+        raise MemoryError("oracle_mla_decode failed")
+    return torch.from_numpy(out), torch.from_numpy(lse)
+
+
+def mla_decode_range(b, t_begin, t_end, q_nope, q_pe, ckv, kpe, kv_indices, kv_indptr, sm_scale,
+                     ckv_scale=None, lib=None):
+    """Partial (out [H,512], lse [H]) of request b over its tokens [t_begin, t_end)."""
+    lib = lib or load()
+    B, H, _ = q_nope.shape
+    P = ckv.shape[1]
+    qn, qp, kp = _u16(q_nope), _u16(q_pe), _u16(kpe)
+    ck, is8, sc = _cache_arrays(ckv, ckv_scale)
+    ind, iptr = _i32(kv_indices), _i32(kv_indptr)
+    out = np.zeros((H, 512), dtype=np.float64)
+    lse = np.zeros((H,), dtype=np.float64)
+    rc = lib.oracle_mla_decode_range(H, P, int(b), _ptr(qn), _ptr(qp), _ptr(ck), is8,
+                                     _ptr(sc) if sc is not None else None, _ptr(kp), _ip(ind), _ip(iptr),
+                                     int(t_begin), int(t_end), float(sm_scale), _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise MemoryError("oracle_mla_decode_range failed")
+    return torch.from_numpy(out), torch.from_numpy(lse)
+
+
+def merge(o_parts, lse_parts, lib=None):
+    """Merge k partials [k,H,D] / [k,H] (fixed order) -> (out [H,D], lse [H])."""
+    lib = lib or load()
+    o = np.ascontiguousarray(torch.as_tensor(o_parts, dtype=torch.float64).numpy())
+    s = np.ascontiguousarray(torch.as_tensor(lse_parts, dtype=torch.float64).numpy())
+    k, H, D = o.shape
+    out = np.zeros((H, D), dtype=np.float64)
+    lse = np.zeros((H,), dtype=np.float64)
+    lib.oracle_merge(k, H, D, _ptr(o), _ptr(s), _ptr(out), _ptr(lse))
+    return torch.from_numpy(out), torch.from_numpy(lse)
+
+
+def e4m3_decode(codes, lib=None) -> np.ndarray:
+    lib = lib or load()
+    return np.array([lib.oracle_e4m3_decode(int(c)) for c in np.asarray(codes).ravel()], dtype=np.float64)
+
+
+def e4m3_encode(values, lib=None) -> np.ndarray:
+    lib = lib or load()
+    return np.array([lib.oracle_e4m3_encode(float(v)) for v in np.asarray(values, dtype=np.float64).ravel()],
+                    dtype=np.uint8)
+
+
+def decode_inputs(inp, threads: int = 0, use_bf16_cache: bool = False):
+    """Run the oracle on a ``workloads.Inputs``.  ``use_bf16_cache`` runs an 8-bit
+    workload on the bf16 cache it was quantised from."""
+    if inp.ckv_scale is not None and not use_bf16_cache:
+        return mla_decode(inp.q_nope, inp.q_pe, inp.ckv, inp.kpe, inp.kv_indices, inp.kv_indptr,
+                          inp.kv_last_page_len, inp.sm_scale, ckv_scale=inp.ckv_scale, threads=threads)
+    ckv = inp.ckv_bf16 if inp.ckv_scale is not None else inp.ckv
+    return mla_decode(inp.q_nope, inp.q_pe, ckv, inp.kpe, inp.kv_indices, inp.kv_indptr,
+                      inp.kv_last_page_len, inp.sm_scale, threads=threads)
