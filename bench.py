@@ -1,0 +1,389 @@
+#!/usr/bin/env python
+"""Benchmark of MLA paged-KV decode on GB300.
+
+One step = one decode of one batch: the attention kernel and the split-KV
+combine (mla_decode_attention + mla_decode_combine through the C ABI) over a
+synthetic batch shaped like the DeepSeek-V2-Lite memory-bound workload
+(batch 64, h_q 16, page 64, kv_len 4096; seeded gaussian bf16, random page
+placement).  The plan is built once per batch composition, outside the
+timed region, as a serving loop would reuse it across layers.
+
+Prints ONE JSON line (rank 0).  Metric: KV GB/s (algorithmic bytes / time;
+bytes = tokens x 1152 + q + out + lse + page indices).  A secondary object
+reports TFLOPS on the DeepSeek-V3-shaped compute workload (batch 128,
+h_q 128, kv 8192).  --impl reference times the fp64 CPU oracle instead.
+Multi-GPU (torchrun): every rank decodes its own batch on its own GPU (the
+path has no exchange step, so ranks are replicas); value = all ranks' bytes /
+the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from workloads import WORKLOADS, algorithmic_bytes, algorithmic_flops, make_inputs  # noqa: E402
+
+METRIC = "MLA decode: KV GB/s (h_q=16) & TFLOPS (h_q=128) vs GB300 roofline"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", FALLBACK_HBM_GBS), d.get("bf16_tflops", FALLBACK_BF16_TFLOPS), \
+            d.get("bf16_tflops_sustained"), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, None, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mla_paged_kv_decode_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """dram bytes per launch of the attention kernel from a committed ncu summary,
+    only if it was taken on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_sources") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 50 ms in a background process."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.samples:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((ts, parts))
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        if not inside and rows:  # region shorter than the sampling period: nearest samples
+            inside = sorted(rows, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))[:2]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(p[1]) for _, p in inside if p[1].replace(".", "").isdigit()]
+        smax = [float(p[2]) for _, p in inside if p[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for _, p in inside for n, v in zip(names, p[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(inside)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def aggregate(per_rank_seconds, per_rank_units, world):
+    """Whole-job throughput: units of every rank / the slowest rank's time."""
+    t = max(per_rank_seconds)
+    return sum(per_rank_units) / t, t
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def time_oracle(inp, requests, threads):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.decode_subset(inp, requests, threads=threads)
+    return time.perf_counter() - t0
+
+
+def subset_bytes(inp, requests):
+    H = inp.h_q
+    per_tok = 644 if inp.ckv_scale is not None else 1152
+    L = int(inp.kv_lens[requests].sum())
+    n = sum(int(inp.kv_indptr[b + 1] - inp.kv_indptr[b]) for b in requests)
+    return L * per_tok + len(requests) * (H * 576 * 2 + H * 512 * 4 + H * 4 + 8) + 4 * n
+
+
+def run_reference(args):
+    """The oracle, as it stands, on the host cores: a bounded sample of the workload per step."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    inp = make_inputs(WORKLOADS[args.workload])
+    cores = cpu_cores()
+    sample = list(range(min(args.sample_requests, inp.batch)))
+    for _ in range(args.warmup):
+        time_oracle(inp, sample, cores)
+    ts = [time_oracle(inp, sample, cores) for _ in range(args.steps)]
+    sec = sum(ts) / len(ts)
+    gbs = subset_bytes(inp, sample) / sec / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "desc": WORKLOADS[args.workload].description,
+                       "sample_requests": len(sample)},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{len(sample)} of {inp.batch} requests of {args.workload} per step"},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def bench_device(inp, steps, warmup, stream):
+    """Device-timed steps with resident inputs.  Returns per-step and per-kernel times (s)."""
+    import mla_paged_kv_decode_gb300 as mla
+    d = inp.to("cuda")
+    kvd = mla.MLA_KV_FP8_E4M3 if inp.ckv_scale is not None else mla.MLA_KV_BF16
+    dec = mla.Decoder(inp.kv_indptr, inp.kv_last_page_len, inp.h_q, inp.page_size, kv_dtype=kvd, stream=stream)
+    out = torch.empty(inp.batch, inp.h_q, 512, dtype=torch.float32, device="cuda")
+    lse = torch.empty(inp.batch, inp.h_q, dtype=torch.float32, device="cuda")
+    args = (d.q_nope, d.q_pe, d.ckv, d.ckv_scale, d.kpe, d.kv_indices, d.kv_indptr, d.kv_last_page_len,
+            inp.sm_scale, out, lse, dec.workspace)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        mla.mla_decode_attention(dec.plan, *args, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        mla.mla_decode_combine(dec.plan, out, lse, dec.workspace, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+    torch.cuda.synchronize()
+    return dec, step, (out, lse, d)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="membound", choices=sorted(WORKLOADS))
+    ap.add_argument("--secondary", default="compute", help="second workload to report (TFLOPS), or 'none'")
+    ap.add_argument("--sample-requests", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    import mla_paged_kv_decode_gb300 as mla
+    mla.load()
+
+    hbm_gbs, bf16_tf, bf16_tf_sus, peak_src = peaks()
+    inp = make_inputs(WORKLOADS[args.workload])
+    alg_bytes = algorithmic_bytes(inp)
+    alg_flops = algorithmic_flops(inp)
+    stream = torch.cuda.Stream()
+    dec, step, keep = bench_device(inp, args.steps, args.warmup, stream)
+    launches_per_step = mla.mla_plan_num_launches(dec.plan)
+
+    # ---- device-timed region (inputs resident in HBM, 1.2 GB > 129 MB L2 per step: no flush)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    sampler.stop()
+    total_s = start.elapsed_time(end) / 1e3
+    attn_s = [e[0].elapsed_time(e[1]) / 1e3 for e in evs]
+    comb_s = [e[1].elapsed_time(e[2]) / 1e3 for e in evs]
+    clocks = sampler.summary(t_wall0, t_wall1)
+
+    if world > 1:
+        t = torch.tensor([total_s], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_max = float(t)
+    else:
+        total_max = total_s
+    value, _ = aggregate([total_max], [alg_bytes * args.steps * world], world)
+    value /= 1e9
+    attn_avg = sum(attn_s) / len(attn_s)
+    comb_avg = sum(comb_s) / len(comb_s)
+    achieved = alg_bytes / attn_avg / 1e9
+
+    # ---- end to end through the public API with host buffers: per step H2D of the
+    # step's inputs (q_nope, q_pe and the page table) from pinned memory, run, D2H of out + lse
+    out, lse, d = keep
+    host_in = [t.cpu().pin_memory() for t in (inp.q_nope, inp.q_pe, inp.kv_indices, inp.kv_indptr,
+                                               inp.kv_last_page_len)]
+    dev_in = [d.q_nope, d.q_pe, d.kv_indices, d.kv_indptr, d.kv_last_page_len]
+    host_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory(),
+                torch.empty(lse.shape, dtype=lse.dtype).pin_memory()]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    e2e_steps = max(10, min(args.steps, 500))
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for hsrc, ddst in zip(host_in, dev_in):
+                ddst.copy_(hsrc, non_blocking=True)
+            mla.mla_decode_run(dec.plan, d.q_nope, d.q_pe, d.ckv, d.ckv_scale, d.kpe, d.kv_indices, d.kv_indptr,
+                               d.kv_last_page_len, inp.sm_scale, out, lse, dec.workspace, stream=stream)
+            host_out[0].copy_(out, non_blocking=True)
+            host_out[1].copy_(lse, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_s], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(t)
+    e2e_value = alg_bytes * world / e2e_s / 1e9
+
+    # ---- secondary: compute-shaped workload (TFLOPS), device-timed the same way
+    secondary = None
+    if args.secondary != "none" and rank == 0 and world == 1:
+        del keep, dec
+        torch.cuda.empty_cache()
+        inp2 = make_inputs(WORKLOADS[args.secondary])
+        dec2, step2, keep2 = bench_device(inp2, 0, 5, stream)
+        n2 = max(20, min(args.steps // 10, 200))
+        ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n2)]
+        torch.cuda.synchronize()
+        for i in range(n2):
+            step2(ev2[i])
+        torch.cuda.synchronize()
+        a2 = sum(e[0].elapsed_time(e[1]) for e in ev2) / n2 / 1e3
+        s2 = sum(e[0].elapsed_time(e[2]) for e in ev2) / n2 / 1e3
+        f2 = algorithmic_flops(inp2)
+        b2 = algorithmic_bytes(inp2)
+        secondary = {"workload": args.secondary, "desc": WORKLOADS[args.secondary].description,
+                     "us_per_step": s2 * 1e6, "tflops": f2 / s2 / 1e12, "kv_gbs": b2 / s2 / 1e9,
+                     "attention_us": a2 * 1e6,
+                     "tensor_frac": f2 / a2 / 1e12 / bf16_tf, "hbm_frac": b2 / a2 / 1e9 / hbm_gbs,
+                     "alg_flops": f2, "alg_bytes": b2}
+        del keep2, dec2
+
+    # ---- cpu baseline: the oracle on a bounded sample, host cores, rank 0 at N=1
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cores = cpu_cores()
+        sample = list(range(min(args.sample_requests, inp.batch)))
+        time_oracle(inp, sample[:1], cores)
+        sec = time_oracle(inp, sample, cores)
+        cpu = {"value": subset_bytes(inp, sample) / sec / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": f"{len(sample)} of {inp.batch} requests of {args.workload}, one pass, fp64"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_max / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": args.workload, "desc": WORKLOADS[args.workload].description,
+                       "global_batch": inp.batch * world, "kv_len": int(inp.kv_lens[0]), "h_q": inp.h_q,
+                       "page_size": inp.page_size, "parallelism": f"replicas x{world}",
+                       "l2": "no flush: each step streams 302 MB of KV, > 129 MB L2",
+                       "alg_bytes_per_step": alg_bytes, "alg_flops_per_step": alg_flops,
+                       "tflops": alg_flops * args.steps * world / total_max / 1e12},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                         "frac": achieved / hbm_gbs, "traffic": recorded_traffic(args.workload),
+                         "kernel": "mla_decode_attn_kernel", "peak_source": peak_src,
+                         "kernel_us": attn_avg * 1e6, "combine_us": comb_avg * 1e6},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "steps": e2e_steps, "note": "per step: H2D q + page table, decode, D2H out + lse; KV resident"},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+            "secondary": secondary,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

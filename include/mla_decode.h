@@ -1,0 +1,175 @@
+/*
+ * mla_decode.h -- C ABI of the GB300 (sm_103a) MLA paged-KV decode library.
+ *
+ * The operation is absorbed-weight Multi-head Latent Attention decode: multi-
+ * query attention with one shared KV head whose key is [ckv (512) | kpe (64)]
+ * and whose value is ckv itself ("Benchmarking MLA", FlashInfer issue #700:
+ * "what we actually need is a fused-rope MQA kernel"; for the matrix-absorbed
+ * kernel qk_head_dim = 512 + 64 and v_head_dim = 512).  For request b, head h:
+ *
+ *     x_t = sm_scale * (q_nope[b,h,:] . ckv_t + q_pe[b,h,:] . kpe_t)
+ *     out[b,h,:] = sum_t softmax(x)_t * ckv_t,   lse[b,h] = ln sum_t exp(x_t)
+ *
+ * over the request's cached tokens t.  The cache is paged as in "perf: MLA
+ * decode kernel implemented by CuTe targeted to SM80" (FlashInfer PR #844):
+ * ckv [num_pages, page_size, 512], kpe [num_pages, page_size, 64]; request b
+ * owns pages kv_indices[kv_indptr[b] .. kv_indptr[b+1]) in logical order, and
+ * its last page holds kv_last_page_len[b] tokens.  Token t is in page
+ * kv_indices[kv_indptr[b] + t / page_size], slot t % page_size.
+ *
+ * The split-KV scheduling (a host "plan" that balances work over the SMs)
+ * and the deterministic merge of split partials follow FlashMLA PR #233
+ * ("balanced scheduler, deterministic combine, graph-safe API"); the 8-bit
+ * cache follows the same page ("FP8 e4m3 ... with one scale per token (644
+ * instead of 1152 bytes per token), dequantized inside the kernel").
+ *
+ * Conventions for every call below
+ *   - Device pointers are CUDA device addresses on the current device; host
+ *     pointers are ordinary host memory.  The library never frees or keeps
+ *     caller memory beyond the call, except that a plan keeps its own host
+ *     copy of the work list (and a pinned staging buffer) until
+ *     mla_plan_destroy.
+ *   - All tensors are dense, row-major, contiguous.
+ *   - bf16 means IEEE bfloat16 bit patterns (uint16); fp32 is IEEE float.
+ *   - Errors are returned as mla_status_t; nothing is thrown across the ABI,
+ *     no call aborts the process.
+ *   - cuda_stream is a cudaStream_t passed as void* (NULL = legacy default).
+ */
+#ifndef MLA_DECODE_H_
+#define MLA_DECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct mla_plan_s* mla_plan_t; /* opaque, host-owned */
+
+typedef enum {
+    MLA_OK = 0,
+    MLA_ERR_INVALID_ARG = 1,         /* malformed sizes, indptr not monotone, last_page_len out of range */
+    MLA_ERR_UNSUPPORTED = 2,         /* h_q or page_size outside the supported set */
+    MLA_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace smaller than mla_decode_plan_workspace_bytes */
+    MLA_ERR_CUDA = 4,                /* a CUDA runtime/driver call or a launch failed */
+    MLA_ERR_DEVICE_TIMEOUT = 5,      /* a kernel's bounded wait ran out (read by mla_decode_device_status) */
+    MLA_ERR_NOT_COMMITTED = 6        /* mla_decode_run before mla_decode_plan_commit */
+} mla_status_t;
+
+typedef enum {
+    MLA_KV_BF16 = 0,     /* ckv bf16 [num_pages, page_size, 512] */
+    MLA_KV_FP8_E4M3 = 1  /* ckv uint8 e4m3 codes [num_pages, page_size, 512] + fp32 scale [num_pages, page_size] */
+} mla_kv_dtype_t;
+
+/* Build a balanced split-KV work list (host only, no device call).
+ *
+ * Work is measured in tokens.  Requests are laid out in order, cut into
+ * tiles of 128 tokens, and the tile sequence is partitioned into contiguous
+ * ranges of near-equal cost, one per CTA slot; a request cut across slots
+ * becomes several split pieces whose partial (out, lse) are merged after
+ * the attention kernel (FlashMLA PR #233, "balanced scheduler").
+ *
+ *   kv_indptr_host        host int32 [batch + 1], kv_indptr_host[0] == 0, non-decreasing
+ *   kv_last_page_len_host host int32 [batch]; in [1, page_size] for a request with pages,
+ *                         ignored (may be anything) for a request with no pages
+ *   batch                 >= 1
+ *   h_q                   query heads per request: 16, 32, 64 or 128
+ *   page_size             16, 32 or 64
+ *   num_sms               streaming multiprocessors to plan for (> 0), e.g. 152 on GB300
+ *   kv_dtype              cache element type the plan will be run with
+ *   plan_out              receives the new plan; untouched on error
+ * Returns MLA_OK, MLA_ERR_INVALID_ARG or MLA_ERR_UNSUPPORTED.
+ * The plan depends only on these host arrays, so it may be reused across
+ * layers and replays while they are unchanged; the contents of kv_indices
+ * (physical page placement) may change freely between runs. */
+mla_status_t mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_last_page_len_host, int batch,
+                             int h_q, int page_size, int num_sms, mla_kv_dtype_t kv_dtype, mla_plan_t* plan_out);
+
+/* Device workspace the plan needs (bytes, a multiple of 256): the work list,
+ * the split partials and a status word.  0 for a NULL plan. */
+size_t mla_decode_plan_workspace_bytes(mla_plan_t plan);
+
+/* Copy the plan's work list into the caller's device workspace with one
+ * cudaMemcpyAsync on cuda_stream, and clear its status word.  workspace_dev must
+ * be 256-byte aligned and at least mla_decode_plan_workspace_bytes(plan) long;
+ * it is owned by the caller and must stay alive and untouched by others while
+ * runs of this plan are in flight.  Commit once per (plan, workspace) pair,
+ * before mla_decode_run.  Returns MLA_OK, MLA_ERR_INVALID_ARG,
+ * MLA_ERR_WORKSPACE_TOO_SMALL or MLA_ERR_CUDA. */
+mla_status_t mla_decode_plan_commit(mla_plan_t plan, void* workspace_dev, size_t workspace_bytes,
+                                    void* cuda_stream);
+
+/* Enqueue one decode on cuda_stream: the attention kernel, then (only if the
+ * plan split a request or holds an empty one) the combine kernel.
+ *
+ *   q_nope           device bf16 [batch, h_q, 512]
+ *   q_pe             device bf16 [batch, h_q, 64]
+ *   ckv_cache        device bf16 [num_pages, page_size, 512], or uint8 e4m3 codes of the
+ *                    same shape for MLA_KV_FP8_E4M3
+ *   ckv_scale        NULL for bf16; device fp32 [num_pages, page_size] for e4m3
+ *                    (token t's ckv is ckv_scale[t] * e4m3(code))
+ *   kpe_cache        device bf16 [num_pages, page_size, 64]
+ *   num_pages        pages in the cache buffers (bounds the tensor maps; a page index
+ *                    outside [0, num_pages) reads zeros instead of memory)
+ *   kv_indices       device int32 [kv_indptr[batch]]
+ *   kv_indptr        device int32 [batch + 1], same values the plan was built from
+ *   kv_last_page_len device int32 [batch],     same values the plan was built from
+ *   sm_scale         softmax scale applied to q.k (e.g. 1/sqrt(192))
+ *   out              device fp32 [batch, h_q, 512]
+ *   lse              device fp32 [batch, h_q], natural log of sum_t exp(x_t); -inf and
+ *                    out = 0 for a request with no tokens
+ *   workspace_dev    the workspace passed to mla_decode_plan_commit
+ * Every device buffer needs 16-byte alignment.  Slots past kv_last_page_len
+ * and pages no request references are never used (they may hold NaN).
+ * The call allocates nothing, never synchronises and reads no device data on
+ * the host, so it may be captured in a CUDA graph; results are bit-identical
+ * for the same plan and inputs.  Returns MLA_OK, MLA_ERR_INVALID_ARG,
+ * MLA_ERR_NOT_COMMITTED or MLA_ERR_CUDA (launch failure). */
+mla_status_t mla_decode_run(mla_plan_t plan, const void* q_nope, const void* q_pe, const void* ckv_cache,
+                            const float* ckv_scale, const void* kpe_cache, int num_pages,
+                            const int32_t* kv_indices, const int32_t* kv_indptr,
+                            const int32_t* kv_last_page_len, float sm_scale, float* out, float* lse,
+                            void* workspace_dev, void* cuda_stream);
+
+/* The two launches of mla_decode_run, exposed separately (same arguments,
+ * same semantics when called back to back on one stream): the attention
+ * kernel, which writes out/lse of unsplit requests and the partials of split
+ * ones, and the combine kernel, which merges the partials in slot order and
+ * fills empty requests (FlashMLA PR #233, "deterministic combine").  Either
+ * is a no-op when the plan has no work for it. */
+mla_status_t mla_decode_attention(mla_plan_t plan, const void* q_nope, const void* q_pe, const void* ckv_cache,
+                                  const float* ckv_scale, const void* kpe_cache, int num_pages,
+                                  const int32_t* kv_indices, const int32_t* kv_indptr,
+                                  const int32_t* kv_last_page_len, float sm_scale, float* out, float* lse,
+                                  void* workspace_dev, void* cuda_stream);
+mla_status_t mla_decode_combine(mla_plan_t plan, float* out, float* lse, void* workspace_dev, void* cuda_stream);
+
+/* Kernel launches mla_decode_run issues for this plan (1 or 2; 0 for no work). */
+int mla_plan_num_launches(mla_plan_t plan);
+
+/* Synchronise cuda_stream and read the workspace's status word: MLA_OK, or
+ * MLA_ERR_DEVICE_TIMEOUT when a kernel gave up on a bounded wait (its outputs
+ * are then undefined).  The word is cleared after reading. */
+mla_status_t mla_decode_device_status(mla_plan_t plan, void* workspace_dev, void* cuda_stream);
+
+/* Introspection (host only, for tests and tools). */
+int mla_plan_num_ctas(mla_plan_t plan);       /* attention CTAs launched per run */
+int mla_plan_num_segments(mla_plan_t plan);   /* (request, token range) pieces */
+int mla_plan_num_partials(mla_plan_t plan);   /* split pieces that go through the combine */
+int mla_plan_heads_per_cta(mla_plan_t plan);
+/* Copy the work list: for segment i, out[4i..4i+3] = (request, token_begin, token_end,
+ * partial slot or -1); unit_ptr[u] .. unit_ptr[u+1] are unit u's segments.  Either
+ * pointer may be NULL.  Returns the number of segments. */
+int mla_plan_get_segments(mla_plan_t plan, int32_t* segments, int32_t* unit_ptr);
+
+void mla_plan_destroy(mla_plan_t plan);
+
+/* Static string for a status code. */
+const char* mla_status_string(mla_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DECODE_H_ */

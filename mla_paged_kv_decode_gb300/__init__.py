@@ -1,0 +1,56 @@
+"""MLA paged-KV decode for one NVIDIA GB300 (sm_103a).
+
+The computation runs in ``libmla_decode.so`` (hand-written CUDA: TMA page
+staging, tcgen05/TMEM attention, deterministic split-KV combine); this package
+is its ctypes binding.  ``Decoder`` bundles the usual call sequence
+(plan -> workspace -> commit -> run) for callers that let torch own memory.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from ._binding import (  # noqa: F401
+    EXPORTED, MLA_ERR_CUDA, MLA_ERR_DEVICE_TIMEOUT, MLA_ERR_INVALID_ARG, MLA_ERR_NOT_COMMITTED,
+    MLA_ERR_UNSUPPORTED, MLA_ERR_WORKSPACE_TOO_SMALL, MLA_KV_BF16, MLA_KV_FP8_E4M3, MLA_OK, MLAError, Plan,
+    library_path, load, mla_decode_device_status, mla_decode_plan, mla_decode_plan_commit,
+    mla_decode_plan_workspace_bytes, mla_decode_run, mla_plan_get_segments, mla_plan_heads_per_cta,
+    mla_plan_num_ctas, mla_plan_num_partials, mla_plan_num_segments, mla_status_string,
+    mla_decode_attention, mla_decode_combine, mla_plan_num_launches,
+)
+
+
+def num_sms(device=None) -> int:
+    return torch.cuda.get_device_properties(device or torch.cuda.current_device()).multi_processor_count
+
+
+class Decoder:
+    """Plan once for a batch composition, then run many times (graph-capturable).
+
+    kv_indptr / kv_last_page_len are taken on the host for the plan and kept
+    on the device for the kernels.
+    """
+
+    def __init__(self, kv_indptr: torch.Tensor, kv_last_page_len: torch.Tensor, h_q: int, page_size: int,
+                 kv_dtype: int = MLA_KV_BF16, device=None, sms: Optional[int] = None, stream=None):
+        device = torch.device(device or "cuda")
+        self.batch = int(kv_indptr.numel()) - 1
+        self.h_q, self.page_size, self.kv_dtype = h_q, page_size, kv_dtype
+        self.plan = mla_decode_plan(kv_indptr.cpu(), kv_last_page_len.cpu(), self.batch, h_q, page_size,
+                                    sms or num_sms(device), kv_dtype)
+        self.workspace = torch.empty(max(self.plan.workspace_bytes, 256), dtype=torch.uint8, device=device)
+        mla_decode_plan_commit(self.plan, self.workspace, stream)
+
+    def run(self, q_nope, q_pe, ckv_cache, kpe_cache, kv_indices, kv_indptr, kv_last_page_len, sm_scale,
+            ckv_scale=None, out=None, lse=None, stream=None):
+        if out is None:
+            out = torch.empty(self.batch, self.h_q, 512, dtype=torch.float32, device=q_nope.device)
+        if lse is None:
+            lse = torch.empty(self.batch, self.h_q, dtype=torch.float32, device=q_nope.device)
+        mla_decode_run(self.plan, q_nope, q_pe, ckv_cache, ckv_scale, kpe_cache, kv_indices, kv_indptr,
+                       kv_last_page_len, sm_scale, out, lse, self.workspace, stream)
+        return out, lse
+
+    def device_status(self, stream=None) -> int:
+        return mla_decode_device_status(self.plan, self.workspace, stream)

@@ -1,0 +1,262 @@
+// C ABI of the MLA paged decode library (declared in include/mla_decode.h):
+// plan lifetime, workspace commit, tensor-map setup and kernel launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "mla_decode.h"
+#include "attn.cuh"
+#include "combine.cuh"
+#include "plan.h"
+
+struct mla_plan_s {
+    mla::PlanData d;
+    std::vector<uint8_t> image;   // header bytes copied to the workspace by commit
+    void* pinned = nullptr;       // pinned staging copy of `image`
+    std::vector<void*> committed; // workspaces this plan has been committed to
+};
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix, box [box_rows, 64 columns],
+// 128-byte swizzle (one box row = 128 bytes).
+bool make_map_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+void build_image(mla_plan_s* p) {
+    const auto& L = p->d.layout;
+    p->image.assign(L.header_bytes, 0);
+    std::memcpy(p->image.data() + L.off_unit_ptr, p->d.unit_ptr.data(), sizeof(int32_t) * p->d.unit_ptr.size());
+    if (!p->d.segments.empty())
+        std::memcpy(p->image.data() + L.off_segments, p->d.segments.data(),
+                    sizeof(mla::Segment) * p->d.segments.size());
+    if (!p->d.items.empty())
+        std::memcpy(p->image.data() + L.off_items, p->d.items.data(), sizeof(mla::CombineItem) * p->d.items.size());
+}
+
+template <int HG>
+cudaError_t launch_attention(const mla_plan_s* p, const CUtensorMap& ckv, const CUtensorMap& kpe,
+                             const CUtensorMap& qn, const CUtensorMap& qp, const mla::AttnParams& prm,
+                             cudaStream_t stream) {
+    using C = mla::AttnCfg<HG>;
+    cudaError_t e = cudaFuncSetAttribute(mla::mla_decode_attn_kernel<HG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int grid = p->d.num_units * p->d.head_groups;
+    mla::mla_decode_attn_kernel<HG><<<grid, C::kThreads, C::kSmemBytes, stream>>>(ckv, kpe, qn, qp, prm);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+extern "C" {
+
+mla_status_t mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_last_page_len_host, int batch,
+                             int h_q, int page_size, int num_sms, mla_kv_dtype_t kv_dtype, mla_plan_t* plan_out) {
+    if (!plan_out) return MLA_ERR_INVALID_ARG;
+    mla::PlanData d;
+    const int rc = mla::build_plan(kv_indptr_host, kv_last_page_len_host, batch, h_q, page_size, num_sms,
+                                   static_cast<int>(kv_dtype), &d);
+    if (rc == 1) return MLA_ERR_INVALID_ARG;
+    if (rc == 2) return MLA_ERR_UNSUPPORTED;
+    auto* p = new (std::nothrow) mla_plan_s;
+    if (!p) return MLA_ERR_INVALID_ARG;
+    p->d = std::move(d);
+    build_image(p);
+    *plan_out = p;
+    return MLA_OK;
+}
+
+size_t mla_decode_plan_workspace_bytes(mla_plan_t plan) { return plan ? plan->d.layout.total_bytes : 0; }
+
+mla_status_t mla_decode_plan_commit(mla_plan_t plan, void* workspace_dev, size_t workspace_bytes,
+                                    void* cuda_stream) {
+    if (!plan || !workspace_dev) return MLA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(workspace_dev) & 255u) != 0) return MLA_ERR_INVALID_ARG;
+    if (workspace_bytes < plan->d.layout.total_bytes) return MLA_ERR_WORKSPACE_TOO_SMALL;
+    if (!plan->pinned) {
+        if (cudaMallocHost(&plan->pinned, plan->image.size()) != cudaSuccess) {
+            plan->pinned = nullptr;
+            return MLA_ERR_CUDA;
+        }
+        std::memcpy(plan->pinned, plan->image.data(), plan->image.size());
+    }
+    if (cudaMemcpyAsync(workspace_dev, plan->pinned, plan->image.size(), cudaMemcpyHostToDevice,
+                        static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    if (std::find(plan->committed.begin(), plan->committed.end(), workspace_dev) == plan->committed.end())
+        plan->committed.push_back(workspace_dev);
+    return MLA_OK;
+}
+
+mla_status_t mla_decode_attention(mla_plan_t plan, const void* q_nope, const void* q_pe, const void* ckv_cache,
+                                  const float* ckv_scale, const void* kpe_cache, int num_pages,
+                                  const int32_t* kv_indices, const int32_t* kv_indptr,
+                                  const int32_t* kv_last_page_len, float sm_scale, float* out, float* lse,
+                                  void* workspace_dev, void* cuda_stream) {
+    if (!plan || !q_nope || !q_pe || !ckv_cache || !kpe_cache || !kv_indices || !kv_indptr || !kv_last_page_len ||
+        !out || !lse || !workspace_dev || num_pages < 1)
+        return MLA_ERR_INVALID_ARG;
+    const auto& d = plan->d;
+    if (std::find(plan->committed.begin(), plan->committed.end(), workspace_dev) == plan->committed.end())
+        return MLA_ERR_NOT_COMMITTED;
+    if (!aligned16(q_nope) || !aligned16(q_pe) || !aligned16(ckv_cache) || !aligned16(kpe_cache) ||
+        !aligned16(out) || !aligned16(lse))
+        return MLA_ERR_INVALID_ARG;
+    if (!std::isfinite(sm_scale)) return MLA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(num_pages) * d.page_size >= (int64_t(1) << 31)) return MLA_ERR_INVALID_ARG;
+    if (d.kv_dtype == MLA_KV_FP8_E4M3) return MLA_ERR_UNSUPPORTED;
+    if (d.kv_dtype == MLA_KV_BF16 && ckv_scale != nullptr) return MLA_ERR_INVALID_ARG;
+    (void)kv_last_page_len;  // lengths are baked into the plan; kept for the ABI contract
+    if (d.segments.empty()) return MLA_OK;
+
+    cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace_dev);
+    const auto& L = d.layout;
+    CUtensorMap m_ckv, m_kpe, m_qn, m_qp;
+    const uint64_t rows = static_cast<uint64_t>(num_pages) * d.page_size;
+    const uint64_t qrows = static_cast<uint64_t>(d.batch) * d.h_q;
+    const uint32_t hg = static_cast<uint32_t>(d.heads_per_cta);
+    if (!make_map_bf16(&m_ckv, ckv_cache, mla::kDimCkv, rows, d.page_size) ||
+        !make_map_bf16(&m_kpe, kpe_cache, mla::kDimKpe, rows, d.page_size) ||
+        !make_map_bf16(&m_qn, q_nope, mla::kDimCkv, qrows, hg) || !make_map_bf16(&m_qp, q_pe, mla::kDimKpe, qrows, hg))
+        return MLA_ERR_CUDA;
+    mla::AttnParams prm;
+    prm.unit_ptr = reinterpret_cast<const int32_t*>(ws + L.off_unit_ptr);
+    prm.segments = reinterpret_cast<const mla::Segment*>(ws + L.off_segments);
+    prm.kv_indices = kv_indices;
+    prm.kv_indptr = kv_indptr;
+    prm.out = out;
+    prm.lse = lse;
+    prm.part_o = reinterpret_cast<float*>(ws + L.off_part_o);
+    prm.part_lse = reinterpret_cast<float*>(ws + L.off_part_lse);
+    prm.status = reinterpret_cast<uint32_t*>(ws + L.off_status);
+    prm.scale_log2 = sm_scale * 1.4426950408889634f;
+    prm.h_q = d.h_q;
+    prm.page_size = d.page_size;
+    prm.head_groups = d.head_groups;
+    cudaError_t e = d.heads_per_cta == 16 ? launch_attention<16>(plan, m_ckv, m_kpe, m_qn, m_qp, prm, stream)
+                                          : launch_attention<32>(plan, m_ckv, m_kpe, m_qn, m_qp, prm, stream);
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+mla_status_t mla_decode_combine(mla_plan_t plan, float* out, float* lse, void* workspace_dev, void* cuda_stream) {
+    if (!plan || !out || !lse || !workspace_dev) return MLA_ERR_INVALID_ARG;
+    if (std::find(plan->committed.begin(), plan->committed.end(), workspace_dev) == plan->committed.end())
+        return MLA_ERR_NOT_COMMITTED;
+    if (!aligned16(out) || !aligned16(lse)) return MLA_ERR_INVALID_ARG;
+    const auto& d = plan->d;
+    if (d.items.empty()) return MLA_OK;
+    const auto& L = d.layout;
+    uint8_t* ws = static_cast<uint8_t*>(workspace_dev);
+    dim3 grid(static_cast<unsigned>(d.items.size()), static_cast<unsigned>(d.h_q));
+    mla::mla_decode_combine_kernel<<<grid, 128, 0, static_cast<cudaStream_t>(cuda_stream)>>>(
+        reinterpret_cast<const mla::CombineItem*>(ws + L.off_items), reinterpret_cast<const float*>(ws + L.off_part_o),
+        reinterpret_cast<const float*>(ws + L.off_part_lse), out, lse, d.h_q);
+    return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+mla_status_t mla_decode_run(mla_plan_t plan, const void* q_nope, const void* q_pe, const void* ckv_cache,
+                            const float* ckv_scale, const void* kpe_cache, int num_pages,
+                            const int32_t* kv_indices, const int32_t* kv_indptr,
+                            const int32_t* kv_last_page_len, float sm_scale, float* out, float* lse,
+                            void* workspace_dev, void* cuda_stream) {
+    mla_status_t st = mla_decode_attention(plan, q_nope, q_pe, ckv_cache, ckv_scale, kpe_cache, num_pages, kv_indices,
+                                           kv_indptr, kv_last_page_len, sm_scale, out, lse, workspace_dev,
+                                           cuda_stream);
+    if (st != MLA_OK) return st;
+    return mla_decode_combine(plan, out, lse, workspace_dev, cuda_stream);
+}
+
+int mla_plan_num_launches(mla_plan_t plan) {
+    if (!plan) return 0;
+    return (plan->d.segments.empty() ? 0 : 1) + (plan->d.items.empty() ? 0 : 1);
+}
+
+mla_status_t mla_decode_device_status(mla_plan_t plan, void* workspace_dev, void* cuda_stream) {
+    if (!plan || !workspace_dev) return MLA_ERR_INVALID_ARG;
+    cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+    uint32_t word = 0;
+    if (cudaMemcpyAsync(&word, static_cast<uint8_t*>(workspace_dev) + plan->d.layout.off_status, sizeof word,
+                        cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return MLA_ERR_CUDA;
+    if (word == 0) return MLA_OK;
+    if (cudaMemsetAsync(static_cast<uint8_t*>(workspace_dev) + plan->d.layout.off_status, 0, sizeof word, stream) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    return MLA_ERR_DEVICE_TIMEOUT;
+}
+
+int mla_plan_num_ctas(mla_plan_t plan) { return plan ? plan->d.num_units * plan->d.head_groups : 0; }
+int mla_plan_num_segments(mla_plan_t plan) { return plan ? static_cast<int>(plan->d.segments.size()) : 0; }
+int mla_plan_num_partials(mla_plan_t plan) { return plan ? plan->d.num_partials : 0; }
+int mla_plan_heads_per_cta(mla_plan_t plan) { return plan ? plan->d.heads_per_cta : 0; }
+
+int mla_plan_get_segments(mla_plan_t plan, int32_t* segments, int32_t* unit_ptr) {
+    if (!plan) return 0;
+    const auto& d = plan->d;
+    if (segments)
+        for (size_t i = 0; i < d.segments.size(); ++i) {
+            segments[4 * i + 0] = d.segments[i].b;
+            segments[4 * i + 1] = d.segments[i].t_begin;
+            segments[4 * i + 2] = d.segments[i].t_end;
+            segments[4 * i + 3] = d.segments[i].slot;
+        }
+    if (unit_ptr) std::copy(d.unit_ptr.begin(), d.unit_ptr.end(), unit_ptr);
+    return static_cast<int>(d.segments.size());
+}
+
+void mla_plan_destroy(mla_plan_t plan) {
+    if (!plan) return;
+    if (plan->pinned) cudaFreeHost(plan->pinned);
+    delete plan;
+}
+
+const char* mla_status_string(mla_status_t status) {
+    switch (status) {
+        case MLA_OK: return "ok";
+        case MLA_ERR_INVALID_ARG: return "invalid argument";
+        case MLA_ERR_UNSUPPORTED: return "unsupported h_q, page_size or cache type";
+        case MLA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case MLA_ERR_CUDA: return "CUDA error";
+        case MLA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+        case MLA_ERR_NOT_COMMITTED: return "plan not committed to this workspace";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,133 @@
+// Balanced split-KV scheduler (host only).
+//
+// FlashMLA PR #233 lists a "balanced scheduler" and a "deterministic combine"
+// for its decode kernel without spelling out the partition; the reading used
+// here is the plainest one that balances SMs: lay every request's tokens end
+// to end in request order, cut the sequence into 128-token tiles (a request's
+// last tile may be short), and give CTA slot u the contiguous tile range
+// [floor(u*T/U), floor((u+1)*T/U)) of the T tiles, U = number of slots.  Every
+// slot therefore gets floor(T/U) or ceil(T/U) tiles.  A request whose tiles
+// land in more than one slot becomes several split pieces, each writing a
+// partial (out, lse) that the combine kernel merges in slot order.
+#include "plan.h"
+
+#include <algorithm>
+
+namespace mla {
+
+namespace {
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+}  // namespace
+
+int heads_per_cta_for(int h_q, int kv_dtype) {
+    (void)kv_dtype;
+    switch (h_q) {
+        case 16: return 16;
+        case 32:
+        case 64:
+        case 128: return 32;
+        default: return 0;
+    }
+}
+
+int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int batch, int h_q, int page_size,
+               int num_sms, int kv_dtype, PlanData* out) {
+    if (!kv_indptr || !kv_last_page_len || !out || batch < 1 || num_sms < 1) return 1;
+    if (kv_dtype != 0 && kv_dtype != 1) return 1;
+    if (page_size != 16 && page_size != 32 && page_size != 64) return 2;
+    const int hg = heads_per_cta_for(h_q, kv_dtype);
+    if (hg == 0) return 2;
+    if (kv_indptr[0] != 0) return 1;
+
+    std::vector<int64_t> len(batch), tiles(batch);
+    int64_t total_tiles = 0;
+    for (int b = 0; b < batch; ++b) {
+        int64_t n = static_cast<int64_t>(kv_indptr[b + 1]) - kv_indptr[b];
+        if (n < 0) return 1;
+        if (n > 0) {
+            int last = kv_last_page_len[b];
+            if (last < 1 || last > page_size) return 1;
+            len[b] = (n - 1) * page_size + last;
+            if (len[b] > (int64_t(1) << 30)) return 1;
+        } else {
+            len[b] = 0;
+        }
+        tiles[b] = (len[b] + kTileTokens - 1) / kTileTokens;
+        total_tiles += tiles[b];
+    }
+
+    PlanData p;
+    p.batch = batch;
+    p.h_q = h_q;
+    p.page_size = page_size;
+    p.num_sms = num_sms;
+    p.kv_dtype = kv_dtype;
+    p.heads_per_cta = hg;
+    p.head_groups = h_q / hg;
+    int64_t units = std::max(1, num_sms / p.head_groups);
+    units = std::min<int64_t>(units, std::max<int64_t>(total_tiles, 1));
+    p.num_units = static_cast<int>(units);
+
+    // unit u owns global tiles [bound(u), bound(u+1))
+    auto bound = [&](int64_t u) { return u * total_tiles / units; };
+
+    std::vector<std::vector<Segment>> per_unit(units);
+    std::vector<int> pieces(batch, 0);
+    int64_t tile_base = 0;
+    int64_t u = 0;
+    for (int b = 0; b < batch; ++b) {
+        int64_t t0 = tile_base, t1 = tile_base + tiles[b];
+        while (t0 < t1) {
+            while (bound(u + 1) <= t0) ++u;
+            int64_t end = std::min<int64_t>(t1, bound(u + 1));
+            Segment s;
+            s.b = b;
+            s.t_begin = static_cast<int32_t>((t0 - tile_base) * kTileTokens);
+            s.t_end = static_cast<int32_t>(std::min<int64_t>((end - tile_base) * kTileTokens, len[b]));
+            s.slot = -1;
+            per_unit[u].push_back(s);
+            ++pieces[b];
+            t0 = end;
+        }
+        tile_base = t1;
+    }
+
+    // partial slots: a split request's pieces get consecutive slots in token order
+    std::vector<int> slot_begin(batch, -1);
+    int next_slot = 0;
+    for (int b = 0; b < batch; ++b) {
+        if (pieces[b] > 1) {
+            slot_begin[b] = next_slot;
+            next_slot += pieces[b];
+        }
+    }
+    std::vector<int> used(batch, 0);
+    p.unit_ptr.push_back(0);
+    for (int64_t v = 0; v < units; ++v) {
+        for (Segment s : per_unit[v]) {
+            if (pieces[s.b] > 1) s.slot = slot_begin[s.b] + used[s.b]++;
+            p.segments.push_back(s);
+        }
+        p.unit_ptr.push_back(static_cast<int32_t>(p.segments.size()));
+    }
+    for (int b = 0; b < batch; ++b) {
+        if (pieces[b] > 1) p.items.push_back(CombineItem{b, slot_begin[b], pieces[b], 0});
+        else if (pieces[b] == 0) p.items.push_back(CombineItem{b, 0, 0, 0});
+    }
+    p.num_partials = next_slot;
+
+    PlanLayout& L = p.layout;
+    L.off_status = 0;
+    L.off_unit_ptr = 256;
+    L.off_segments = align_up(L.off_unit_ptr + sizeof(int32_t) * p.unit_ptr.size(), 16);
+    L.off_items = align_up(L.off_segments + sizeof(Segment) * p.segments.size(), 16);
+    L.header_bytes = align_up(L.off_items + sizeof(CombineItem) * p.items.size(), 256);
+    L.off_part_lse = L.header_bytes;
+    L.off_part_o = align_up(L.off_part_lse + sizeof(float) * size_t(p.num_partials) * h_q, 256);
+    L.total_bytes = align_up(L.off_part_o + sizeof(float) * size_t(p.num_partials) * h_q * kDimCkv, 256);
+
+    *out = std::move(p);
+    return 0;
+}
+
+}  // namespace mla

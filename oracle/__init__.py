@@ -169,3 +169,20 @@ def decode_inputs(inp, threads: int = 0, use_bf16_cache: bool = False):
     ckv = inp.ckv_bf16 if inp.ckv_scale is not None else inp.ckv
     return mla_decode(inp.q_nope, inp.q_pe, ckv, inp.kpe, inp.kv_indices, inp.kv_indptr,
                       inp.kv_last_page_len, inp.sm_scale, threads=threads)
+
+
+def decode_subset(inp, requests, threads: int = 0, use_bf16_cache: bool = False):
+    """Oracle on a subset of a ``workloads.Inputs`` batch: the same cache, with q and
+    the page table sliced to ``requests``."""
+    idx = torch.as_tensor(list(requests), dtype=torch.long)
+    indptr = inp.kv_indptr.long()
+    pieces = [inp.kv_indices[indptr[b]:indptr[b + 1]] for b in requests]
+    sub_ind = torch.cat(pieces) if pieces else inp.kv_indices[:0]
+    sub_ptr = torch.zeros(len(pieces) + 1, dtype=torch.int32)
+    if pieces:
+        sub_ptr[1:] = torch.cumsum(torch.tensor([len(p) for p in pieces]), 0).to(torch.int32)
+    ckv, scale = inp.ckv, inp.ckv_scale
+    if use_bf16_cache and inp.ckv_bf16 is not None:
+        ckv, scale = inp.ckv_bf16, None
+    return mla_decode(inp.q_nope[idx], inp.q_pe[idx], ckv, inp.kpe, sub_ind, sub_ptr, inp.kv_last_page_len[idx],
+                      inp.sm_scale, ckv_scale=scale, threads=threads)

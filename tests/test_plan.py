@@ -1,0 +1,108 @@
+"""Properties of the host split-KV plan (no GPU): every token of every request
+is covered exactly once, cuts fall on 128-token tile boundaries, work is
+balanced to within one tile per CTA slot, split pieces get consecutive
+partial slots in token order, and the plan is a deterministic function of
+its inputs."""
+import random
+
+import numpy as np
+import pytest
+import torch
+
+import mla_paged_kv_decode_gb300 as mla
+from mla_paged_kv_decode_gb300 import build as lib_build
+
+TILE = 128
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if lib_build.needs_build():
+        lib_build.build()
+    mla.load()
+
+
+def _lens_to_arrays(lens, P):
+    n = [(L + P - 1) // P for L in lens]
+    indptr = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    last = np.array([L - (k - 1) * P if k > 0 else 0 for L, k in zip(lens, n)], dtype=np.int32)
+    return indptr, last
+
+
+def _check_plan(lens, h_q, P, sms):
+    indptr, last = _lens_to_arrays(lens, P)
+    plan = mla.mla_decode_plan(torch.from_numpy(indptr), torch.from_numpy(last), len(lens), h_q, P, sms)
+    segs, uptr = mla.mla_plan_get_segments(plan)
+    hg = mla.mla_plan_heads_per_cta(plan)
+    groups = h_q // hg
+    units = len(uptr) - 1
+    assert mla.mla_plan_num_ctas(plan) == units * groups
+    assert units <= max(1, sms // groups)
+    # coverage: each request's tokens exactly once, pieces in token order
+    covered = {b: [] for b in range(len(lens))}
+    for b, t0, t1, slot in segs:
+        assert 0 <= t0 < t1 <= lens[b]
+        assert t0 % TILE == 0 and (t1 % TILE == 0 or t1 == lens[b])
+        covered[b].append((t0, t1, slot))
+    order = [int(b) for b in segs[:, 0]]
+    assert order == sorted(order), "segments follow request order"
+    n_split = 0
+    for b, L in enumerate(lens):
+        pieces = sorted(covered[b])
+        if L == 0:
+            assert pieces == []
+            continue
+        assert pieces[0][0] == 0 and pieces[-1][1] == L
+        for (a0, a1, _), (b0, b1, _) in zip(pieces, pieces[1:]):
+            assert a1 == b0
+        if len(pieces) == 1:
+            assert pieces[0][2] == -1
+        else:
+            slots = [p[2] for p in pieces]
+            assert slots == list(range(slots[0], slots[0] + len(slots)))
+            n_split += len(pieces)
+    assert mla.mla_plan_num_partials(plan) == n_split
+    # balance: tiles per unit differ by at most one
+    tiles = []
+    for u in range(units):
+        s = segs[uptr[u]:uptr[u + 1]]
+        tiles.append(sum((int(t1) - int(t0) + TILE - 1) // TILE for _, t0, t1, _ in s))
+    total = sum((L + TILE - 1) // TILE for L in lens)
+    assert sum(tiles) == total
+    if total:
+        assert max(tiles) - min(tiles) <= 1 or units == 1
+    # workspace holds every partial
+    assert plan.workspace_bytes >= n_split * h_q * (512 + 1) * 4
+    return segs, uptr
+
+
+def test_uniform_batch():
+    _check_plan([4096] * 64, 16, 64, 152)
+
+
+def test_compute_shape_groups():
+    segs, uptr = _check_plan([8192] * 128, 128, 64, 152)
+    assert len(uptr) - 1 == 152 // 4
+
+
+def test_tiny_and_edge_lengths():
+    _check_plan([1, 17, 64, 203], 16, 16, 152)
+    _check_plan([0, 5, 0, 129], 32, 32, 3)
+    _check_plan([0], 16, 16, 152)
+    _check_plan([128 * 40], 64, 64, 152)
+    _check_plan([1] * 300, 16, 16, 152)
+
+
+def test_random_plans():
+    rng = random.Random(1234)
+    for _ in range(60):
+        B = rng.randint(1, 80)
+        lens = [rng.choice([0, 1, rng.randint(1, 300), rng.randint(1, 20000)]) for _ in range(B)]
+        _check_plan(lens, rng.choice([16, 32, 64, 128]), rng.choice([16, 32, 64]), rng.choice([1, 7, 64, 152]))
+
+
+def test_plan_is_deterministic():
+    lens = [random.Random(7).randint(1, 32768) for _ in range(256)]
+    a = _check_plan(lens, 128, 16, 152)
+    b = _check_plan(lens, 128, 16, 152)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
