@@ -100,8 +100,11 @@ size_t mla_decode_plan_workspace_bytes(mla_plan_t plan);
 mla_status_t mla_decode_plan_commit(mla_plan_t plan, void* workspace_dev, size_t workspace_bytes,
                                     void* cuda_stream);
 
-/* Enqueue one decode on cuda_stream: the attention kernel, then (only if the
- * plan split a request or holds an empty one) the combine kernel.
+/* Enqueue one decode on cuda_stream: a single kernel launch.  Each CTA runs
+ * its slot of the plan; a split request's pieces write partial (out, lse) to
+ * the workspace and the CTA that finishes the request's last piece merges
+ * them in slot order (FlashMLA PR #233, "deterministic combine"), so the
+ * result does not depend on which CTA merges.
  *
  *   q_nope           device bf16 [batch, h_q, 512]
  *   q_pe             device bf16 [batch, h_q, 64]
@@ -132,20 +135,7 @@ mla_status_t mla_decode_run(mla_plan_t plan, const void* q_nope, const void* q_p
                             const int32_t* kv_last_page_len, float sm_scale, float* out, float* lse,
                             void* workspace_dev, void* cuda_stream);
 
-/* The two launches of mla_decode_run, exposed separately (same arguments,
- * same semantics when called back to back on one stream): the attention
- * kernel, which writes out/lse of unsplit requests and the partials of split
- * ones, and the combine kernel, which merges the partials in slot order and
- * fills empty requests (FlashMLA PR #233, "deterministic combine").  Either
- * is a no-op when the plan has no work for it. */
-mla_status_t mla_decode_attention(mla_plan_t plan, const void* q_nope, const void* q_pe, const void* ckv_cache,
-                                  const float* ckv_scale, const void* kpe_cache, int num_pages,
-                                  const int32_t* kv_indices, const int32_t* kv_indptr,
-                                  const int32_t* kv_last_page_len, float sm_scale, float* out, float* lse,
-                                  void* workspace_dev, void* cuda_stream);
-mla_status_t mla_decode_combine(mla_plan_t plan, float* out, float* lse, void* workspace_dev, void* cuda_stream);
-
-/* Kernel launches mla_decode_run issues for this plan (1 or 2; 0 for no work). */
+/* Kernel launches mla_decode_run issues for this plan (1, or 0 when no request has work). */
 int mla_plan_num_launches(mla_plan_t plan);
 
 /* Synchronise cuda_stream and read the workspace's status word: MLA_OK, or

@@ -31,7 +31,7 @@ EXPORTED = (
     "mla_decode_plan", "mla_decode_plan_workspace_bytes", "mla_decode_plan_commit", "mla_decode_run",
     "mla_decode_device_status", "mla_plan_num_ctas", "mla_plan_num_segments", "mla_plan_num_partials",
     "mla_plan_heads_per_cta", "mla_plan_get_segments", "mla_plan_destroy", "mla_status_string",
-    "mla_decode_attention", "mla_decode_combine", "mla_plan_num_launches",
+    "mla_plan_num_launches",
 )
 
 _lib = None
@@ -68,10 +68,6 @@ def load(path: Optional[str] = None):
     lib.mla_decode_plan_commit.argtypes = [vp, vp, sz, vp]
     lib.mla_decode_run.restype = ctypes.c_int
     lib.mla_decode_run.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_int, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp]
-    lib.mla_decode_attention.restype = ctypes.c_int
-    lib.mla_decode_attention.argtypes = lib.mla_decode_run.argtypes
-    lib.mla_decode_combine.restype = ctypes.c_int
-    lib.mla_decode_combine.argtypes = [vp, vp, vp, vp, vp]
     lib.mla_plan_num_launches.restype = ctypes.c_int
     lib.mla_plan_num_launches.argtypes = [vp]
     lib.mla_decode_device_status.restype = ctypes.c_int
@@ -158,20 +154,6 @@ def mla_decode_run(plan: Plan, q_nope, q_pe, ckv_cache, ckv_scale, kpe_cache, kv
                                  _ptr(kpe_cache), npages, _ptr(kv_indices), _ptr(kv_indptr), _ptr(kv_last_page_len),
                                  float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace), _stream(stream)),
            "mla_decode_run")
-
-
-def mla_decode_attention(plan: Plan, q_nope, q_pe, ckv_cache, ckv_scale, kpe_cache, kv_indices, kv_indptr,
-                         kv_last_page_len, sm_scale: float, out, lse, workspace, stream=None, num_pages=None):
-    npages = int(ckv_cache.shape[0]) if num_pages is None else int(num_pages)
-    _check(load().mla_decode_attention(plan.handle, _ptr(q_nope), _ptr(q_pe), _ptr(ckv_cache), _ptr(ckv_scale),
-                                       _ptr(kpe_cache), npages, _ptr(kv_indices), _ptr(kv_indptr),
-                                       _ptr(kv_last_page_len), float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace),
-                                       _stream(stream)), "mla_decode_attention")
-
-
-def mla_decode_combine(plan: Plan, out, lse, workspace, stream=None):
-    _check(load().mla_decode_combine(plan.handle, _ptr(out), _ptr(lse), _ptr(workspace), _stream(stream)),
-           "mla_decode_combine")
 
 
 def mla_plan_num_launches(plan: Plan) -> int:

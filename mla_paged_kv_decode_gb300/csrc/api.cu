@@ -13,11 +13,21 @@
 
 #include "mla_decode.h"
 #include "attn.cuh"
-#include "combine.cuh"
+#include "attn_narrow.cuh"
 #include "plan.h"
+
+// Tensor maps of the last run's buffers (re-encoded when an address changes).
+struct MapCache {
+    bool valid = false;
+    const void *ckv = nullptr, *kpe = nullptr, *qn = nullptr, *qp = nullptr;
+    int num_pages = 0;
+    CUtensorMap m_ckv, m_kpe, m_qn, m_qp;
+};
 
 struct mla_plan_s {
     mla::PlanData d;
+    MapCache maps;
+    uint64_t* trace = nullptr;    // device timeline buffer (builds with MLA_TRACE only)
     std::vector<uint8_t> image;   // header bytes copied to the workspace by commit
     void* pinned = nullptr;       // pinned staging copy of `image`
     std::vector<void*> committed; // workspaces this plan has been committed to
@@ -53,6 +63,21 @@ bool make_map_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t r
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D view of the ckv cache for the narrow kernel: dims (64 dims, rows, 8 chunks) with
+// strides (2 B, 1024 B, 128 B); a box (64, box_rows, 8) copies box_rows whole rows into
+// shared memory as [chunk][row][128 B] with the 128-byte swizzle.
+bool make_map_ckv_chunked(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {64, rows, 8};
+    cuuint64_t strides[2] = {mla::kDimCkv * 2, 128};
+    cuuint32_t box[3] = {64, box_rows, 8};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 void build_image(mla_plan_s* p) {
@@ -62,8 +87,19 @@ void build_image(mla_plan_s* p) {
     if (!p->d.segments.empty())
         std::memcpy(p->image.data() + L.off_segments, p->d.segments.data(),
                     sizeof(mla::Segment) * p->d.segments.size());
-    if (!p->d.items.empty())
-        std::memcpy(p->image.data() + L.off_items, p->d.items.data(), sizeof(mla::CombineItem) * p->d.items.size());
+}
+
+template <int HG>
+cudaError_t launch_narrow(const mla_plan_s* p, const CUtensorMap& ckv, const CUtensorMap& kpe, const mla::AttnParams& prm,
+                          const void* q_nope, const void* q_pe, cudaStream_t stream) {
+    using C = mla::NarrowCfg<HG>;
+    cudaError_t e = cudaFuncSetAttribute(mla::mla_decode_narrow_kernel<HG>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int grid = p->d.num_units * p->d.head_groups;
+    mla::mla_decode_narrow_kernel<HG><<<grid, C::kThreads, C::kSmemBytes, stream>>>(
+        ckv, kpe, prm, static_cast<const uint16_t*>(q_nope), static_cast<const uint16_t*>(q_pe));
+    return cudaGetLastError();
 }
 
 template <int HG>
@@ -74,6 +110,7 @@ cudaError_t launch_attention(const mla_plan_s* p, const CUtensorMap& ckv, const 
     cudaError_t e = cudaFuncSetAttribute(mla::mla_decode_attn_kernel<HG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
+    static_assert(sizeof(mla::AttnParams) % 8 == 0, "kernel parameter block");
     const int grid = p->d.num_units * p->d.head_groups;
     mla::mla_decode_attn_kernel<HG><<<grid, C::kThreads, C::kSmemBytes, stream>>>(ckv, kpe, qn, qp, prm);
     return cudaGetLastError();
@@ -121,11 +158,11 @@ mla_status_t mla_decode_plan_commit(mla_plan_t plan, void* workspace_dev, size_t
     return MLA_OK;
 }
 
-mla_status_t mla_decode_attention(mla_plan_t plan, const void* q_nope, const void* q_pe, const void* ckv_cache,
-                                  const float* ckv_scale, const void* kpe_cache, int num_pages,
-                                  const int32_t* kv_indices, const int32_t* kv_indptr,
-                                  const int32_t* kv_last_page_len, float sm_scale, float* out, float* lse,
-                                  void* workspace_dev, void* cuda_stream) {
+mla_status_t mla_decode_run(mla_plan_t plan, const void* q_nope, const void* q_pe, const void* ckv_cache,
+                            const float* ckv_scale, const void* kpe_cache, int num_pages,
+                            const int32_t* kv_indices, const int32_t* kv_indptr,
+                            const int32_t* kv_last_page_len, float sm_scale, float* out, float* lse,
+                            void* workspace_dev, void* cuda_stream) {
     if (!plan || !q_nope || !q_pe || !ckv_cache || !kpe_cache || !kv_indices || !kv_indptr || !kv_last_page_len ||
         !out || !lse || !workspace_dev || num_pages < 1)
         return MLA_ERR_INVALID_ARG;
@@ -145,65 +182,64 @@ mla_status_t mla_decode_attention(mla_plan_t plan, const void* q_nope, const voi
     cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace_dev);
     const auto& L = d.layout;
-    CUtensorMap m_ckv, m_kpe, m_qn, m_qp;
-    const uint64_t rows = static_cast<uint64_t>(num_pages) * d.page_size;
-    const uint64_t qrows = static_cast<uint64_t>(d.batch) * d.h_q;
-    const uint32_t hg = static_cast<uint32_t>(d.heads_per_cta);
-    if (!make_map_bf16(&m_ckv, ckv_cache, mla::kDimCkv, rows, d.page_size) ||
-        !make_map_bf16(&m_kpe, kpe_cache, mla::kDimKpe, rows, d.page_size) ||
-        !make_map_bf16(&m_qn, q_nope, mla::kDimCkv, qrows, hg) || !make_map_bf16(&m_qp, q_pe, mla::kDimKpe, qrows, hg))
-        return MLA_ERR_CUDA;
+    // tensor maps depend only on the buffer addresses: re-encode when they change
+    MapCache& mc = plan->maps;
+    if (!mc.valid || mc.ckv != ckv_cache || mc.kpe != kpe_cache || mc.qn != q_nope || mc.qp != q_pe ||
+        mc.num_pages != num_pages) {
+        const uint64_t rows = static_cast<uint64_t>(num_pages) * d.page_size;
+        const uint64_t qrows = static_cast<uint64_t>(d.batch) * d.h_q;
+        const uint32_t hg = static_cast<uint32_t>(d.heads_per_cta);
+        // box rows: a whole page for the tcgen05 kernel, a 32-token ring stage at most for the narrow one
+        const uint32_t box = d.narrow ? std::min(d.page_size, mla::kNarrowStageTok) : d.page_size;
+        // the narrow kernel takes a whole 32-token stage of ckv in one 3-D box when a page holds it
+        const bool chunked = d.narrow && box == static_cast<uint32_t>(mla::kNarrowStageTok);
+        mc.valid = (chunked ? make_map_ckv_chunked(&mc.m_ckv, ckv_cache, rows, box)
+                            : make_map_bf16(&mc.m_ckv, ckv_cache, mla::kDimCkv, rows, box)) &&
+                   make_map_bf16(&mc.m_kpe, kpe_cache, mla::kDimKpe, rows, box) &&
+                   make_map_bf16(&mc.m_qn, q_nope, mla::kDimCkv, qrows, hg) &&
+                   make_map_bf16(&mc.m_qp, q_pe, mla::kDimKpe, qrows, hg);
+        if (!mc.valid) return MLA_ERR_CUDA;
+        mc.ckv = ckv_cache;
+        mc.kpe = kpe_cache;
+        mc.qn = q_nope;
+        mc.qp = q_pe;
+        mc.num_pages = num_pages;
+    }
     mla::AttnParams prm;
     prm.unit_ptr = reinterpret_cast<const int32_t*>(ws + L.off_unit_ptr);
     prm.segments = reinterpret_cast<const mla::Segment*>(ws + L.off_segments);
     prm.kv_indices = kv_indices;
     prm.kv_indptr = kv_indptr;
+    prm.ckv = static_cast<const uint8_t*>(ckv_cache);
+    prm.kpe = static_cast<const uint8_t*>(kpe_cache);
     prm.out = out;
     prm.lse = lse;
     prm.part_o = reinterpret_cast<float*>(ws + L.off_part_o);
     prm.part_lse = reinterpret_cast<float*>(ws + L.off_part_lse);
+    prm.counters = reinterpret_cast<int32_t*>(ws + L.off_counters);
     prm.status = reinterpret_cast<uint32_t*>(ws + L.off_status);
+    prm.trace = plan->trace;
     prm.scale_log2 = sm_scale * 1.4426950408889634f;
     prm.h_q = d.h_q;
     prm.page_size = d.page_size;
     prm.head_groups = d.head_groups;
-    cudaError_t e = d.heads_per_cta == 16 ? launch_attention<16>(plan, m_ckv, m_kpe, m_qn, m_qp, prm, stream)
-                                          : launch_attention<32>(plan, m_ckv, m_kpe, m_qn, m_qp, prm, stream);
+    cudaError_t e;
+    if (d.narrow)
+        e = d.h_q == 16 ? launch_narrow<16>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream)
+                        : launch_narrow<32>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream);
+    else
+        e = launch_attention<32>(plan, mc.m_ckv, mc.m_kpe, mc.m_qn, mc.m_qp, prm, stream);
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
-mla_status_t mla_decode_combine(mla_plan_t plan, float* out, float* lse, void* workspace_dev, void* cuda_stream) {
-    if (!plan || !out || !lse || !workspace_dev) return MLA_ERR_INVALID_ARG;
-    if (std::find(plan->committed.begin(), plan->committed.end(), workspace_dev) == plan->committed.end())
-        return MLA_ERR_NOT_COMMITTED;
-    if (!aligned16(out) || !aligned16(lse)) return MLA_ERR_INVALID_ARG;
-    const auto& d = plan->d;
-    if (d.items.empty()) return MLA_OK;
-    const auto& L = d.layout;
-    uint8_t* ws = static_cast<uint8_t*>(workspace_dev);
-    dim3 grid(static_cast<unsigned>(d.items.size()), static_cast<unsigned>(d.h_q));
-    mla::mla_decode_combine_kernel<<<grid, 128, 0, static_cast<cudaStream_t>(cuda_stream)>>>(
-        reinterpret_cast<const mla::CombineItem*>(ws + L.off_items), reinterpret_cast<const float*>(ws + L.off_part_o),
-        reinterpret_cast<const float*>(ws + L.off_part_lse), out, lse, d.h_q);
-    return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+#ifdef MLA_TRACE
+// Debug builds only: device buffer of 4 * 8 * 256 uint64 timestamps filled by the next runs.
+void mla_debug_set_trace(mla_plan_t plan, void* dev_buf) {
+    if (plan) plan->trace = static_cast<uint64_t*>(dev_buf);
 }
+#endif
 
-mla_status_t mla_decode_run(mla_plan_t plan, const void* q_nope, const void* q_pe, const void* ckv_cache,
-                            const float* ckv_scale, const void* kpe_cache, int num_pages,
-                            const int32_t* kv_indices, const int32_t* kv_indptr,
-                            const int32_t* kv_last_page_len, float sm_scale, float* out, float* lse,
-                            void* workspace_dev, void* cuda_stream) {
-    mla_status_t st = mla_decode_attention(plan, q_nope, q_pe, ckv_cache, ckv_scale, kpe_cache, num_pages, kv_indices,
-                                           kv_indptr, kv_last_page_len, sm_scale, out, lse, workspace_dev,
-                                           cuda_stream);
-    if (st != MLA_OK) return st;
-    return mla_decode_combine(plan, out, lse, workspace_dev, cuda_stream);
-}
-
-int mla_plan_num_launches(mla_plan_t plan) {
-    if (!plan) return 0;
-    return (plan->d.segments.empty() ? 0 : 1) + (plan->d.items.empty() ? 0 : 1);
-}
+int mla_plan_num_launches(mla_plan_t plan) { return (plan && !plan->d.segments.empty()) ? 1 : 0; }
 
 mla_status_t mla_decode_device_status(mla_plan_t plan, void* workspace_dev, void* cuda_stream) {
     if (!plan || !workspace_dev) return MLA_ERR_INVALID_ARG;

@@ -1,0 +1,550 @@
+// MLA paged decode attention for narrow head counts (16 or 32 query heads per
+// CTA) on sm_103a: TMA page staging into an mbarrier ring, tensor-core math
+// with warp-level mma.sync (m16n8k16, bf16 in, fp32 accumulate).
+//
+// Why warp MMA here: the score contraction of a 16-head request has only 16
+// rows per query, and a tcgen05.mma costs 60-150 SM cycles per instruction
+// whatever its N (measured on GB300), so a 16-column tcgen05 tile runs at a
+// small fraction of the tensor pipe and cannot keep up with HBM.  The warp
+// MMA has no such floor: 16 heads x 1088 MACs per cached token is ~17 cycles
+// per token per SM, against the ~49 cycles per token an SM may spend at full
+// HBM bandwidth.  The wide-head path (64/128 heads) uses tcgen05 (attn.cuh).
+//
+// Absorbed MLA decode is MQA with one KV head: key [ckv | kpe] (576), value
+// ckv (512) ("Benchmarking MLA", FlashInfer issue #700).  The layout of the
+// work follows the split-K idea of FlashMLA PR #233's sm86 kernel ("Q in
+// registers, split-K QK inside the CTA, a multi-stage ... KV ring"), rebuilt
+// for TMA and the GB300 memory system:
+//
+//   * a CTA owns HG heads of every segment of its plan slot and walks it in
+//     64-token tiles; a tile is two 32-token ring stages of 36 KB (8 ckv
+//     chunks of 64 dims + kpe, 128-byte swizzle, one TMA box per page piece);
+//   * warp 0 is the TMA producer and also prefetches the pages of the tile two
+//     ahead into L2 (cp.async.bulk.prefetch), so the ring only covers L2
+//     latency;
+//   * 4 compute warps per 16-head group: warp k holds q for dims
+//     [144k, 144k + 144) in registers and computes the partial scores of all
+//     64 tokens over those dims; the 4 partials go through shared memory and
+//     every warp sums them in the same order, so all 4 hold identical scores;
+//   * each warp then runs the same online softmax (row max via quad shuffles)
+//     and keeps P in registers as the A operand of O += P V for its own 128
+//     latent dims (V loaded with ldmatrix.trans).
+//
+// The running max is updated every tile (rescaling O in registers is cheap
+// here).  A split request's pieces write normalised partials; the last CTA to
+// finish one merges them in slot order (FlashMLA PR #233, "deterministic
+// combine"), as in attn.cuh.  Every mbarrier wait is bounded.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "attn.cuh"
+#include "plan.h"
+#include "ptx.cuh"
+
+namespace mla {
+
+constexpr int kNarrowTile = 32;        // tokens per tile (= one ring stage)
+constexpr int kNarrowStageTok = 32;    // tokens per ring stage
+constexpr int kNarrowPrefetchTiles = 0; // L2 prefetch distance in tiles (0: off; the bulk prefetch shares the TMA engine with the stage loads and measured slower)
+
+template <int HG>
+struct NarrowCfg {
+    static_assert(HG == 16 || HG == 32, "heads per CTA");
+    static constexpr int kHeadGroups = HG / 16;               // 16-head groups
+    static constexpr int kTokenGroups = (HG == 16) ? 2 : 1;   // groups taking alternate tiles
+    static constexpr int kGroups = kHeadGroups * kTokenGroups; // 4-warp compute groups
+    static constexpr int kComputeWarps = 4 * kGroups;          // 8 in both cases: 2 warps per SM sub-partition
+    static constexpr int kThreads = 32 * (1 + kComputeWarps);
+    static constexpr int kChunkBytes = kNarrowStageTok * 128;  // 64 dims x 32 tokens = 4 KB
+    static constexpr int kStageBytes = 9 * kChunkBytes;        // 8 ckv chunks + kpe = 36 KB
+    static constexpr int kStages = 5;
+    static constexpr int kPartBytes = 4 * 32 * 16 * 4;         // per group: 4 warps x 32 lanes x 16 floats = 8 KB
+    static constexpr int kOffStage = 0;
+    static constexpr int kOffPart = kOffStage + kStages * kStageBytes;
+    static constexpr int kOffMisc = kOffPart + kGroups * kPartBytes;
+    static constexpr int kMiscBytes = 1024;
+    static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+    // the token-group merge passes one group's O (16 heads x 512 dims fp32) in two halves
+    // through the partial-score buffers of both groups
+    static_assert(kTokenGroups == 1 || 2 * kGroups * kPartBytes >= 16 * kDimCkv * 4, "merge buffer");
+};
+
+struct NarrowMisc {
+    uint64_t full[5], empty[5];
+    int abort_flag;
+    int merge_flag[2];
+    float mrg_max[2][16];
+    float mrg_inv[2][16];
+    float tg_m[16], tg_l[16];   // token-group merge: running max and row sum of group 1
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Address of the 16-byte unit holding (row, dims 8u..8u+7) of a 64-dim chunk stored as
+// rows of 128 bytes with the 128-byte swizzle (unit index XOR row % 8).
+__device__ __forceinline__ uint32_t sw_unit(uint32_t chunk_base, uint32_t row, uint32_t unit) {
+    return chunk_base + row * 128 + ((unit ^ (row & 7)) << 4);
+}
+
+template <int HG>
+__global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
+    mla_decode_narrow_kernel(const __grid_constant__ CUtensorMap tm_ckv, const __grid_constant__ CUtensorMap tm_kpe,
+                             const AttnParams prm, const uint16_t* __restrict__ q_nope,
+                             const uint16_t* __restrict__ q_pe) {
+    using C = NarrowCfg<HG>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* stage_base = smem + C::kOffStage;
+    float* part_base = reinterpret_cast<float*>(smem + C::kOffPart);
+    NarrowMisc* misc = reinterpret_cast<NarrowMisc*>(smem + C::kOffMisc);
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const int unit = blockIdx.x / prm.head_groups;
+    const int group_cta = blockIdx.x % prm.head_groups;
+    const int seg_begin = prm.unit_ptr[unit];
+    const int seg_end = prm.unit_ptr[unit + 1];
+    const int P = prm.page_size;
+    const int box_rows = P < kNarrowStageTok ? P : kNarrowStageTok;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::kStages; ++i) {
+            mbar_init(&misc->full[i], 1);
+            mbar_init(&misc->empty[i], 4);   // released by the 4 warps of the group that consumed it
+        }
+        misc->abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tensormap(&tm_ckv);
+            prefetch_tensormap(&tm_kpe);
+        }
+        uint32_t scount = 0, tile_idx = 0;
+        bool ok = true;
+        TileCursorT<kNarrowTile> cur;
+        bool more = cur.init(prm.segments, seg_begin, seg_end);
+        bool new_seg = true;
+        int win_base = -(1 << 30), win_page = 0;
+        const int32_t* pages = nullptr;
+        TileCursorT<kNarrowTile> pf;
+        bool pf_more = pf.init(prm.segments, seg_begin, seg_end);
+        bool pf_new = true;
+        int pf_win_base = -(1 << 30), pf_win_page = 0;
+        const int32_t* pf_pages = nullptr;
+        auto prefetch_next_tile = [&]() {
+            if (!pf_more) return;
+            if (pf_new) {
+                pf_pages = prm.kv_indices + prm.kv_indptr[pf.sg.b];
+                pf_win_base = -(1 << 30);
+            }
+            const int fp = pf.t0 / P;
+            const int np = (pf.ntok() + P - 1) / P;
+            if (fp + np > pf_win_base + 32) {
+                const int last_page = (pf.sg.t_end - 1) / P;
+                pf_win_base = fp;
+                pf_win_page = (pf_win_base + lane <= last_page) ? pf_pages[pf_win_base + lane] : 0;
+            }
+            const int pg = __shfl_sync(0xffffffffu, pf_win_page, (fp - pf_win_base + lane) & 31);
+            if (lane < np) {
+                // whole pages: a tile's pages may extend past it; prefetching them early is harmless
+                l2_prefetch(prm.ckv + static_cast<size_t>(pg) * P * (kDimCkv * 2), static_cast<uint32_t>(P * kDimCkv * 2));
+                l2_prefetch(prm.kpe + static_cast<size_t>(pg) * P * (kDimKpe * 2), static_cast<uint32_t>(P * kDimKpe * 2));
+            }
+            pf_more = pf.advance(pf_new);
+        };
+        for (int d = 0; d < kNarrowPrefetchTiles; ++d) prefetch_next_tile();
+        while (more && ok) {
+            if (kNarrowPrefetchTiles > 0) prefetch_next_tile();
+            if (new_seg) {
+                pages = prm.kv_indices + prm.kv_indptr[cur.sg.b];
+                win_base = -(1 << 30);
+            }
+            const int ntok = cur.ntok();
+            const int nst = (ntok + kNarrowStageTok - 1) / kNarrowStageTok;
+            for (int st = 0; st < nst && ok; ++st) {
+                const int t_st = cur.t0 + st * kNarrowStageTok;                   // first token of the stage
+                const int n_st = min(kNarrowStageTok, cur.sg.t_end - t_st);        // tokens in the stage
+                const int nbox = (n_st + box_rows - 1) / box_rows;
+                const int first_page = t_st / P;
+                const int last_page_st = (t_st + nbox * box_rows - 1) / P;
+                if (last_page_st + 1 > win_base + 32 || first_page < win_base) {
+                    const int seg_last_page = (cur.sg.t_end - 1) / P;
+                    win_base = first_page;
+                    win_page = (win_base + lane <= seg_last_page) ? pages[win_base + lane] : 0;
+                }
+                const uint32_t s = scount % C::kStages, use = scount / C::kStages;
+                if (lane == 0 && use > 0) ok = wait_phase_flag(&misc->empty[s], (use - 1) & 1, &misc->abort_flag, prm.status, 21);
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                if (!ok) break;
+                uint8_t* dst = stage_base + s * C::kStageBytes;
+                if (lane == 0) mbar_arrive_expect_tx(&misc->full[s], static_cast<uint32_t>(nbox * box_rows * 128 * 9));
+                if (lane == 0) MLA_TRACE_EVENT(st == 0 ? 0 : 1, tile_idx);
+                for (int bx = 0; bx < nbox; ++bx) {
+                    const int t = t_st + bx * box_rows;
+                    const int pg = __shfl_sync(0xffffffffu, win_page, (t / P - win_base) & 31);
+                    if (lane == 0) {
+                        const int y = pg * P + (t % P);
+                        if (box_rows == kNarrowStageTok) {
+                            // all 8 ckv chunks in one 3-D box (64 dims, 32 rows, 8 chunks), which lands as
+                            // [chunk][row][128 B] -- the stage layout the ldmatrix addressing expects
+                            tma_load_3d(dst, &tm_ckv, &misc->full[s], 0, y, 0);
+                        } else {
+                            for (int c = 0; c < 8; ++c)
+                                tma_load_2d(dst + c * C::kChunkBytes + bx * box_rows * 128, &tm_ckv, &misc->full[s],
+                                            c * 64, y);
+                        }
+                        tma_load_2d(dst + 8 * C::kChunkBytes + bx * box_rows * 128, &tm_kpe, &misc->full[s], 0, y);
+                    }
+                }
+                ++scount;
+            }
+            ++tile_idx;
+            more = cur.advance(new_seg);
+        }
+        if (lane == 0) {
+            const uint64_t t0 = global_timer_ns();
+            for (int s = 0; s < C::kStages; ++s) {
+                const uint32_t uses = scount / C::kStages + (static_cast<uint32_t>(s) < scount % C::kStages ? 1 : 0);
+                if (uses == 0) continue;
+                while (!mbar_try_wait(&misc->full[s], (uses - 1) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {}
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ compute warps
+        const int cw = warp - 1;                 // 0 .. kComputeWarps-1
+        const int grp = cw / 4;                  // compute group (4 warps)
+        const int hgi = grp / C::kTokenGroups;   // 16-head group within the CTA
+        const int tg = grp % C::kTokenGroups;    // token group: takes tiles t with t % kTokenGroups == tg
+        const int kr = cw % 4;                   // score split: dims [144 kr, 144 kr + 144); PV: dims [128 kr, +128)
+        const int g = lane >> 2, c4 = lane & 3;  // mma fragment row group / column pair
+        const uint32_t named_bar = 1 + grp;      // 4-warp group barrier
+        const uint32_t merge_bar = 1 + C::kGroups + hgi;   // both token groups of a head group
+        const int head0 = group_cta * HG + hgi * 16;   // first head of this warp's group
+        const uint32_t stage0 = smem_u32(stage_base);
+        float* part = part_base + grp * (C::kPartBytes / 4);
+        uint32_t scount = 0;     // ring stages consumed so far by the CTA (both token groups)
+        bool ok = true;
+        for (int si = seg_begin; si < seg_end && ok; ++si) {
+            const Segment sg = prm.segments[si];
+            if (sg.t_end <= sg.t_begin) {
+                if (tg == 0) {
+                    float* o = prm.out + (static_cast<size_t>(sg.b) * prm.h_q + head0) * kDimCkv;
+                    for (int i = kr * 32 + lane; i < 16 * kDimCkv; i += 128) o[i] = 0.f;
+                    if (kr == 0 && lane < 16) prm.lse[static_cast<size_t>(sg.b) * prm.h_q + head0 + lane] = -INFINITY;
+                }
+                continue;
+            }
+            // ---- q fragments for dims [144 kr, 144 kr + 144): 9 k-steps of 16 (dims >= 512 are q_pe)
+            uint32_t qa[9][4];
+            {
+                const size_t qrow0 = static_cast<size_t>(sg.b) * prm.h_q + head0;
+#pragma unroll
+                for (int ks = 0; ks < 9; ++ks) {
+                    const int kd = kr * 144 + ks * 16;
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int row = g + ((r & 1) ? 8 : 0);
+                        const int dim = kd + 2 * c4 + ((r & 2) ? 8 : 0);
+                        const uint16_t* src = dim < kDimCkv ? q_nope + (qrow0 + row) * kDimCkv + dim
+                                                            : q_pe + (qrow0 + row) * kDimKpe + (dim - kDimCkv);
+                        qa[ks][r] = *reinterpret_cast<const uint32_t*>(src);
+                    }
+                }
+            }
+            float o[16][4];
+#pragma unroll
+            for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+            float m_run[2] = {-INFINITY, -INFINITY};   // rows g and g + 8 (log2 domain)
+            float l_part[2] = {0.f, 0.f};
+            int tile_in_seg = 0;
+            for (int t0 = sg.t_begin; t0 < sg.t_end; t0 += kNarrowTile, ++tile_in_seg) {
+                const int ntok = min(kNarrowTile, sg.t_end - t0);
+                if (tile_in_seg % C::kTokenGroups != tg) {   // the other token group's tile
+                    ++scount;
+                    continue;
+                }
+                const uint32_t sl = scount % C::kStages;
+                ok = wait_phase_flag(&misc->full[sl], (scount / C::kStages) & 1, &misc->abort_flag, prm.status, 22);
+                const uint32_t st_addr = stage0 + sl * C::kStageBytes;
+                ok = !named_barrier_or(named_bar, 128, !ok || *reinterpret_cast<volatile int*>(&misc->abort_flag));
+                if (!ok) break;
+                if (cw == 0 && lane == 0) MLA_TRACE_EVENT(2, (uint32_t)tile_in_seg);
+                // ---- partial scores over this warp's 144 dims for the 4 n8 token tiles
+                float sc[4][4];
+#pragma unroll
+                for (int n = 0; n < 4; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+#pragma unroll
+                for (int ks = 0; ks < 9; ++ks) {
+                    const int kd = kr * 144 + ks * 16;
+                    const int chunk = kd >> 6;                 // 0..7 ckv, 8 kpe
+                    const int unit0 = (kd & 63) >> 3;          // 16-byte unit of the k-step's first 8 dims
+                    uint32_t bf[2][4];
+#pragma unroll
+                    for (int np = 0; np < 2; ++np) {           // pairs of n8 tiles = 16 tokens
+                        const int tok = np * 16 + (lane & 7) + ((lane & 16) ? 8 : 0);
+                        ldsm_x4(sw_unit(st_addr + chunk * C::kChunkBytes, tok, unit0 + ((lane & 8) ? 1 : 0)),
+                                bf[np][0], bf[np][1], bf[np][2], bf[np][3]);
+                    }
+#pragma unroll
+                    for (int np = 0; np < 2; ++np) {
+                        if (np * 16 < ntok) {
+                            mma_bf16_16816(sc[2 * np], qa[ks], bf[np][0], bf[np][1]);
+                            mma_bf16_16816(sc[2 * np + 1], qa[ks], bf[np][2], bf[np][3]);
+                        }
+                    }
+                }
+                // ---- exchange partials within the group, sum in fixed warp order
+                {
+                    float4* dst = reinterpret_cast<float4*>(part) + kr * 4 * 32;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) dst[i * 32 + lane] = make_float4(sc[i][0], sc[i][1], sc[i][2], sc[i][3]);
+                }
+                // zero the value rows of a partial 16-token step (stale or NaN bytes past the last token)
+                if (ntok < kNarrowTile && (ntok & 15)) {
+                    const int r_end = (ntok + 15) & ~15;
+                    for (int tok = ntok + kr; tok < r_end; tok += 4) {
+                        uint4* rowp = reinterpret_cast<uint4*>(stage_base + (st_addr - stage0) + tok * 128);
+                        for (int c = 0; c < 8; ++c) rowp[c * (C::kChunkBytes / 16) + (lane & 7)] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                named_barrier_sync(named_bar, 128);
+                if (cw == 0 && lane == 0) MLA_TRACE_EVENT(3, (uint32_t)tile_in_seg);
+                {
+                    const float4* src = reinterpret_cast<const float4*>(part);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float4 a0 = src[(0 * 4 + i) * 32 + lane], a1 = src[(1 * 4 + i) * 32 + lane];
+                        const float4 a2 = src[(2 * 4 + i) * 32 + lane], a3 = src[(3 * 4 + i) * 32 + lane];
+                        sc[i][0] = ((a0.x + a1.x) + a2.x) + a3.x;
+                        sc[i][1] = ((a0.y + a1.y) + a2.y) + a3.y;
+                        sc[i][2] = ((a0.z + a1.z) + a2.z) + a3.z;
+                        sc[i][3] = ((a0.w + a1.w) + a2.w) + a3.w;
+                    }
+                }
+                // the partial buffer is rewritten by the group's next tile only after every warp has read it
+                named_barrier_sync(named_bar, 128);
+                // ---- online softmax, rows g and g + 8 (log2 domain), masked past the last token
+                float mt[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+                for (int n = 0; n < 4; ++n)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int tok = n * 8 + 2 * c4 + (e & 1);
+                        const float v = tok < ntok ? sc[n][e] * prm.scale_log2 : -INFINITY;
+                        sc[n][e] = v;
+                        mt[e >> 1] = fmaxf(mt[e >> 1], v);
+                    }
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    mt[r] = fmaxf(mt[r], __shfl_xor_sync(0xffffffffu, mt[r], 1));
+                    mt[r] = fmaxf(mt[r], __shfl_xor_sync(0xffffffffu, mt[r], 2));
+                }
+                float alpha[2];
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const float mn = fmaxf(m_run[r], mt[r]);
+                    alpha[r] = exp2f(m_run[r] - mn);
+                    m_run[r] = mn;
+                    l_part[r] *= alpha[r];
+                }
+#pragma unroll
+                for (int n = 0; n < 16; ++n) {
+                    o[n][0] *= alpha[0];
+                    o[n][1] *= alpha[0];
+                    o[n][2] *= alpha[1];
+                    o[n][3] *= alpha[1];
+                }
+                uint32_t pa[2][4];   // P as the A operand of the 2 k16 token steps
+#pragma unroll
+                for (int n = 0; n < 4; ++n) {
+                    const float p0 = exp2f(sc[n][0] - m_run[0]), p1 = exp2f(sc[n][1] - m_run[0]);
+                    const float p2 = exp2f(sc[n][2] - m_run[1]), p3 = exp2f(sc[n][3] - m_run[1]);
+                    l_part[0] += p0 + p1;
+                    l_part[1] += p2 + p3;
+                    pa[n >> 1][(n & 1) * 2 + 0] = pack_bf16(p0, p1);
+                    pa[n >> 1][(n & 1) * 2 + 1] = pack_bf16(p2, p3);
+                }
+                if (cw == 0 && lane == 0) MLA_TRACE_EVENT(4, (uint32_t)tile_in_seg);
+                // ---- O[16 x 128 dims of this warp] += P V
+#pragma unroll
+                for (int kt = 0; kt < 2; ++kt) {
+                    if (kt * 16 >= ntok) break;
+                    const int tok = kt * 16 + (lane & 7) + ((lane & 8) ? 8 : 0);
+                    uint32_t vf[8][4];
+#pragma unroll
+                    for (int dp = 0; dp < 8; ++dp) {          // pairs of n8 dim tiles = 16 dims
+                        const int d0 = kr * 128 + dp * 16;
+                        const int unit = ((d0 & 63) >> 3) + ((lane & 16) ? 1 : 0);
+                        ldsm_x4_t(sw_unit(st_addr + (d0 >> 6) * C::kChunkBytes, tok, unit), vf[dp][0], vf[dp][1],
+                                  vf[dp][2], vf[dp][3]);
+                    }
+#pragma unroll
+                    for (int dp = 0; dp < 8; ++dp) {
+                        mma_bf16_16816(o[2 * dp], pa[kt], vf[dp][0], vf[dp][1]);
+                        mma_bf16_16816(o[2 * dp + 1], pa[kt], vf[dp][2], vf[dp][3]);
+                    }
+                }
+                __syncwarp();
+                if (cw == 0 && lane == 0) MLA_TRACE_EVENT(5, (uint32_t)tile_in_seg);
+                if (lane == 0) mbar_arrive(&misc->empty[sl]);
+                ++scount;
+            }
+            if (!ok) break;
+            // ---- row sums over the quad (every warp of the group holds identical m and l)
+            float l[2];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                l[r] = l_part[r];
+                l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
+                l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
+            }
+            if (C::kTokenGroups == 2) {
+                // ---- merge the two token groups: group 1 passes (O, m, l) to group 0 through shared
+                // memory (the partial-score buffers of both groups, two halves of O), group 0 combines
+                float4* xo = reinterpret_cast<float4*>(part_base + (hgi * C::kTokenGroups) * (C::kPartBytes / 4));
+                named_barrier_sync(merge_bar, 256);
+                if (tg == 1 && kr == 0 && c4 == 0) {
+                    misc->tg_m[g] = m_run[0];
+                    misc->tg_m[g + 8] = m_run[1];
+                    misc->tg_l[g] = l[0];
+                    misc->tg_l[g + 8] = l[1];
+                }
+                float w0[2] = {1.f, 1.f}, w1[2] = {0.f, 0.f};
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    if (tg == 1) {
+#pragma unroll
+                        for (int n = 0; n < 8; ++n)
+                            xo[(kr * 8 + n) * 32 + lane] =
+                                make_float4(o[half * 8 + n][0], o[half * 8 + n][1], o[half * 8 + n][2], o[half * 8 + n][3]);
+                    }
+                    named_barrier_sync(merge_bar, 256);
+                    if (tg == 0) {
+                        if (half == 0) {
+                            const float m1[2] = {misc->tg_m[g], misc->tg_m[g + 8]};
+                            const float l1[2] = {misc->tg_l[g], misc->tg_l[g + 8]};
+#pragma unroll
+                            for (int r = 0; r < 2; ++r) {
+                                const float mm = fmaxf(m_run[r], m1[r]);
+                                w0[r] = exp2f(m_run[r] - mm);
+                                w1[r] = (m1[r] == -INFINITY) ? 0.f : exp2f(m1[r] - mm);
+                                m_run[r] = mm;
+                                l[r] = l[r] * w0[r] + l1[r] * w1[r];
+                            }
+                        }
+#pragma unroll
+                        for (int n = 0; n < 8; ++n) {
+                            const float4 v = xo[(kr * 8 + n) * 32 + lane];
+                            float* on = o[half * 8 + n];
+                            on[0] = on[0] * w0[0] + v.x * w1[0];
+                            on[1] = on[1] * w0[0] + v.y * w1[0];
+                            on[2] = on[2] * w0[1] + v.z * w1[1];
+                            on[3] = on[3] * w0[1] + v.w * w1[1];
+                        }
+                    }
+                    named_barrier_sync(merge_bar, 256);   // the buffer is rewritten next
+                }
+                if (tg == 1) continue;
+            }
+            // ---- epilogue (token group 0): normalise and store this warp's 128 dims
+            const float inv0 = 1.f / l[0], inv1 = 1.f / l[1];
+            float* obase;
+            float* lbase;
+            if (sg.slot < 0) {
+                obase = prm.out + (static_cast<size_t>(sg.b) * prm.h_q + head0) * kDimCkv;
+                lbase = prm.lse + static_cast<size_t>(sg.b) * prm.h_q + head0;
+            } else {
+                obase = prm.part_o + (static_cast<size_t>(sg.slot) * prm.h_q + head0) * kDimCkv;
+                lbase = prm.part_lse + static_cast<size_t>(sg.slot) * prm.h_q + head0;
+            }
+#pragma unroll
+            for (int n = 0; n < 16; ++n) {
+                const int d = kr * 128 + n * 8 + 2 * c4;
+                *reinterpret_cast<float2*>(obase + static_cast<size_t>(g) * kDimCkv + d) =
+                    make_float2(o[n][0] * inv0, o[n][1] * inv0);
+                *reinterpret_cast<float2*>(obase + static_cast<size_t>(g + 8) * kDimCkv + d) =
+                    make_float2(o[n][2] * inv1, o[n][3] * inv1);
+            }
+            if (kr == 0 && c4 == 0) {
+                lbase[g] = (m_run[0] + log2f(l[0])) * 0.69314718055994530942f;
+                lbase[g + 8] = (m_run[1] + log2f(l[1])) * 0.69314718055994530942f;
+            }
+            if (sg.slot >= 0) {
+                // ---- split request: the last piece to arrive merges all of them in slot order
+                __threadfence();
+                named_barrier_sync(named_bar, 128);
+                const int gt = kr * 32 + lane;   // 0..127 within the group
+                const int ctr = (sg.item * prm.head_groups + group_cta) * C::kHeadGroups + hgi;
+                if (gt == 0) {
+                    const int old = atomicAdd(&prm.counters[ctr], 1);
+                    misc->merge_flag[hgi] = (old == sg.n_slots - 1);
+                }
+                named_barrier_sync(named_bar, 128);
+                if (misc->merge_flag[hgi]) {
+                    __threadfence();
+                    if (gt < 16) {
+                        float M = -INFINITY;
+                        for (int i = 0; i < sg.n_slots; ++i)
+                            M = fmaxf(M, __ldcg(prm.part_lse + static_cast<size_t>(sg.slot_begin + i) * prm.h_q + head0 + gt));
+                        float ws = 0.f;
+                        for (int i = 0; i < sg.n_slots; ++i)
+                            ws += expf(__ldcg(prm.part_lse + static_cast<size_t>(sg.slot_begin + i) * prm.h_q + head0 + gt) - M);
+                        misc->mrg_max[hgi][gt] = M;
+                        misc->mrg_inv[hgi][gt] = 1.f / ws;
+                        prm.lse[static_cast<size_t>(sg.b) * prm.h_q + head0 + gt] = M + logf(ws);
+                    }
+                    named_barrier_sync(named_bar, 128);
+                    float* out_b = prm.out + (static_cast<size_t>(sg.b) * prm.h_q + head0) * kDimCkv;
+                    for (int h = 0; h < 16; ++h) {
+                        const float M = misc->mrg_max[hgi][h], inv = misc->mrg_inv[hgi][h];
+                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                        for (int i = 0; i < sg.n_slots; ++i) {
+                            const size_t s = static_cast<size_t>(sg.slot_begin + i) * prm.h_q + head0 + h;
+                            const float w = expf(__ldcg(prm.part_lse + s) - M);
+                            const float* op = prm.part_o + s * kDimCkv + gt;
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) acc[c] = fmaf(w, __ldcg(op + c * 128), acc[c]);
+                        }
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) out_b[static_cast<size_t>(h) * kDimCkv + c * 128 + gt] = acc[c] * inv;
+                    }
+                    if (gt == 0) prm.counters[ctr] = 0;
+                }
+                named_barrier_sync(named_bar, 128);
+            }
+        }
+    }
+    __syncthreads();
+}
+
+}  // namespace mla

@@ -3,12 +3,14 @@
 // FlashMLA PR #233 lists a "balanced scheduler" and a "deterministic combine"
 // for its decode kernel without spelling out the partition; the reading used
 // here is the plainest one that balances SMs: lay every request's tokens end
-// to end in request order, cut the sequence into 128-token tiles (a request's
+// to end in request order, cut the sequence into tiles of the kernel's tile size
+// (32 tokens for 16/32 heads, 128 for 64/128 heads; a request's
 // last tile may be short), and give CTA slot u the contiguous tile range
 // [floor(u*T/U), floor((u+1)*T/U)) of the T tiles, U = number of slots.  Every
 // slot therefore gets floor(T/U) or ceil(T/U) tiles.  A request whose tiles
 // land in more than one slot becomes several split pieces, each writing a
-// partial (out, lse) that the combine kernel merges in slot order.
+// partial (out, lse); the CTA finishing the last piece merges them in slot
+// order.
 #include "plan.h"
 
 #include <algorithm>
@@ -23,7 +25,7 @@ int heads_per_cta_for(int h_q, int kv_dtype) {
     (void)kv_dtype;
     switch (h_q) {
         case 16: return 16;
-        case 32:
+        case 32: return 32;
         case 64:
         case 128: return 32;
         default: return 0;
@@ -39,6 +41,8 @@ int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int ba
     if (hg == 0) return 2;
     if (kv_indptr[0] != 0) return 1;
 
+    const bool narrow = h_q <= 32;
+    const int tile_tok = narrow ? kNarrowTileTokens : kTileTokens;
     std::vector<int64_t> len(batch), tiles(batch);
     int64_t total_tiles = 0;
     for (int b = 0; b < batch; ++b) {
@@ -52,7 +56,7 @@ int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int ba
         } else {
             len[b] = 0;
         }
-        tiles[b] = (len[b] + kTileTokens - 1) / kTileTokens;
+        tiles[b] = (len[b] + tile_tok - 1) / tile_tok;
         total_tiles += tiles[b];
     }
 
@@ -64,6 +68,8 @@ int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int ba
     p.kv_dtype = kv_dtype;
     p.heads_per_cta = hg;
     p.head_groups = h_q / hg;
+    p.tile_tokens = tile_tok;
+    p.narrow = narrow;
     int64_t units = std::max(1, num_sms / p.head_groups);
     units = std::min<int64_t>(units, std::max<int64_t>(total_tiles, 1));
     p.num_units = static_cast<int>(units);
@@ -80,11 +86,12 @@ int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int ba
         while (t0 < t1) {
             while (bound(u + 1) <= t0) ++u;
             int64_t end = std::min<int64_t>(t1, bound(u + 1));
-            Segment s;
+            Segment s{};
             s.b = b;
-            s.t_begin = static_cast<int32_t>((t0 - tile_base) * kTileTokens);
-            s.t_end = static_cast<int32_t>(std::min<int64_t>((end - tile_base) * kTileTokens, len[b]));
+            s.t_begin = static_cast<int32_t>((t0 - tile_base) * tile_tok);
+            s.t_end = static_cast<int32_t>(std::min<int64_t>((end - tile_base) * tile_tok, len[b]));
             s.slot = -1;
+            s.item = -1;
             per_unit[u].push_back(s);
             ++pieces[b];
             t0 = end;
@@ -101,27 +108,41 @@ int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int ba
             next_slot += pieces[b];
         }
     }
+    // split requests get an arrival counter each; empty requests become zero-length
+    // segments spread round-robin over the units (their CTA writes out = 0, lse = -inf)
+    std::vector<int> item_of(batch, -1);
+    int next_item = 0;
+    for (int b = 0; b < batch; ++b)
+        if (pieces[b] > 1) item_of[b] = next_item++;
+    int rr = 0;
+    for (int b = 0; b < batch; ++b)
+        if (pieces[b] == 0) {
+            per_unit[rr % units].push_back(Segment{b, 0, 0, -1, -1, 0, 0, 0});
+            ++rr;
+        }
     std::vector<int> used(batch, 0);
     p.unit_ptr.push_back(0);
     for (int64_t v = 0; v < units; ++v) {
         for (Segment s : per_unit[v]) {
-            if (pieces[s.b] > 1) s.slot = slot_begin[s.b] + used[s.b]++;
+            if (pieces[s.b] > 1) {
+                s.slot = slot_begin[s.b] + used[s.b]++;
+                s.item = item_of[s.b];
+                s.slot_begin = slot_begin[s.b];
+                s.n_slots = pieces[s.b];
+            }
             p.segments.push_back(s);
         }
         p.unit_ptr.push_back(static_cast<int32_t>(p.segments.size()));
     }
-    for (int b = 0; b < batch; ++b) {
-        if (pieces[b] > 1) p.items.push_back(CombineItem{b, slot_begin[b], pieces[b], 0});
-        else if (pieces[b] == 0) p.items.push_back(CombineItem{b, 0, 0, 0});
-    }
     p.num_partials = next_slot;
+    p.num_split = next_item;
 
     PlanLayout& L = p.layout;
     L.off_status = 0;
     L.off_unit_ptr = 256;
     L.off_segments = align_up(L.off_unit_ptr + sizeof(int32_t) * p.unit_ptr.size(), 16);
-    L.off_items = align_up(L.off_segments + sizeof(Segment) * p.segments.size(), 16);
-    L.header_bytes = align_up(L.off_items + sizeof(CombineItem) * p.items.size(), 256);
+    L.off_counters = align_up(L.off_segments + sizeof(Segment) * p.segments.size(), 16);
+    L.header_bytes = align_up(L.off_counters + sizeof(int32_t) * size_t(p.num_split) * (h_q / 16), 256);
     L.off_part_lse = L.header_bytes;
     L.off_part_o = align_up(L.off_part_lse + sizeof(float) * size_t(p.num_partials) * h_q, 256);
     L.total_bytes = align_up(L.off_part_o + sizeof(float) * size_t(p.num_partials) * h_q * kDimCkv, 256);

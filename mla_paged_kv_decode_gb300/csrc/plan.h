@@ -8,28 +8,27 @@
 
 namespace mla {
 
-constexpr int kTileTokens = 128;   // tokens per attention tile (UMMA M of the score MMA)
+constexpr int kTileTokens = 128;   // tokens per tile of the wide-head (tcgen05) kernel
+constexpr int kNarrowTileTokens = 32;  // tokens per tile of the narrow-head (warp MMA) kernel
 constexpr int kDimCkv = 512;
 constexpr int kDimKpe = 64;
 
 // One (request, token range) piece of work.  slot < 0: the piece is the whole
-// request and the kernel writes out/lse directly; otherwise it writes the
-// partial (out, lse) to partial slot `slot`.
+// request and the kernel writes out/lse directly (t_begin == t_end == 0 for a
+// request with no tokens: out = 0, lse = -inf); otherwise it writes the
+// partial (out, lse) to partial slot `slot`, and the CTA that finishes the
+// request's last piece merges slots [slot_begin, slot_begin + n_slots) using
+// the arrival counter `item`.
 struct Segment {
     int32_t b, t_begin, t_end, slot;
-};
-
-// One request the combine kernel finalises: merges partial slots
-// [slot_begin, slot_begin + n_slots), or zero-fills when n_slots == 0.
-struct CombineItem {
-    int32_t b, slot_begin, n_slots, pad;
+    int32_t item, slot_begin, n_slots, pad;
 };
 
 struct PlanLayout {
     size_t off_status = 0;      // uint32 status word
     size_t off_unit_ptr = 0;    // int32 [num_units + 1]
     size_t off_segments = 0;    // Segment [num_segments]
-    size_t off_items = 0;       // CombineItem [num_items]
+    size_t off_counters = 0;    // int32 [num_split_requests * h_q / 16], zero between runs
     size_t header_bytes = 0;    // bytes copied by commit
     size_t off_part_lse = 0;    // fp32 [num_partials, h_q]
     size_t off_part_o = 0;      // fp32 [num_partials, h_q, 512]
@@ -39,10 +38,12 @@ struct PlanLayout {
 struct PlanData {
     int batch = 0, h_q = 0, page_size = 0, num_sms = 0, kv_dtype = 0;
     int heads_per_cta = 0, head_groups = 0, num_units = 0;
+    int tile_tokens = 0;              // plan granularity = the kernel's tile
+    bool narrow = false;              // h_q <= 32: warp-MMA kernel, else tcgen05 kernel
     std::vector<int32_t> unit_ptr;
     std::vector<Segment> segments;
-    std::vector<CombineItem> items;
     int num_partials = 0;
+    int num_split = 0;                // requests cut into several pieces
     PlanLayout layout;
 };
 
@@ -50,7 +51,8 @@ struct PlanData {
 int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int batch, int h_q, int page_size,
                int num_sms, int kv_dtype, PlanData* out);
 
-// Heads handled by one CTA for a given h_q (0 if unsupported).
+// Heads handled by one CTA for a given h_q (0 if unsupported): all of them for the
+// narrow-head kernel (h_q <= 32), 32-head groups for the tcgen05 kernel.
 int heads_per_cta_for(int h_q, int kv_dtype);
 
 }  // namespace mla

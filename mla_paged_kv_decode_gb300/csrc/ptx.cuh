@@ -76,6 +76,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking probe of a phase (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // ------------------------------------------------------------------ TMA
 
 // 2-D tiled tensor load into shared memory, completion counted in bytes on `bar`.
@@ -89,6 +102,16 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
+// 3-D tiled tensor load (x innermost).
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int32_t x, int32_t y,
+                                            int32_t z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::
+            "r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
 // Plain bulk copy global -> shared (both addresses 16-byte aligned, bytes % 16 == 0).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile(
@@ -96,6 +119,12 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
             smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
+}
+
+// Bulk prefetch of a global range into L2 (no shared memory, no completion tracking).
+__device__ __forceinline__ void l2_prefetch(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+                 : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
@@ -193,6 +222,17 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo
     d |= static_cast<uint64_t>(1) << 46;  // descriptor version for tcgen05
     d |= static_cast<uint64_t>(2) << 61;  // SWIZZLE_128B
     return d;
+}
+
+// Same descriptor with compile-time strides; the start address (bits 0..13) can then be
+// advanced by adding (byte offset >> 4), which never carries out of the 14-bit field
+// because shared-memory addresses stay below 256 KB.
+template <uint32_t LBO, uint32_t SBO>
+__device__ __forceinline__ uint64_t umma_desc_sw128_c(uint32_t saddr) {
+    constexpr uint64_t hi = (static_cast<uint64_t>((LBO >> 4) & 0x3FFFu) << 16) |
+                            (static_cast<uint64_t>((SBO >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46) |
+                            (static_cast<uint64_t>(2) << 61);
+    return hi | static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
 }
 
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulation.

@@ -12,7 +12,6 @@ import torch
 import mla_paged_kv_decode_gb300 as mla
 from mla_paged_kv_decode_gb300 import build as lib_build
 
-TILE = 128
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -30,6 +29,7 @@ def _lens_to_arrays(lens, P):
 
 
 def _check_plan(lens, h_q, P, sms):
+    TILE = 32 if h_q <= 32 else 128          # the kernel's tile: narrow (warp MMA) or tcgen05
     indptr, last = _lens_to_arrays(lens, P)
     plan = mla.mla_decode_plan(torch.from_numpy(indptr), torch.from_numpy(last), len(lens), h_q, P, sms)
     segs, uptr = mla.mla_plan_get_segments(plan)
@@ -40,11 +40,17 @@ def _check_plan(lens, h_q, P, sms):
     assert units <= max(1, sms // groups)
     # coverage: each request's tokens exactly once, pieces in token order
     covered = {b: [] for b in range(len(lens))}
+    empties = []
     for b, t0, t1, slot in segs:
+        if lens[b] == 0:
+            assert t0 == 0 and t1 == 0 and slot == -1   # zero-length segment: write out = 0, lse = -inf
+            empties.append(int(b))
+            continue
         assert 0 <= t0 < t1 <= lens[b]
         assert t0 % TILE == 0 and (t1 % TILE == 0 or t1 == lens[b])
         covered[b].append((t0, t1, slot))
-    order = [int(b) for b in segs[:, 0]]
+    assert sorted(empties) == [b for b, L in enumerate(lens) if L == 0], "each empty request exactly once"
+    order = [int(b) for b, t0, t1, _ in segs if t1 > t0]
     assert order == sorted(order), "segments follow request order"
     n_split = 0
     for b, L in enumerate(lens):
@@ -66,7 +72,7 @@ def _check_plan(lens, h_q, P, sms):
     tiles = []
     for u in range(units):
         s = segs[uptr[u]:uptr[u + 1]]
-        tiles.append(sum((int(t1) - int(t0) + TILE - 1) // TILE for _, t0, t1, _ in s))
+        tiles.append(sum((int(t1) - int(t0) + TILE - 1) // TILE for _, t0, t1, _ in s if t1 > t0))
     total = sum((L + TILE - 1) // TILE for L in lens)
     assert sum(tiles) == total
     if total:
