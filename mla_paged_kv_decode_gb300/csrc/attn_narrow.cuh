@@ -62,9 +62,12 @@ struct NarrowCfg {
     static constexpr int kStageBytes = 9 * kChunkBytes;        // 8 ckv chunks + kpe = 36 KB
     static constexpr int kStages = 5;
     static constexpr int kPartBytes = 4 * 32 * 16 * 4;         // per group: 4 warps x 32 lanes x 16 floats = 8 KB
+    static constexpr int kPRowBytes = 80;                       // P row: 32 bf16 tokens + 16 B pad (conflict-free ldmatrix)
+    static constexpr int kGroupScratch = 16 * kPRowBytes + 4 * 16 * 4;   // P tile + per-warp row maxima
     static constexpr int kOffStage = 0;
     static constexpr int kOffPart = kOffStage + kStages * kStageBytes;
-    static constexpr int kOffMisc = kOffPart + kGroups * kPartBytes;
+    static constexpr int kOffScratch = kOffPart + kGroups * kPartBytes;
+    static constexpr int kOffMisc = kOffScratch + kGroups * kGroupScratch;
     static constexpr int kMiscBytes = 1024;
     static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -99,6 +102,13 @@ __device__ __forceinline__ void mma_bf16_16816(float* c, const uint32_t* a, uint
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// 2^x with the hardware approximation (a few ulp; the inputs are <= 0 here)
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -252,6 +262,8 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
         const int head0 = group_cta * HG + hgi * 16;   // first head of this warp's group
         const uint32_t stage0 = smem_u32(stage_base);
         float* part = part_base + grp * (C::kPartBytes / 4);
+        uint8_t* pbuf = smem + C::kOffScratch + grp * C::kGroupScratch;              // P tile [16][80 B]
+        float* rowmax = reinterpret_cast<float*>(pbuf + 16 * C::kPRowBytes);           // [4 warps][16 rows]
         uint32_t scount = 0;     // ring stages consumed so far by the CTA (both token groups)
         bool ok = true;
         for (int si = seg_begin; si < seg_end && ok; ++si) {
@@ -323,7 +335,7 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                         }
                     }
                 }
-                // ---- exchange partials within the group, sum in fixed warp order
+                // ---- exchange partials within the group; warp kr finishes the scores of n8 tile kr
                 {
                     float4* dst = reinterpret_cast<float4*>(part) + kr * 4 * 32;
 #pragma unroll
@@ -339,60 +351,68 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                 }
                 named_barrier_sync(named_bar, 128);
                 if (cw == 0 && lane == 0) MLA_TRACE_EVENT(3, (uint32_t)tile_in_seg);
+                float s4[4];   // scores of (row g, tokens 8kr + 2c4, +1) and (row g + 8, same tokens)
                 {
                     const float4* src = reinterpret_cast<const float4*>(part);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float4 a0 = src[(0 * 4 + i) * 32 + lane], a1 = src[(1 * 4 + i) * 32 + lane];
-                        const float4 a2 = src[(2 * 4 + i) * 32 + lane], a3 = src[(3 * 4 + i) * 32 + lane];
-                        sc[i][0] = ((a0.x + a1.x) + a2.x) + a3.x;
-                        sc[i][1] = ((a0.y + a1.y) + a2.y) + a3.y;
-                        sc[i][2] = ((a0.z + a1.z) + a2.z) + a3.z;
-                        sc[i][3] = ((a0.w + a1.w) + a2.w) + a3.w;
-                    }
+                    const float4 a0 = src[(0 * 4 + kr) * 32 + lane], a1 = src[(1 * 4 + kr) * 32 + lane];
+                    const float4 a2 = src[(2 * 4 + kr) * 32 + lane], a3 = src[(3 * 4 + kr) * 32 + lane];
+                    s4[0] = ((a0.x + a1.x) + a2.x) + a3.x;
+                    s4[1] = ((a0.y + a1.y) + a2.y) + a3.y;
+                    s4[2] = ((a0.z + a1.z) + a2.z) + a3.z;
+                    s4[3] = ((a0.w + a1.w) + a2.w) + a3.w;
                 }
-                // the partial buffer is rewritten by the group's next tile only after every warp has read it
-                named_barrier_sync(named_bar, 128);
-                // ---- online softmax, rows g and g + 8 (log2 domain), masked past the last token
-                float mt[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-                for (int n = 0; n < 4; ++n)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int tok = n * 8 + 2 * c4 + (e & 1);
-                        const float v = tok < ntok ? sc[n][e] * prm.scale_log2 : -INFINITY;
-                        sc[n][e] = v;
-                        mt[e >> 1] = fmaxf(mt[e >> 1], v);
-                    }
+                if (ntok < kNarrowTile) {
+                    const int tok = kr * 8 + 2 * c4;
+                    if (tok >= ntok) s4[0] = s4[2] = -INFINITY;
+                    if (tok + 1 >= ntok) s4[1] = s4[3] = -INFINITY;
+                }
+                // ---- row maxima of the tile (raw scores; sm_scale > 0 keeps the order)
+                float mt[2] = {fmaxf(s4[0], s4[1]), fmaxf(s4[2], s4[3])};
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     mt[r] = fmaxf(mt[r], __shfl_xor_sync(0xffffffffu, mt[r], 1));
                     mt[r] = fmaxf(mt[r], __shfl_xor_sync(0xffffffffu, mt[r], 2));
                 }
-                float alpha[2];
+                if (c4 == 0) {
+                    rowmax[kr * 16 + g] = mt[0];
+                    rowmax[kr * 16 + g + 8] = mt[1];
+                }
+                named_barrier_sync(named_bar, 128);
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    const float mn = fmaxf(m_run[r], mt[r]);
-                    alpha[r] = exp2f(m_run[r] - mn);
-                    m_run[r] = mn;
-                    l_part[r] *= alpha[r];
-                }
+                    const int row = g + 8 * r;
+                    const float m4 = fmaxf(fmaxf(rowmax[row], rowmax[16 + row]), fmaxf(rowmax[32 + row], rowmax[48 + row]));
+                    // lazy running max (log2 units): move it, and rescale O and l, only when the tile max
+                    // exceeds it by more than 8; every warp of the group takes the same decision
+                    const float ms = m4 * prm.scale_log2;
+                    if (ms > m_run[r] + 8.f) {
+                        const float alpha = fast_exp2(m_run[r] - ms);
+                        m_run[r] = ms;
+                        l_part[r] *= alpha;
 #pragma unroll
-                for (int n = 0; n < 16; ++n) {
-                    o[n][0] *= alpha[0];
-                    o[n][1] *= alpha[0];
-                    o[n][2] *= alpha[1];
-                    o[n][3] *= alpha[1];
+                        for (int n = 0; n < 16; ++n) {
+                            o[n][2 * r] *= alpha;
+                            o[n][2 * r + 1] *= alpha;
+                        }
+                    }
                 }
-                uint32_t pa[2][4];   // P as the A operand of the 2 k16 token steps
-#pragma unroll
-                for (int n = 0; n < 4; ++n) {
-                    const float p0 = exp2f(sc[n][0] - m_run[0]), p1 = exp2f(sc[n][1] - m_run[0]);
-                    const float p2 = exp2f(sc[n][2] - m_run[1]), p3 = exp2f(sc[n][3] - m_run[1]);
+                {
+                    const float p0 = fast_exp2(fmaf(s4[0], prm.scale_log2, -m_run[0]));
+                    const float p1 = fast_exp2(fmaf(s4[1], prm.scale_log2, -m_run[0]));
+                    const float p2 = fast_exp2(fmaf(s4[2], prm.scale_log2, -m_run[1]));
+                    const float p3 = fast_exp2(fmaf(s4[3], prm.scale_log2, -m_run[1]));
                     l_part[0] += p0 + p1;
                     l_part[1] += p2 + p3;
-                    pa[n >> 1][(n & 1) * 2 + 0] = pack_bf16(p0, p1);
-                    pa[n >> 1][(n & 1) * 2 + 1] = pack_bf16(p2, p3);
+                    *reinterpret_cast<uint32_t*>(pbuf + g * C::kPRowBytes + (kr * 8 + 2 * c4) * 2) = pack_bf16(p0, p1);
+                    *reinterpret_cast<uint32_t*>(pbuf + (g + 8) * C::kPRowBytes + (kr * 8 + 2 * c4) * 2) = pack_bf16(p2, p3);
+                }
+                named_barrier_sync(named_bar, 128);
+                uint32_t pa[2][4];   // P as the A operand of the 2 k16 token steps
+#pragma unroll
+                for (int kt = 0; kt < 2; ++kt) {
+                    const int prow = (lane & 7) + ((lane & 8) ? 8 : 0);
+                    const int pcol = kt * 16 + ((lane & 16) ? 8 : 0);
+                    ldsm_x4(smem_u32(pbuf) + prow * C::kPRowBytes + pcol * 2, pa[kt][0], pa[kt][1], pa[kt][2], pa[kt][3]);
                 }
                 if (cw == 0 && lane == 0) MLA_TRACE_EVENT(4, (uint32_t)tile_in_seg);
                 // ---- O[16 x 128 dims of this warp] += P V
@@ -420,13 +440,24 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                 ++scount;
             }
             if (!ok) break;
-            // ---- row sums over the quad (every warp of the group holds identical m and l)
+            // ---- row sums: quad, then the 4 warps of the group (each summed its own 8 tokens per tile)
             float l[2];
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
                 l[r] = l_part[r];
                 l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
                 l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
+            }
+            named_barrier_sync(named_bar, 128);
+            if (c4 == 0) {
+                rowmax[kr * 16 + g] = l[0];
+                rowmax[kr * 16 + g + 8] = l[1];
+            }
+            named_barrier_sync(named_bar, 128);
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int row = g + 8 * r;
+                l[r] = (rowmax[row] + rowmax[16 + row]) + (rowmax[32 + row] + rowmax[48 + row]);
             }
             if (C::kTokenGroups == 2) {
                 // ---- merge the two token groups: group 1 passes (O, m, l) to group 0 through shared
