@@ -153,6 +153,33 @@ int mla_plan_heads_per_cta(mla_plan_t plan);
  * pointer may be NULL.  Returns the number of segments. */
 int mla_plan_get_segments(mla_plan_t plan, int32_t* segments, int32_t* unit_ptr);
 
+/* Decode for callers that cannot allocate device memory: cudaMalloc may be off
+ * limits (an allocator that must not be re-entered, a memory pool fixed at start-up,
+ * or a framework that owns every device allocation).  This call takes no workspace;
+ * it allocates nothing and calls no cudaMalloc, cudaFree or other allocating routine.
+ * The paper has no counterpart to this call: it is an alternative to mla_decode_plan_commit +
+ * mla_decode_run with the same arguments and results (minus workspace_dev).
+ *
+ * The workspace is a fixed device array inside this library, of
+ * mla_decode_noalloc_max_workspace_bytes() bytes (16 MiB), present on every GPU that
+ * loads the library until the process exits.  A plan whose
+ * mla_decode_plan_workspace_bytes exceeds it is rejected with
+ * MLA_ERR_WORKSPACE_TOO_SMALL.  Each call first copies the plan's work list (and
+ * zeroed merge counters and status word) into the array on cuda_stream, then
+ * launches the decode.  The first call on a device also looks up the array's device
+ * address (cudaGetSymbolAddress); make that first call before any stream capture.
+ * All calls share the one array: calls whose work may overlap on the GPU (different
+ * streams, or different host threads) race and corrupt each other's partials; order
+ * them on one stream.  Returns the codes of mla_decode_run, or
+ * MLA_ERR_WORKSPACE_TOO_SMALL. */
+mla_status_t mla_decode_run_noalloc(mla_plan_t plan, const void* q_nope, const void* q_pe, const void* ckv_cache,
+                                    const float* ckv_scale, const void* kpe_cache, int num_pages,
+                                    const int32_t* kv_indices, const int32_t* kv_indptr,
+                                    const int32_t* kv_last_page_len, float sm_scale, float* out, float* lse,
+                                    void* cuda_stream);
+/* Size of the fixed workspace array mla_decode_run_noalloc uses (bytes). */
+size_t mla_decode_noalloc_max_workspace_bytes(void);
+
 void mla_plan_destroy(mla_plan_t plan);
 
 /* Static string for a status code. */

@@ -31,7 +31,7 @@ EXPORTED = (
     "mla_decode_plan", "mla_decode_plan_workspace_bytes", "mla_decode_plan_commit", "mla_decode_run",
     "mla_decode_device_status", "mla_plan_num_ctas", "mla_plan_num_segments", "mla_plan_num_partials",
     "mla_plan_heads_per_cta", "mla_plan_get_segments", "mla_plan_destroy", "mla_status_string",
-    "mla_plan_num_launches",
+    "mla_plan_num_launches", "mla_decode_run_noalloc", "mla_decode_noalloc_max_workspace_bytes",
 )
 
 _lib = None
@@ -68,6 +68,11 @@ def load(path: Optional[str] = None):
     lib.mla_decode_plan_commit.argtypes = [vp, vp, sz, vp]
     lib.mla_decode_run.restype = ctypes.c_int
     lib.mla_decode_run.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_int, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp]
+    lib.mla_decode_run_noalloc.restype = ctypes.c_int
+    lib.mla_decode_run_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_int, vp, vp, vp, ctypes.c_float, vp, vp,
+                                           vp]
+    lib.mla_decode_noalloc_max_workspace_bytes.restype = sz
+    lib.mla_decode_noalloc_max_workspace_bytes.argtypes = []
     lib.mla_plan_num_launches.restype = ctypes.c_int
     lib.mla_plan_num_launches.argtypes = [vp]
     lib.mla_decode_device_status.restype = ctypes.c_int
@@ -154,6 +159,21 @@ def mla_decode_run(plan: Plan, q_nope, q_pe, ckv_cache, ckv_scale, kpe_cache, kv
                                  _ptr(kpe_cache), npages, _ptr(kv_indices), _ptr(kv_indptr), _ptr(kv_last_page_len),
                                  float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace), _stream(stream)),
            "mla_decode_run")
+
+
+def mla_decode_run_noalloc(plan: Plan, q_nope, q_pe, ckv_cache, ckv_scale, kpe_cache, kv_indices, kv_indptr,
+                           kv_last_page_len, sm_scale: float, out, lse, stream=None, num_pages=None):
+    """mla_decode_run without a workspace: the library's fixed device array is used instead
+    (for callers that cannot allocate device memory; calls that overlap on the GPU race)."""
+    npages = int(ckv_cache.shape[0]) if num_pages is None else int(num_pages)
+    _check(load().mla_decode_run_noalloc(plan.handle, _ptr(q_nope), _ptr(q_pe), _ptr(ckv_cache), _ptr(ckv_scale),
+                                         _ptr(kpe_cache), npages, _ptr(kv_indices), _ptr(kv_indptr),
+                                         _ptr(kv_last_page_len), float(sm_scale), _ptr(out), _ptr(lse), _stream(stream)),
+           "mla_decode_run_noalloc")
+
+
+def mla_decode_noalloc_max_workspace_bytes() -> int:
+    return int(load().mla_decode_noalloc_max_workspace_bytes())
 
 
 def mla_plan_num_launches(plan: Plan) -> int:

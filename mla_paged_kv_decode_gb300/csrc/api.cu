@@ -296,3 +296,114 @@ const char* mla_status_string(mla_status_t status) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------------
+// Decode without any device allocation by the caller or the library.
+//
+// The workspace (work-list header, split partials, status word) lives in a fixed, file-scope
+// device array instead of caller-allocated memory.  It exists once per GPU that loads this
+// library and stays allocated until the process exits.  Host code may not use its address
+// directly (in host code `g_noalloc_scratch` names a host-side stand-in), so the device address
+// is fetched with cudaGetSymbolAddress once per device, with that device current, and cached.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
+constexpr int kMaxDevices = 64;
+
+__device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (set up on first use).
+void* noalloc_scratch_address() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        g_noalloc_ptr[dev] = p;
+    }
+    return g_noalloc_ptr[dev];
+}
+
+}  // namespace
+
+extern "C" size_t mla_decode_noalloc_max_workspace_bytes(void) { return kNoAllocScratchBytes; }
+
+extern "C" mla_status_t mla_decode_run_noalloc(mla_plan_t plan, const void* q_nope, const void* q_pe,
+                                               const void* ckv_cache, const float* ckv_scale, const void* kpe_cache,
+                                               int num_pages, const int32_t* kv_indices, const int32_t* kv_indptr,
+                                               const int32_t* kv_last_page_len, float sm_scale, float* out,
+                                               float* lse, void* cuda_stream) {
+    if (!plan || !q_nope || !q_pe || !ckv_cache || !kpe_cache || !kv_indices || !kv_indptr || !kv_last_page_len ||
+        !out || !lse || num_pages < 1)
+        return MLA_ERR_INVALID_ARG;
+    const auto& d = plan->d;
+    if (d.layout.total_bytes > kNoAllocScratchBytes) return MLA_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned16(q_nope) || !aligned16(q_pe) || !aligned16(ckv_cache) || !aligned16(kpe_cache) ||
+        !aligned16(out) || !aligned16(lse))
+        return MLA_ERR_INVALID_ARG;
+    if (!std::isfinite(sm_scale)) return MLA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(num_pages) * d.page_size >= (int64_t(1) << 31)) return MLA_ERR_INVALID_ARG;
+    if (d.kv_dtype == MLA_KV_FP8_E4M3) return MLA_ERR_UNSUPPORTED;
+    if (d.kv_dtype == MLA_KV_BF16 && ckv_scale != nullptr) return MLA_ERR_INVALID_ARG;
+    (void)kv_last_page_len;
+
+    uint8_t* ws = static_cast<uint8_t*>(noalloc_scratch_address());
+    if (!ws) return MLA_ERR_CUDA;
+    cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+    // The plan's header (work list, zeroed status word and merge counters) is copied in on every
+    // call, straight from the plan's host image: the array keeps the previous call's contents.
+    if (cudaMemcpyAsync(ws, plan->image.data(), plan->image.size(), cudaMemcpyHostToDevice, stream) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    if (d.segments.empty()) return MLA_OK;
+
+    const auto& L = d.layout;
+    MapCache& mc = plan->maps;
+    if (!mc.valid || mc.ckv != ckv_cache || mc.kpe != kpe_cache || mc.qn != q_nope || mc.qp != q_pe ||
+        mc.num_pages != num_pages) {
+        const uint64_t rows = static_cast<uint64_t>(num_pages) * d.page_size;
+        const uint64_t qrows = static_cast<uint64_t>(d.batch) * d.h_q;
+        const uint32_t hg = static_cast<uint32_t>(d.heads_per_cta);
+        const uint32_t box = d.narrow ? std::min(d.page_size, mla::kNarrowStageTok) : d.page_size;
+        const bool chunked = d.narrow && box == static_cast<uint32_t>(mla::kNarrowStageTok);
+        mc.valid = (chunked ? make_map_ckv_chunked(&mc.m_ckv, ckv_cache, rows, box)
+                            : make_map_bf16(&mc.m_ckv, ckv_cache, mla::kDimCkv, rows, box)) &&
+                   make_map_bf16(&mc.m_kpe, kpe_cache, mla::kDimKpe, rows, box) &&
+                   make_map_bf16(&mc.m_qn, q_nope, mla::kDimCkv, qrows, hg) &&
+                   make_map_bf16(&mc.m_qp, q_pe, mla::kDimKpe, qrows, hg);
+        if (!mc.valid) return MLA_ERR_CUDA;
+        mc.ckv = ckv_cache;
+        mc.kpe = kpe_cache;
+        mc.qn = q_nope;
+        mc.qp = q_pe;
+        mc.num_pages = num_pages;
+    }
+    mla::AttnParams prm;
+    prm.unit_ptr = reinterpret_cast<const int32_t*>(ws + L.off_unit_ptr);
+    prm.segments = reinterpret_cast<const mla::Segment*>(ws + L.off_segments);
+    prm.kv_indices = kv_indices;
+    prm.kv_indptr = kv_indptr;
+    prm.ckv = static_cast<const uint8_t*>(ckv_cache);
+    prm.kpe = static_cast<const uint8_t*>(kpe_cache);
+    prm.out = out;
+    prm.lse = lse;
+    prm.part_o = reinterpret_cast<float*>(ws + L.off_part_o);
+    prm.part_lse = reinterpret_cast<float*>(ws + L.off_part_lse);
+    prm.counters = reinterpret_cast<int32_t*>(ws + L.off_counters);
+    prm.status = reinterpret_cast<uint32_t*>(ws + L.off_status);
+    prm.trace = nullptr;
+    prm.scale_log2 = sm_scale * 1.4426950408889634f;
+    prm.h_q = d.h_q;
+    prm.page_size = d.page_size;
+    prm.head_groups = d.head_groups;
+    cudaError_t e;
+    if (d.narrow)
+        e = d.h_q == 16 ? launch_narrow<16>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream)
+                        : launch_narrow<32>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream);
+    else
+        e = launch_attention<32>(plan, mc.m_ckv, mc.m_kpe, mc.m_qn, mc.m_qp, prm, stream);
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
