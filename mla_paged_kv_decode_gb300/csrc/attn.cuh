@@ -137,6 +137,7 @@ struct AttnMisc {
     float red_sum[4][32];
     float mrg_max[32];
     float mrg_inv[32];
+    float mrg_w[128];
 };
 
 static_assert(sizeof(AttnMisc) <= 3072, "misc region");
@@ -174,9 +175,17 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, AttnM
         if (prm.trace && blockIdx.x < 4 && (idx) < 256)                                       \
             prm.trace[(blockIdx.x * 8 + (ev)) * 256 + (idx)] = global_timer_ns();            \
     } while (0)
+// Every CTA also records 8 milestones (entry, producer done, ...) after the per-tile area.
+#define MLA_TRACE_CTA(k)                                                                      \
+    do {                                                                                      \
+        if (prm.trace) prm.trace[4 * 8 * 256 + blockIdx.x * 8 + (k)] = global_timer_ns();     \
+    } while (0)
 #else
 #define MLA_TRACE_EVENT(ev, idx) \
     do {                         \
+    } while (0)
+#define MLA_TRACE_CTA(k) \
+    do {                 \
     } while (0)
 #endif
 
@@ -190,6 +199,96 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
+}
+
+// Merge of the split pieces of one request for heads [head0, head0 + NH), run by the CTA
+// whose piece arrived last (FlashMLA PR #233, "deterministic combine"): with lse_i the
+// natural-log partial lse of piece i and o_i its normalised partial output,
+//     M = max_i lse_i,  w_i = exp(lse_i - M) / sum_j exp(lse_j - M),
+//     out = sum_i w_i o_i,  lse = M + ln sum_j exp(lse_j - M).
+// Every sum runs in a fixed order (pieces in slot order, fixed shuffle trees), so reruns
+// give identical bits.  The loads are issued in batches (all heads of a piece at once) so
+// the merge costs a few memory round trips rather than one per (piece, head).
+// NTHR threads (tid 0..NTHR-1) call it together and synchronise on named barrier `bar`.
+// Scratch in shared memory: s_max[NH], s_inv[NH], s_w[NTHR] (NTHR >= 8 * 16).
+template <int NH, int NTHR>
+__device__ __forceinline__ void merge_split_pieces(const AttnParams& prm, int b, int slot_begin, int n_slots,
+                                                   int head0, int tid, uint32_t bar, float* s_max, float* s_inv,
+                                                   float* s_w) {
+    static_assert(NTHR == 128 && NH % 16 == 0 && NTHR % NH == 0, "merge layout");
+    constexpr int kTph = NTHR / NH;    // threads per head in the lse pass
+    constexpr int kChunk = NTHR / 16;  // pieces whose weights are staged at a time (8)
+    const size_t hq = static_cast<size_t>(prm.h_q);
+    {
+        // ---- lse pass: thread (h, sub) scans pieces sub, sub + kTph, ... with a running (max, sum)
+        const int h = tid / kTph, sub = tid % kTph;
+        float m = -INFINITY, s = 0.f;
+        for (int i = sub; i < n_slots; i += kTph) {
+            const float x = __ldcg(prm.part_lse + (slot_begin + i) * hq + head0 + h);
+            if (x > m) {
+                s = (m == -INFINITY ? 0.f : s * expf(m - x)) + 1.f;
+                m = x;
+            } else {
+                s += expf(x - m);
+            }
+        }
+#pragma unroll
+        for (int o = kTph / 2; o > 0; o >>= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+            const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+            const float mm = fmaxf(m, m2);
+            const float a = (m == -INFINITY) ? 0.f : s * expf(m - mm);
+            const float c = (m2 == -INFINITY) ? 0.f : s2 * expf(m2 - mm);
+            s = a + c;   // both lanes of the pair add the same two values (addition commutes exactly)
+            m = mm;
+        }
+        if (sub == 0) {
+            s_max[h] = m;
+            s_inv[h] = 1.f / s;
+            prm.lse[static_cast<size_t>(b) * hq + head0 + h] = m + logf(s);
+        }
+    }
+    named_barrier_sync(bar, NTHR);
+    // ---- outputs: thread tid owns dims [4 tid, 4 tid + 4) of every head
+    float4* out4 = reinterpret_cast<float4*>(prm.out + (static_cast<size_t>(b) * hq + head0) * kDimCkv) + tid;
+#pragma unroll 1
+    for (int hb = 0; hb < NH; hb += 16) {
+        float4 acc[16];
+#pragma unroll
+        for (int h = 0; h < 16; ++h) acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+        for (int c0 = 0; c0 < n_slots; c0 += kChunk) {
+            {
+                const int i = tid / 16, h = tid % 16;   // weight of piece c0 + i for head hb + h
+                float w = 0.f;
+                if (c0 + i < n_slots)
+                    w = expf(__ldcg(prm.part_lse + (slot_begin + c0 + i) * hq + head0 + hb + h) - s_max[hb + h]) *
+                        s_inv[hb + h];
+                s_w[tid] = w;
+            }
+            named_barrier_sync(bar, NTHR);
+            const int n = min(kChunk, n_slots - c0);
+#pragma unroll 1
+            for (int i = 0; i < n; ++i) {
+                const float4* src =
+                    reinterpret_cast<const float4*>(prm.part_o + ((slot_begin + c0 + i) * hq + head0 + hb) * kDimCkv) + tid;
+                float4 v[16];
+#pragma unroll
+                for (int h = 0; h < 16; ++h) v[h] = __ldcg(src + h * (kDimCkv / 4));
+#pragma unroll
+                for (int h = 0; h < 16; ++h) {
+                    const float w = s_w[i * 16 + h];
+                    acc[h].x = fmaf(w, v[h].x, acc[h].x);
+                    acc[h].y = fmaf(w, v[h].y, acc[h].y);
+                    acc[h].z = fmaf(w, v[h].z, acc[h].z);
+                    acc[h].w = fmaf(w, v[h].w, acc[h].w);
+                }
+            }
+            named_barrier_sync(bar, NTHR);   // s_w is rewritten next
+        }
+#pragma unroll
+        for (int h = 0; h < 16; ++h) out4[(hb + h) * (kDimCkv / 4)] = acc[h];
+    }
 }
 
 // Walks the non-empty segments of one CTA slot tile by tile.
@@ -252,6 +351,7 @@ __global__ void __launch_bounds__(AttnCfg<HG>::kThreads, 1)
     const int P = prm.page_size;
 
     if (threadIdx.x == 0) {
+        MLA_TRACE_CTA(0);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&misc->q_full[i], 1);
             mbar_init(&misc->q_empty[i], 1);
@@ -418,6 +518,7 @@ __global__ void __launch_bounds__(AttnCfg<HG>::kThreads, 1)
         }
         // teardown: let every copy this warp issued land before the CTA can exit
         if (lane == 0) {
+            MLA_TRACE_CTA(1);
             const uint64_t t0 = global_timer_ns();
             auto drain = [&](uint64_t* bar, uint32_t uses) {
                 if (uses == 0) return;
@@ -717,34 +818,12 @@ __global__ void __launch_bounds__(AttnCfg<HG>::kThreads, 1)
                 }
                 named_barrier_sync(1, C::kSoftmaxThreads);
                 if (misc->merge_flag) {
+                    if (gtid == 0) MLA_TRACE_CTA(4);
                     __threadfence();
-                    if (gtid < HG) {
-                        float M = -INFINITY;
-                        for (int i = 0; i < sg.n_slots; ++i)
-                            M = fmaxf(M, __ldcg(prm.part_lse + static_cast<size_t>(sg.slot_begin + i) * prm.h_q + head0 + gtid));
-                        float ws = 0.f;
-                        for (int i = 0; i < sg.n_slots; ++i)
-                            ws += expf(__ldcg(prm.part_lse + static_cast<size_t>(sg.slot_begin + i) * prm.h_q + head0 + gtid) - M);
-                        misc->mrg_max[gtid] = M;
-                        misc->mrg_inv[gtid] = 1.f / ws;
-                        prm.lse[static_cast<size_t>(sg.b) * prm.h_q + head0 + gtid] = M + logf(ws);
-                    }
-                    named_barrier_sync(1, C::kSoftmaxThreads);
-                    float* out_b = prm.out + (static_cast<size_t>(sg.b) * prm.h_q + head0) * kDimCkv;
-                    for (int h = 0; h < HG; ++h) {
-                        const float M = misc->mrg_max[h], inv = misc->mrg_inv[h];
-                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                        for (int i = 0; i < sg.n_slots; ++i) {
-                            const size_t s = static_cast<size_t>(sg.slot_begin + i) * prm.h_q + head0 + h;
-                            const float w = expf(__ldcg(prm.part_lse + s) - M);
-                            const float* op = prm.part_o + s * kDimCkv + gtid;
-#pragma unroll
-                            for (int c = 0; c < 4; ++c) acc[c] = fmaf(w, __ldcg(op + c * 128), acc[c]);
-                        }
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) out_b[static_cast<size_t>(h) * kDimCkv + c * 128 + gtid] = acc[c] * inv;
-                    }
+                    merge_split_pieces<HG, C::kSoftmaxThreads>(prm, sg.b, sg.slot_begin, sg.n_slots, head0, gtid, 1,
+                                                               misc->mrg_max, misc->mrg_inv, misc->mrg_w);
                     if (gtid == 0) prm.counters[sg.item * prm.head_groups + group] = 0;
+                    if (gtid == 0) MLA_TRACE_CTA(5);
                 }
             }
             // red_sum / merge scratch are reused by the next segment only after this barrier
@@ -756,6 +835,7 @@ __global__ void __launch_bounds__(AttnCfg<HG>::kThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
+    if (threadIdx.x == 0) MLA_TRACE_CTA(6);
 }
 
 }  // namespace mla

@@ -82,6 +82,7 @@ struct NarrowMisc {
     int merge_flag[2];
     float mrg_max[2][16];
     float mrg_inv[2][16];
+    float mrg_w[2][128];
     float tg_m[16], tg_l[16];   // token-group merge: running max and row sum of group 1
 };
 
@@ -144,6 +145,7 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
     const int box_rows = P < kNarrowStageTok ? P : kNarrowStageTok;
 
     if (threadIdx.x == 0) {
+        MLA_TRACE_CTA(0);
         for (int i = 0; i < C::kStages; ++i) {
             mbar_init(&misc->full[i], 1);
             mbar_init(&misc->empty[i], 4);   // released by the 4 warps of the group that consumed it
@@ -242,6 +244,7 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
             more = cur.advance(new_seg);
         }
         if (lane == 0) {
+            MLA_TRACE_CTA(1);
             const uint64_t t0 = global_timer_ns();
             for (int s = 0; s < C::kStages; ++s) {
                 const uint32_t uses = scount / C::kStages + (static_cast<uint32_t>(s) < scount % C::kStages ? 1 : 0);
@@ -440,6 +443,7 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                 ++scount;
             }
             if (!ok) break;
+            if (kr == 0 && lane == 0) MLA_TRACE_CTA(2 + grp);
             // ---- row sums: quad, then the 4 warps of the group (each summed its own 8 tokens per tile)
             float l[2];
 #pragma unroll
@@ -542,40 +546,19 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                 }
                 named_barrier_sync(named_bar, 128);
                 if (misc->merge_flag[hgi]) {
+                    if (gt == 0) MLA_TRACE_CTA(4);
                     __threadfence();
-                    if (gt < 16) {
-                        float M = -INFINITY;
-                        for (int i = 0; i < sg.n_slots; ++i)
-                            M = fmaxf(M, __ldcg(prm.part_lse + static_cast<size_t>(sg.slot_begin + i) * prm.h_q + head0 + gt));
-                        float ws = 0.f;
-                        for (int i = 0; i < sg.n_slots; ++i)
-                            ws += expf(__ldcg(prm.part_lse + static_cast<size_t>(sg.slot_begin + i) * prm.h_q + head0 + gt) - M);
-                        misc->mrg_max[hgi][gt] = M;
-                        misc->mrg_inv[hgi][gt] = 1.f / ws;
-                        prm.lse[static_cast<size_t>(sg.b) * prm.h_q + head0 + gt] = M + logf(ws);
-                    }
-                    named_barrier_sync(named_bar, 128);
-                    float* out_b = prm.out + (static_cast<size_t>(sg.b) * prm.h_q + head0) * kDimCkv;
-                    for (int h = 0; h < 16; ++h) {
-                        const float M = misc->mrg_max[hgi][h], inv = misc->mrg_inv[hgi][h];
-                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                        for (int i = 0; i < sg.n_slots; ++i) {
-                            const size_t s = static_cast<size_t>(sg.slot_begin + i) * prm.h_q + head0 + h;
-                            const float w = expf(__ldcg(prm.part_lse + s) - M);
-                            const float* op = prm.part_o + s * kDimCkv + gt;
-#pragma unroll
-                            for (int c = 0; c < 4; ++c) acc[c] = fmaf(w, __ldcg(op + c * 128), acc[c]);
-                        }
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) out_b[static_cast<size_t>(h) * kDimCkv + c * 128 + gt] = acc[c] * inv;
-                    }
+                    merge_split_pieces<16, 128>(prm, sg.b, sg.slot_begin, sg.n_slots, head0, gt, named_bar,
+                                                misc->mrg_max[hgi], misc->mrg_inv[hgi], misc->mrg_w[hgi]);
                     if (gt == 0) prm.counters[ctr] = 0;
+                    if (gt == 0) MLA_TRACE_CTA(5);
                 }
                 named_barrier_sync(named_bar, 128);
             }
         }
     }
     __syncthreads();
+    if (threadIdx.x == 0) MLA_TRACE_CTA(6);
 }
 
 }  // namespace mla
