@@ -82,7 +82,7 @@ struct AttnParams {
     float* lse;                   // [B, h_q]
     float* part_o;                // [num_partials, h_q, 512]
     float* part_lse;              // [num_partials, h_q]
-    int32_t* counters;            // [num_split * head_groups]
+    int32_t* counters;            // arrivals per (split request, 16- or 32-head block)
     uint32_t* status;
     uint64_t* trace;              // per-tile event timestamps when built with MLA_TRACE, else unused
     float scale_log2;             // sm_scale * log2(e)
@@ -137,7 +137,7 @@ struct AttnMisc {
     float red_sum[4][32];
     float mrg_max[32];
     float mrg_inv[32];
-    float mrg_w[128];
+    float mrg_w[8 * 32];
 };
 
 static_assert(sizeof(AttnMisc) <= 3072, "misc region");

@@ -68,7 +68,7 @@ struct NarrowCfg {
     static constexpr int kOffPart = kOffStage + kStages * kStageBytes;
     static constexpr int kOffScratch = kOffPart + kGroups * kPartBytes;
     static constexpr int kOffMisc = kOffScratch + kGroups * kGroupScratch;
-    static constexpr int kMiscBytes = 1024;
+    static constexpr int kMiscBytes = 2048;
     static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     // the token-group merge passes one group's O (16 heads x 512 dims fp32) in two halves
@@ -129,6 +129,7 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                              const AttnParams prm, const uint16_t* __restrict__ q_nope,
                              const uint16_t* __restrict__ q_pe) {
     using C = NarrowCfg<HG>;
+    static_assert(sizeof(NarrowMisc) <= C::kMiscBytes, "misc region");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stage_base = smem + C::kOffStage;
@@ -146,9 +147,18 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
 
     if (threadIdx.x == 0) {
         MLA_TRACE_CTA(0);
+#ifdef MLA_TRACE
+        if (prm.trace) {
+            uint32_t smid;
+            asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+            prm.trace[4 * 8 * 256 + blockIdx.x * 8 + 7] = smid;
+        }
+#endif
         for (int i = 0; i < C::kStages; ++i) {
             mbar_init(&misc->full[i], 1);
-            mbar_init(&misc->empty[i], 4);   // released by the 4 warps of the group that consumed it
+            // released by the 4 warps of every 16-head group that consumes the stage: one token
+            // group takes each tile, and all kHeadGroups head groups read it
+            mbar_init(&misc->empty[i], 4 * C::kHeadGroups);
         }
         misc->abort_flag = 0;
         fence_mbarrier_init();
@@ -269,6 +279,23 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
         float* rowmax = reinterpret_cast<float*>(pbuf + 16 * C::kPRowBytes);           // [4 warps][16 rows]
         uint32_t scount = 0;     // ring stages consumed so far by the CTA (both token groups)
         bool ok = true;
+        // q fragments for dims [144 kr, 144 kr + 144): 9 k-steps of 16 (dims >= 512 are q_pe)
+        uint32_t qa[9][4];
+        auto load_q = [&](int b) {
+            const size_t qrow0 = static_cast<size_t>(b) * prm.h_q + head0;
+#pragma unroll
+            for (int ks = 0; ks < 9; ++ks) {
+                const int kd = kr * 144 + ks * 16;
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int row = g + ((r & 1) ? 8 : 0);
+                    const int dim = kd + 2 * c4 + ((r & 2) ? 8 : 0);
+                    const uint16_t* src = dim < kDimCkv ? q_nope + (qrow0 + row) * kDimCkv + dim
+                                                        : q_pe + (qrow0 + row) * kDimKpe + (dim - kDimCkv);
+                    qa[ks][r] = *reinterpret_cast<const uint32_t*>(src);
+                }
+            }
+        };
         for (int si = seg_begin; si < seg_end && ok; ++si) {
             const Segment sg = prm.segments[si];
             if (sg.t_end <= sg.t_begin) {
@@ -279,23 +306,7 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                 }
                 continue;
             }
-            // ---- q fragments for dims [144 kr, 144 kr + 144): 9 k-steps of 16 (dims >= 512 are q_pe)
-            uint32_t qa[9][4];
-            {
-                const size_t qrow0 = static_cast<size_t>(sg.b) * prm.h_q + head0;
-#pragma unroll
-                for (int ks = 0; ks < 9; ++ks) {
-                    const int kd = kr * 144 + ks * 16;
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        const int row = g + ((r & 1) ? 8 : 0);
-                        const int dim = kd + 2 * c4 + ((r & 2) ? 8 : 0);
-                        const uint16_t* src = dim < kDimCkv ? q_nope + (qrow0 + row) * kDimCkv + dim
-                                                            : q_pe + (qrow0 + row) * kDimKpe + (dim - kDimCkv);
-                        qa[ks][r] = *reinterpret_cast<const uint32_t*>(src);
-                    }
-                }
-            }
+            load_q(sg.b);
             float o[16][4];
 #pragma unroll
             for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
@@ -309,7 +320,22 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                     continue;
                 }
                 const uint32_t sl = scount % C::kStages;
-                ok = wait_phase_flag(&misc->full[sl], (scount / C::kStages) & 1, &misc->abort_flag, prm.status, 22);
+                const uint32_t use = scount / C::kStages;
+                // With two token groups the stages are consumed by the groups in turn: this
+                // stage's previous use (5 tiles back) is the other group's tile, which may not
+                // have landed yet, and a parity wait on the full barrier alone could then match
+                // that older phase.  So wait first until the previous use is released (its
+                // empty-barrier phase): the use before it (10 tiles back) is this group's own
+                // tile or from a segment both groups have finished, so that empty barrier is in
+                // the previous use's phase or this one and the wait is unambiguous.  Once the
+                // previous use is released the full barrier is in this use's phase.
+                // One warp of the group waits; the group barrier after it orders the other warps'
+                // reads of the stage after that warp's observation of the completed copy.
+                if (kr == 0) {
+                    if (C::kTokenGroups > 1 && use > 0)
+                        ok = wait_phase_flag(&misc->empty[sl], (use - 1) & 1, &misc->abort_flag, prm.status, 23);
+                    if (ok) ok = wait_phase_flag(&misc->full[sl], use & 1, &misc->abort_flag, prm.status, 22);
+                }
                 const uint32_t st_addr = stage0 + sl * C::kStageBytes;
                 ok = !named_barrier_or(named_bar, 128, !ok || *reinterpret_cast<volatile int*>(&misc->abort_flag));
                 if (!ok) break;
@@ -441,6 +467,12 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                 if (cw == 0 && lane == 0) MLA_TRACE_EVENT(5, (uint32_t)tile_in_seg);
                 if (lane == 0) mbar_arrive(&misc->empty[sl]);
                 ++scount;
+            }
+            if (C::kTokenGroups == 2) {
+                // Both token groups meet at every segment end, also after a bounded wait ran out,
+                // and leave together: neither can then block in the cross-group barriers below
+                // waiting for a group that has left.
+                ok = !named_barrier_or(merge_bar, 256, !ok || *reinterpret_cast<volatile int*>(&misc->abort_flag));
             }
             if (!ok) break;
             if (kr == 0 && lane == 0) MLA_TRACE_CTA(2 + grp);
