@@ -148,6 +148,10 @@ int mla_plan_num_ctas(mla_plan_t plan);       /* attention CTAs launched per run
 int mla_plan_num_segments(mla_plan_t plan);   /* (request, token range) pieces */
 int mla_plan_num_partials(mla_plan_t plan);   /* split pieces that go through the combine */
 int mla_plan_heads_per_cta(mla_plan_t plan);
+/* Partition cost, in tiles (32 tokens for h_q <= 32, else 128), that the balanced plan
+ * charges for each request start after the first: CTA slots are cut so that tiles plus
+ * these costs are equal to within one tile. */
+int mla_plan_segment_cost_tiles(mla_plan_t plan);
 /* Copy the work list: for segment i, out[4i..4i+3] = (request, token_begin, token_end,
  * partial slot or -1); unit_ptr[u] .. unit_ptr[u+1] are unit u's segments.  Either
  * pointer may be NULL.  Returns the number of segments. */

@@ -32,6 +32,7 @@ EXPORTED = (
     "mla_decode_device_status", "mla_plan_num_ctas", "mla_plan_num_segments", "mla_plan_num_partials",
     "mla_plan_heads_per_cta", "mla_plan_get_segments", "mla_plan_destroy", "mla_status_string",
     "mla_plan_num_launches", "mla_decode_run_noalloc", "mla_decode_noalloc_max_workspace_bytes",
+    "mla_plan_segment_cost_tiles",
 )
 
 _lib = None
@@ -77,7 +78,8 @@ def load(path: Optional[str] = None):
     lib.mla_plan_num_launches.argtypes = [vp]
     lib.mla_decode_device_status.restype = ctypes.c_int
     lib.mla_decode_device_status.argtypes = [vp, vp, vp]
-    for name in ("mla_plan_num_ctas", "mla_plan_num_segments", "mla_plan_num_partials", "mla_plan_heads_per_cta"):
+    for name in ("mla_plan_num_ctas", "mla_plan_num_segments", "mla_plan_num_partials", "mla_plan_heads_per_cta",
+                 "mla_plan_segment_cost_tiles"):
         getattr(lib, name).restype = ctypes.c_int
         getattr(lib, name).argtypes = [vp]
     lib.mla_plan_get_segments.restype = ctypes.c_int
@@ -198,6 +200,10 @@ def mla_plan_num_partials(plan: Plan) -> int:
 
 def mla_plan_heads_per_cta(plan: Plan) -> int:
     return int(load().mla_plan_heads_per_cta(plan.handle))
+
+
+def mla_plan_segment_cost_tiles(plan: Plan) -> int:
+    return int(load().mla_plan_segment_cost_tiles(plan.handle))
 
 
 def mla_plan_get_segments(plan: Plan):

@@ -261,6 +261,7 @@ int mla_plan_num_ctas(mla_plan_t plan) { return plan ? plan->d.num_units * plan-
 int mla_plan_num_segments(mla_plan_t plan) { return plan ? static_cast<int>(plan->d.segments.size()) : 0; }
 int mla_plan_num_partials(mla_plan_t plan) { return plan ? plan->d.num_partials : 0; }
 int mla_plan_heads_per_cta(mla_plan_t plan) { return plan ? plan->d.heads_per_cta : 0; }
+int mla_plan_segment_cost_tiles(mla_plan_t plan) { return plan ? plan->d.segment_cost : 0; }
 
 int mla_plan_get_segments(mla_plan_t plan, int32_t* segments, int32_t* unit_ptr) {
     if (!plan) return 0;

@@ -4,13 +4,14 @@
 // for its decode kernel without spelling out the partition; the reading used
 // here is the plainest one that balances SMs: lay every request's tokens end
 // to end in request order, cut the sequence into tiles of the kernel's tile size
-// (32 tokens for 16/32 heads, 128 for 64/128 heads; a request's
-// last tile may be short), and give CTA slot u the contiguous tile range
-// [floor(u*T/U), floor((u+1)*T/U)) of the T tiles, U = number of slots.  Every
-// slot therefore gets floor(T/U) or ceil(T/U) tiles.  A request whose tiles
-// land in more than one slot becomes several split pieces, each writing a
-// partial (out, lse); the CTA finishing the last piece merges them in slot
-// order.
+// (32 tokens for 16/32 heads, 128 for 64/128 heads; a request's last tile may
+// be short), and cut the sequence into U contiguous ranges of equal cost, one
+// per CTA slot.  A tile costs 1; every request start after the first also costs
+// kSegmentCost tiles, because a CTA that crosses into a new request pays a second
+// segment prologue and epilogue (query load, merge of its warp groups, output or
+// partial write).  A request whose tiles land in more than one slot becomes
+// several split pieces, each writing a partial (out, lse); the CTA finishing the
+// last piece merges them in slot order.
 #include "plan.h"
 
 #include <algorithm>
@@ -73,30 +74,44 @@ int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int ba
     int64_t units = std::max(1, num_sms / p.head_groups);
     units = std::min<int64_t>(units, std::max<int64_t>(total_tiles, 1));
     p.num_units = static_cast<int>(units);
+    p.segment_cost = narrow ? kNarrowSegmentCost : kSegmentCost;
 
-    // unit u owns global tiles [bound(u), bound(u+1))
-    auto bound = [&](int64_t u) { return u * total_tiles / units; };
+    // cost axis: request b occupies [start_b, start_b + c_b + tiles_b), its first c_b units
+    // being the request-start cost (0 for the first non-empty request)
+    int64_t total_cost = 0;
+    bool first = true;
+    for (int b = 0; b < batch; ++b) {
+        if (tiles[b] == 0) continue;
+        total_cost += (first ? 0 : p.segment_cost) + tiles[b];
+        first = false;
+    }
+    // unit u owns cost positions [bound(u), bound(u+1))
+    auto bound = [&](int64_t u) { return u * total_cost / units; };
 
     std::vector<std::vector<Segment>> per_unit(units);
     std::vector<int> pieces(batch, 0);
-    int64_t tile_base = 0;
+    int64_t cost_base = 0;
     int64_t u = 0;
+    first = true;
     for (int b = 0; b < batch; ++b) {
-        int64_t t0 = tile_base, t1 = tile_base + tiles[b];
-        while (t0 < t1) {
+        if (tiles[b] == 0) continue;
+        const int64_t r0 = cost_base + (first ? 0 : p.segment_cost);   // cost position of tile 0
+        const int64_t r1 = r0 + tiles[b];
+        first = false;
+        for (int64_t t0 = r0; t0 < r1;) {
             while (bound(u + 1) <= t0) ++u;
-            int64_t end = std::min<int64_t>(t1, bound(u + 1));
+            const int64_t end = std::min<int64_t>(r1, bound(u + 1));
             Segment s{};
             s.b = b;
-            s.t_begin = static_cast<int32_t>((t0 - tile_base) * tile_tok);
-            s.t_end = static_cast<int32_t>(std::min<int64_t>((end - tile_base) * tile_tok, len[b]));
+            s.t_begin = static_cast<int32_t>((t0 - r0) * tile_tok);
+            s.t_end = static_cast<int32_t>(std::min<int64_t>((end - r0) * tile_tok, len[b]));
             s.slot = -1;
             s.item = -1;
             per_unit[u].push_back(s);
             ++pieces[b];
             t0 = end;
         }
-        tile_base = t1;
+        cost_base = r1;
     }
 
     // partial slots: a split request's pieces get consecutive slots in token order

@@ -10,6 +10,11 @@ namespace mla {
 
 constexpr int kTileTokens = 128;   // tokens per tile of the wide-head (tcgen05) kernel
 constexpr int kNarrowTileTokens = 32;  // tokens per tile of the narrow-head (warp MMA) kernel
+// Partition cost of a request start (after the first), in tiles: what a CTA that crosses
+// into another request pays for the second segment's prologue and epilogue, measured on
+// GB300 against the time of one tile.
+constexpr int kNarrowSegmentCost = 8;
+constexpr int kSegmentCost = 1;
 constexpr int kDimCkv = 512;
 constexpr int kDimKpe = 64;
 
@@ -40,6 +45,7 @@ struct PlanData {
     int heads_per_cta = 0, head_groups = 0, num_units = 0;
     int tile_tokens = 0;              // plan granularity = the kernel's tile
     bool narrow = false;              // h_q <= 32: warp-MMA kernel, else tcgen05 kernel
+    int segment_cost = 0;             // partition cost of a request start, in tiles
     std::vector<int32_t> unit_ptr;
     std::vector<Segment> segments;
     int num_partials = 0;

@@ -1,8 +1,9 @@
 """Properties of the host split-KV plan (no GPU): every token of every request
-is covered exactly once, cuts fall on 128-token tile boundaries, work is
-balanced to within one tile per CTA slot, split pieces get consecutive
-partial slots in token order, and the plan is a deterministic function of
-its inputs."""
+is covered exactly once, cuts fall on the kernel's tile boundaries (32 tokens
+for 16/32 heads, 128 for 64/128), the cost per CTA slot (tiles plus a fixed
+cost per request start) is balanced, split pieces get consecutive partial
+slots in token order, and the plan is a deterministic function of its
+inputs."""
 import random
 
 import numpy as np
@@ -68,15 +69,26 @@ def _check_plan(lens, h_q, P, sms):
             assert slots == list(range(slots[0], slots[0] + len(slots)))
             n_split += len(pieces)
     assert mla.mla_plan_num_partials(plan) == n_split
-    # balance: tiles per unit differ by at most one
-    tiles = []
+    # balance: a unit's cost is its tiles plus c per request it starts (other than the
+    # batch's first non-empty request); the cut points sit on an equal-cost grid, but a
+    # request-start cost may straddle a cut (part of it then lies in the unit before the one
+    # holding the request's first tile), so counted this way costs agree to within 2c + 1
+    c = mla.mla_plan_segment_cost_tiles(plan)
+    assert c >= 0
+    first_b = next((b for b, L in enumerate(lens) if L > 0), None)
+    tiles, cost = [], []
     for u in range(units):
         s = segs[uptr[u]:uptr[u + 1]]
-        tiles.append(sum((int(t1) - int(t0) + TILE - 1) // TILE for _, t0, t1, _ in s if t1 > t0))
+        nt = sum((int(t1) - int(t0) + TILE - 1) // TILE for _, t0, t1, _ in s if t1 > t0)
+        starts = sum(1 for b, t0, t1, _ in s if t1 > t0 and t0 == 0 and b != first_b)
+        tiles.append(nt)
+        cost.append(nt + c * starts)
     total = sum((L + TILE - 1) // TILE for L in lens)
     assert sum(tiles) == total
-    if total:
-        assert max(tiles) - min(tiles) <= 1 or units == 1
+    if total and units > 1:
+        assert max(cost) - min(cost) <= 2 * c + 1, (max(cost), min(cost), c)
+        if c == 0:
+            assert max(tiles) - min(tiles) <= 1
     # workspace holds every partial
     assert plan.workspace_bytes >= n_split * h_q * (512 + 1) * 4
     return segs, uptr
@@ -112,3 +124,20 @@ def test_plan_is_deterministic():
     a = _check_plan(lens, 128, 16, 152)
     b = _check_plan(lens, 128, 16, 152)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_request_starts_cost_tiles():
+    """Units that cross into another request get fewer tiles than units inside one."""
+    segs, uptr = _check_plan([4096] * 64, 16, 64, 152)
+    TILE = 32
+    indptr, last = _lens_to_arrays([4096] * 64, 64)
+    plan = mla.mla_decode_plan(torch.from_numpy(indptr), torch.from_numpy(last), 64, 16, 64, 152)
+    c = mla.mla_plan_segment_cost_tiles(plan)
+    inside, crossing = [], []
+    for u in range(len(uptr) - 1):
+        s = segs[uptr[u]:uptr[u + 1]]
+        nt = sum((int(t1) - int(t0) + TILE - 1) // TILE for _, t0, t1, _ in s)
+        (crossing if len(s) > 1 else inside).append(nt)
+    assert inside and crossing
+    # a unit ending inside the next request's start cost also has fewer tiles, so compare means
+    assert sum(inside) / len(inside) - sum(crossing) / len(crossing) >= c / 2
