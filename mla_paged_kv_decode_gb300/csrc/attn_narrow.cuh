@@ -57,7 +57,15 @@ struct NarrowCfg {
     static constexpr int kTokenGroups = (HG == 16) ? 2 : 1;   // groups taking alternate tiles
     static constexpr int kGroups = kHeadGroups * kTokenGroups; // 4-warp compute groups
     static constexpr int kComputeWarps = 4 * kGroups;          // 8 in both cases: 2 warps per SM sub-partition
-    static constexpr int kThreads = 32 * (1 + kComputeWarps);
+    // warpgroup 0: the TMA producer (warp 0) and three helper warps; warpgroups 1 and 2: the
+    // compute groups.  Launched at 168 registers a thread (65536 / 384); warpgroup 0 gives
+    // registers back and the compute warpgroups take them (128 x 80 + 256 x 208 <= 384 x 168).
+    static constexpr int kProducerWarps = 4;
+    static constexpr int kThreads = 32 * (kProducerWarps + kComputeWarps);
+    static constexpr uint32_t kProducerRegs = 80;
+    static constexpr uint32_t kComputeRegs = 208;
+    static_assert(128 * kProducerRegs + 32 * kComputeWarps * kComputeRegs <= 65536 / kThreads / 8 * 8 * kThreads,
+                  "register split");
     static constexpr int kChunkBytes = kNarrowStageTok * 128;  // 64 dims x 32 tokens = 4 KB
     static constexpr int kStageBytes = 9 * kChunkBytes;        // 8 ckv chunks + kpe = 36 KB
     static constexpr int kStages = 5;
@@ -165,6 +173,9 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
     }
     __syncthreads();
 
+    if (warp < C::kProducerWarps) regs_dec<C::kProducerRegs>();
+    else regs_inc<C::kComputeRegs>();
+
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -262,9 +273,9 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                 while (!mbar_try_wait(&misc->full[s], (uses - 1) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {}
             }
         }
-    } else {
+    } else if (warp >= C::kProducerWarps) {
         // ------------------------------------------------------------ compute warps
-        const int cw = warp - 1;                 // 0 .. kComputeWarps-1
+        const int cw = warp - C::kProducerWarps;  // 0 .. kComputeWarps-1
         const int grp = cw / 4;                  // compute group (4 warps)
         const int hgi = grp / C::kTokenGroups;   // 16-head group within the CTA
         const int tg = grp % C::kTokenGroups;    // token group: takes tiles t with t % kTokenGroups == tg
