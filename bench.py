@@ -189,6 +189,20 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def time_workload(inp, n, stream):
+    """Seconds per decode step (one event pair around n steps after 5 warm-up steps)."""
+    dec, step, keep = bench_device(inp, 0, 5, stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    del keep, dec
+    return e0.elapsed_time(e1) / n / 1e3
+
+
 def bench_device(inp, steps, warmup, stream):
     """Device-timed steps with resident inputs.  Returns per-step and per-kernel times (s)."""
     import mla_paged_kv_decode_gb300 as mla
@@ -223,6 +237,7 @@ def main():
     ap.add_argument("--workload", default="membound", choices=sorted(WORKLOADS))
     ap.add_argument("--secondary", default="compute", help="second workload to report (TFLOPS), or 'none'")
     ap.add_argument("--sample-requests", type=int, default=16)
+    ap.add_argument("--fp8", type=int, default=1, help="also time the 8-bit cache workload against bf16 (1/0)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -322,27 +337,40 @@ def main():
 
     # ---- secondary: compute-shaped workload (TFLOPS), device-timed the same way
     secondary = None
-    if args.secondary != "none" and rank == 0 and world == 1:
+    fp8 = None
+    if (args.secondary != "none" or args.fp8) and rank == 0 and world == 1:
         del keep, dec
         torch.cuda.empty_cache()
+    if args.secondary != "none" and rank == 0 and world == 1:
         inp2 = make_inputs(WORKLOADS[args.secondary])
-        dec2, step2, keep2 = bench_device(inp2, 0, 5, stream)
-        n2 = max(20, min(args.steps // 10, 200))
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        e0.record(stream)
-        for i in range(n2):
-            step2()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        s2 = e0.elapsed_time(e1) / n2 / 1e3
+        s2 = time_workload(inp2, max(20, min(args.steps // 10, 200)), stream)
         f2 = algorithmic_flops(inp2)
         b2 = algorithmic_bytes(inp2)
         secondary = {"workload": args.secondary, "desc": WORKLOADS[args.secondary].description,
                      "us_per_step": s2 * 1e6, "tflops": f2 / s2 / 1e12, "kv_gbs": b2 / s2 / 1e9,
                      "tensor_frac": f2 / s2 / 1e12 / bf16_tf, "hbm_frac": b2 / s2 / 1e9 / hbm_gbs,
                      "alg_flops": f2, "alg_bytes": b2}
-        del keep2, dec2
+        del inp2
+        torch.cuda.empty_cache()
+
+    # ---- 8-bit cache: e4m3 + per-token scale against the same shape with a bf16 cache
+    if args.fp8 and rank == 0 and world == 1:
+        n8 = max(20, min(args.steps // 20, 100))
+        inp8 = make_inputs(WORKLOADS["fp8"])
+        t8 = time_workload(inp8, n8, stream)
+        b8 = algorithmic_bytes(inp8)
+        tok = int(inp8.kv_lens.sum())
+        del inp8
+        torch.cuda.empty_cache()
+        inp16 = make_inputs(WORKLOADS["fp8"], fp8=False)
+        t16 = time_workload(inp16, n8, stream)
+        b16 = algorithmic_bytes(inp16)
+        del inp16
+        torch.cuda.empty_cache()
+        fp8 = {"workload": "fp8", "desc": WORKLOADS["fp8"].description, "us_per_step": t8 * 1e6,
+               "gbs": b8 / t8 / 1e9, "hbm_frac": b8 / t8 / 1e9 / hbm_gbs, "tokens_per_s": tok / t8,
+               "bf16_us_per_step": t16 * 1e6, "bf16_gbs": b16 / t16 / 1e9,
+               "speedup_vs_bf16": t16 / t8, "bytes_per_token": {"fp8": 644, "bf16": 1152}}
 
     # ---- cpu baseline: the oracle on a bounded sample, host cores, rank 0 at N=1
     cpu = None
@@ -367,7 +395,8 @@ def main():
                        "tflops": alg_flops * args.steps * world / total_max / 1e12},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
                          "frac": achieved / hbm_gbs, "traffic": recorded_traffic(args.workload),
-                         "kernel": "mla_decode_attn_kernel", "peak_source": peak_src,
+                         "kernel": ("mla_decode_narrow_kernel" if inp.h_q <= 32 else "mla_decode_attn_kernel"),
+                         "peak_source": peak_src,
                          "kernel_us": attn_avg * 1e6},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -375,6 +404,7 @@ def main():
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
             "secondary": secondary,
+            "fp8": fp8,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -78,6 +78,30 @@ bool make_map_ckv_chunked(CUtensorMap* map, const void* base, uint64_t rows, uin
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// e4m3 codes of the ckv cache ([rows, 512] bytes) for the narrow kernel: with whole 32-token
+// stages a 3-D view (128 code columns, rows, 4 chunks; strides 512 B, 128 B) whose box lands
+// as [chunk][row][128 B]; otherwise a 2-D view with 128-column boxes, one per chunk.  Both
+// with the 128-byte swizzle.
+bool make_map_codes(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows, bool chunked) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint32_t es[3] = {1, 1, 1};
+    if (chunked) {
+        cuuint64_t dims[3] = {128, rows, 4};
+        cuuint64_t strides[2] = {mla::kDimCkv, 128};
+        cuuint32_t box[3] = {128, box_rows, 4};
+        return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
+    cuuint64_t dims[2] = {mla::kDimCkv, rows};
+    cuuint64_t strides[1] = {mla::kDimCkv};
+    cuuint32_t box[2] = {128, box_rows};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 void build_image(mla_plan_s* p) {
@@ -89,15 +113,15 @@ void build_image(mla_plan_s* p) {
                     sizeof(mla::Segment) * p->d.segments.size());
 }
 
-template <int HG>
+template <int HG, bool F8>
 cudaError_t launch_narrow(const mla_plan_s* p, const CUtensorMap& ckv, const CUtensorMap& kpe, const mla::AttnParams& prm,
                           const void* q_nope, const void* q_pe, cudaStream_t stream) {
-    using C = mla::NarrowCfg<HG>;
-    cudaError_t e = cudaFuncSetAttribute(mla::mla_decode_narrow_kernel<HG>,
+    using C = mla::NarrowCfg<HG, F8>;
+    cudaError_t e = cudaFuncSetAttribute(mla::mla_decode_narrow_kernel<HG, F8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int grid = p->d.num_units * p->d.head_groups;
-    mla::mla_decode_narrow_kernel<HG><<<grid, C::kThreads, C::kSmemBytes, stream>>>(
+    mla::mla_decode_narrow_kernel<HG, F8><<<grid, C::kThreads, C::kSmemBytes, stream>>>(
         ckv, kpe, prm, static_cast<const uint16_t*>(q_nope), static_cast<const uint16_t*>(q_pe));
     return cudaGetLastError();
 }
@@ -114,6 +138,94 @@ cudaError_t launch_attention(const mla_plan_s* p, const CUtensorMap& ckv, const 
     const int grid = p->d.num_units * p->d.head_groups;
     mla::mla_decode_attn_kernel<HG><<<grid, C::kThreads, C::kSmemBytes, stream>>>(ckv, kpe, qn, qp, prm);
     return cudaGetLastError();
+}
+
+// Argument checks, tensor maps and the launch shared by mla_decode_run and
+// mla_decode_run_noalloc; `ws` is the committed workspace (device).
+mla_status_t run_checked(mla_plan_t plan, const void* q_nope, const void* q_pe, const void* ckv_cache,
+                         const float* ckv_scale, const void* kpe_cache, int num_pages, const int32_t* kv_indices,
+                         const int32_t* kv_indptr, float sm_scale, float* out, float* lse, uint8_t* ws,
+                         cudaStream_t stream, uint64_t* trace) {
+    const auto& d = plan->d;
+    const bool f8 = d.kv_dtype == MLA_KV_FP8_E4M3;
+    const auto& L = d.layout;
+    // tensor maps depend only on the buffer addresses: re-encode when they change
+    MapCache& mc = plan->maps;
+    if (!mc.valid || mc.ckv != ckv_cache || mc.kpe != kpe_cache || mc.qn != q_nope || mc.qp != q_pe ||
+        mc.num_pages != num_pages) {
+        const uint64_t rows = static_cast<uint64_t>(num_pages) * d.page_size;
+        const uint64_t qrows = static_cast<uint64_t>(d.batch) * d.h_q;
+        const uint32_t hg = static_cast<uint32_t>(d.heads_per_cta);
+        // box rows: a whole page for the tcgen05 kernel, a 32-token ring stage at most for the narrow one
+        const uint32_t box = d.narrow ? std::min(d.page_size, mla::kNarrowStageTok) : d.page_size;
+        // the narrow kernel takes a whole 32-token stage of ckv in one 3-D box when a page holds it
+        const bool chunked = d.narrow && box == static_cast<uint32_t>(mla::kNarrowStageTok);
+        bool ok_ckv;
+        if (f8)
+            ok_ckv = make_map_codes(&mc.m_ckv, ckv_cache, rows, box, chunked);
+        else
+            ok_ckv = chunked ? make_map_ckv_chunked(&mc.m_ckv, ckv_cache, rows, box)
+                             : make_map_bf16(&mc.m_ckv, ckv_cache, mla::kDimCkv, rows, box);
+        mc.valid = ok_ckv && make_map_bf16(&mc.m_kpe, kpe_cache, mla::kDimKpe, rows, box) &&
+                   make_map_bf16(&mc.m_qn, q_nope, mla::kDimCkv, qrows, hg) &&
+                   make_map_bf16(&mc.m_qp, q_pe, mla::kDimKpe, qrows, hg);
+        if (!mc.valid) return MLA_ERR_CUDA;
+        mc.ckv = ckv_cache;
+        mc.kpe = kpe_cache;
+        mc.qn = q_nope;
+        mc.qp = q_pe;
+        mc.num_pages = num_pages;
+    }
+    mla::AttnParams prm;
+    prm.unit_ptr = reinterpret_cast<const int32_t*>(ws + L.off_unit_ptr);
+    prm.segments = reinterpret_cast<const mla::Segment*>(ws + L.off_segments);
+    prm.kv_indices = kv_indices;
+    prm.kv_indptr = kv_indptr;
+    prm.ckv = static_cast<const uint8_t*>(ckv_cache);
+    prm.kpe = static_cast<const uint8_t*>(kpe_cache);
+    prm.out = out;
+    prm.lse = lse;
+    prm.part_o = reinterpret_cast<float*>(ws + L.off_part_o);
+    prm.part_lse = reinterpret_cast<float*>(ws + L.off_part_lse);
+    prm.ckv_scale = ckv_scale;
+    prm.counters = reinterpret_cast<int32_t*>(ws + L.off_counters);
+    prm.status = reinterpret_cast<uint32_t*>(ws + L.off_status);
+    prm.trace = trace;
+    prm.scale_log2 = sm_scale * 1.4426950408889634f;
+    prm.h_q = d.h_q;
+    prm.page_size = d.page_size;
+    prm.head_groups = d.head_groups;
+    cudaError_t e;
+    if (d.narrow) {
+        if (f8)
+            e = d.h_q == 16 ? launch_narrow<16, true>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream)
+                            : launch_narrow<32, true>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream);
+        else
+            e = d.h_q == 16 ? launch_narrow<16, false>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream)
+                            : launch_narrow<32, false>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream);
+    } else {
+        e = launch_attention<32>(plan, mc.m_ckv, mc.m_kpe, mc.m_qn, mc.m_qp, prm, stream);
+    }
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+// Host-side argument checks common to both run entry points.
+mla_status_t check_run_args(mla_plan_t plan, const void* q_nope, const void* q_pe, const void* ckv_cache,
+                            const float* ckv_scale, const void* kpe_cache, int num_pages, const int32_t* kv_indices,
+                            const int32_t* kv_indptr, const int32_t* kv_last_page_len, float sm_scale,
+                            const float* out, const float* lse) {
+    if (!plan || !q_nope || !q_pe || !ckv_cache || !kpe_cache || !kv_indices || !kv_indptr || !kv_last_page_len ||
+        !out || !lse || num_pages < 1)
+        return MLA_ERR_INVALID_ARG;
+    const auto& d = plan->d;
+    if (!aligned16(q_nope) || !aligned16(q_pe) || !aligned16(ckv_cache) || !aligned16(kpe_cache) ||
+        !aligned16(out) || !aligned16(lse))
+        return MLA_ERR_INVALID_ARG;
+    if (!std::isfinite(sm_scale)) return MLA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(num_pages) * d.page_size >= (int64_t(1) << 31)) return MLA_ERR_INVALID_ARG;
+    if (d.kv_dtype == MLA_KV_BF16 && ckv_scale != nullptr) return MLA_ERR_INVALID_ARG;
+    if (d.kv_dtype == MLA_KV_FP8_E4M3 && (ckv_scale == nullptr || !aligned16(ckv_scale))) return MLA_ERR_INVALID_ARG;
+    return MLA_OK;
 }
 
 }  // namespace
@@ -163,73 +275,16 @@ mla_status_t mla_decode_run(mla_plan_t plan, const void* q_nope, const void* q_p
                             const int32_t* kv_indices, const int32_t* kv_indptr,
                             const int32_t* kv_last_page_len, float sm_scale, float* out, float* lse,
                             void* workspace_dev, void* cuda_stream) {
-    if (!plan || !q_nope || !q_pe || !ckv_cache || !kpe_cache || !kv_indices || !kv_indptr || !kv_last_page_len ||
-        !out || !lse || !workspace_dev || num_pages < 1)
-        return MLA_ERR_INVALID_ARG;
-    const auto& d = plan->d;
+    mla_status_t st = check_run_args(plan, q_nope, q_pe, ckv_cache, ckv_scale, kpe_cache, num_pages, kv_indices,
+                                     kv_indptr, kv_last_page_len, sm_scale, out, lse);
+    if (st != MLA_OK) return st;
+    if (!workspace_dev) return MLA_ERR_INVALID_ARG;
     if (std::find(plan->committed.begin(), plan->committed.end(), workspace_dev) == plan->committed.end())
         return MLA_ERR_NOT_COMMITTED;
-    if (!aligned16(q_nope) || !aligned16(q_pe) || !aligned16(ckv_cache) || !aligned16(kpe_cache) ||
-        !aligned16(out) || !aligned16(lse))
-        return MLA_ERR_INVALID_ARG;
-    if (!std::isfinite(sm_scale)) return MLA_ERR_INVALID_ARG;
-    if (static_cast<int64_t>(num_pages) * d.page_size >= (int64_t(1) << 31)) return MLA_ERR_INVALID_ARG;
-    if (d.kv_dtype == MLA_KV_FP8_E4M3) return MLA_ERR_UNSUPPORTED;
-    if (d.kv_dtype == MLA_KV_BF16 && ckv_scale != nullptr) return MLA_ERR_INVALID_ARG;
-    (void)kv_last_page_len;  // lengths are baked into the plan; kept for the ABI contract
-    if (d.segments.empty()) return MLA_OK;
-
-    cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
-    uint8_t* ws = static_cast<uint8_t*>(workspace_dev);
-    const auto& L = d.layout;
-    // tensor maps depend only on the buffer addresses: re-encode when they change
-    MapCache& mc = plan->maps;
-    if (!mc.valid || mc.ckv != ckv_cache || mc.kpe != kpe_cache || mc.qn != q_nope || mc.qp != q_pe ||
-        mc.num_pages != num_pages) {
-        const uint64_t rows = static_cast<uint64_t>(num_pages) * d.page_size;
-        const uint64_t qrows = static_cast<uint64_t>(d.batch) * d.h_q;
-        const uint32_t hg = static_cast<uint32_t>(d.heads_per_cta);
-        // box rows: a whole page for the tcgen05 kernel, a 32-token ring stage at most for the narrow one
-        const uint32_t box = d.narrow ? std::min(d.page_size, mla::kNarrowStageTok) : d.page_size;
-        // the narrow kernel takes a whole 32-token stage of ckv in one 3-D box when a page holds it
-        const bool chunked = d.narrow && box == static_cast<uint32_t>(mla::kNarrowStageTok);
-        mc.valid = (chunked ? make_map_ckv_chunked(&mc.m_ckv, ckv_cache, rows, box)
-                            : make_map_bf16(&mc.m_ckv, ckv_cache, mla::kDimCkv, rows, box)) &&
-                   make_map_bf16(&mc.m_kpe, kpe_cache, mla::kDimKpe, rows, box) &&
-                   make_map_bf16(&mc.m_qn, q_nope, mla::kDimCkv, qrows, hg) &&
-                   make_map_bf16(&mc.m_qp, q_pe, mla::kDimKpe, qrows, hg);
-        if (!mc.valid) return MLA_ERR_CUDA;
-        mc.ckv = ckv_cache;
-        mc.kpe = kpe_cache;
-        mc.qn = q_nope;
-        mc.qp = q_pe;
-        mc.num_pages = num_pages;
-    }
-    mla::AttnParams prm;
-    prm.unit_ptr = reinterpret_cast<const int32_t*>(ws + L.off_unit_ptr);
-    prm.segments = reinterpret_cast<const mla::Segment*>(ws + L.off_segments);
-    prm.kv_indices = kv_indices;
-    prm.kv_indptr = kv_indptr;
-    prm.ckv = static_cast<const uint8_t*>(ckv_cache);
-    prm.kpe = static_cast<const uint8_t*>(kpe_cache);
-    prm.out = out;
-    prm.lse = lse;
-    prm.part_o = reinterpret_cast<float*>(ws + L.off_part_o);
-    prm.part_lse = reinterpret_cast<float*>(ws + L.off_part_lse);
-    prm.counters = reinterpret_cast<int32_t*>(ws + L.off_counters);
-    prm.status = reinterpret_cast<uint32_t*>(ws + L.off_status);
-    prm.trace = plan->trace;
-    prm.scale_log2 = sm_scale * 1.4426950408889634f;
-    prm.h_q = d.h_q;
-    prm.page_size = d.page_size;
-    prm.head_groups = d.head_groups;
-    cudaError_t e;
-    if (d.narrow)
-        e = d.h_q == 16 ? launch_narrow<16>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream)
-                        : launch_narrow<32>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream);
-    else
-        e = launch_attention<32>(plan, mc.m_ckv, mc.m_kpe, mc.m_qn, mc.m_qp, prm, stream);
-    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+    if (plan->d.segments.empty()) return MLA_OK;
+    return run_checked(plan, q_nope, q_pe, ckv_cache, ckv_scale, kpe_cache, num_pages, kv_indices, kv_indptr,
+                       sm_scale, out, lse, static_cast<uint8_t*>(workspace_dev),
+                       static_cast<cudaStream_t>(cuda_stream), plan->trace);
 }
 
 #ifdef MLA_TRACE
@@ -338,20 +393,10 @@ extern "C" mla_status_t mla_decode_run_noalloc(mla_plan_t plan, const void* q_no
                                                int num_pages, const int32_t* kv_indices, const int32_t* kv_indptr,
                                                const int32_t* kv_last_page_len, float sm_scale, float* out,
                                                float* lse, void* cuda_stream) {
-    if (!plan || !q_nope || !q_pe || !ckv_cache || !kpe_cache || !kv_indices || !kv_indptr || !kv_last_page_len ||
-        !out || !lse || num_pages < 1)
-        return MLA_ERR_INVALID_ARG;
-    const auto& d = plan->d;
-    if (d.layout.total_bytes > kNoAllocScratchBytes) return MLA_ERR_WORKSPACE_TOO_SMALL;
-    if (!aligned16(q_nope) || !aligned16(q_pe) || !aligned16(ckv_cache) || !aligned16(kpe_cache) ||
-        !aligned16(out) || !aligned16(lse))
-        return MLA_ERR_INVALID_ARG;
-    if (!std::isfinite(sm_scale)) return MLA_ERR_INVALID_ARG;
-    if (static_cast<int64_t>(num_pages) * d.page_size >= (int64_t(1) << 31)) return MLA_ERR_INVALID_ARG;
-    if (d.kv_dtype == MLA_KV_FP8_E4M3) return MLA_ERR_UNSUPPORTED;
-    if (d.kv_dtype == MLA_KV_BF16 && ckv_scale != nullptr) return MLA_ERR_INVALID_ARG;
-    (void)kv_last_page_len;
-
+    mla_status_t st = check_run_args(plan, q_nope, q_pe, ckv_cache, ckv_scale, kpe_cache, num_pages, kv_indices,
+                                     kv_indptr, kv_last_page_len, sm_scale, out, lse);
+    if (st != MLA_OK) return st;
+    if (plan->d.layout.total_bytes > kNoAllocScratchBytes) return MLA_ERR_WORKSPACE_TOO_SMALL;
     uint8_t* ws = static_cast<uint8_t*>(noalloc_scratch_address());
     if (!ws) return MLA_ERR_CUDA;
     cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
@@ -359,52 +404,7 @@ extern "C" mla_status_t mla_decode_run_noalloc(mla_plan_t plan, const void* q_no
     // call, straight from the plan's host image: the array keeps the previous call's contents.
     if (cudaMemcpyAsync(ws, plan->image.data(), plan->image.size(), cudaMemcpyHostToDevice, stream) != cudaSuccess)
         return MLA_ERR_CUDA;
-    if (d.segments.empty()) return MLA_OK;
-
-    const auto& L = d.layout;
-    MapCache& mc = plan->maps;
-    if (!mc.valid || mc.ckv != ckv_cache || mc.kpe != kpe_cache || mc.qn != q_nope || mc.qp != q_pe ||
-        mc.num_pages != num_pages) {
-        const uint64_t rows = static_cast<uint64_t>(num_pages) * d.page_size;
-        const uint64_t qrows = static_cast<uint64_t>(d.batch) * d.h_q;
-        const uint32_t hg = static_cast<uint32_t>(d.heads_per_cta);
-        const uint32_t box = d.narrow ? std::min(d.page_size, mla::kNarrowStageTok) : d.page_size;
-        const bool chunked = d.narrow && box == static_cast<uint32_t>(mla::kNarrowStageTok);
-        mc.valid = (chunked ? make_map_ckv_chunked(&mc.m_ckv, ckv_cache, rows, box)
-                            : make_map_bf16(&mc.m_ckv, ckv_cache, mla::kDimCkv, rows, box)) &&
-                   make_map_bf16(&mc.m_kpe, kpe_cache, mla::kDimKpe, rows, box) &&
-                   make_map_bf16(&mc.m_qn, q_nope, mla::kDimCkv, qrows, hg) &&
-                   make_map_bf16(&mc.m_qp, q_pe, mla::kDimKpe, qrows, hg);
-        if (!mc.valid) return MLA_ERR_CUDA;
-        mc.ckv = ckv_cache;
-        mc.kpe = kpe_cache;
-        mc.qn = q_nope;
-        mc.qp = q_pe;
-        mc.num_pages = num_pages;
-    }
-    mla::AttnParams prm;
-    prm.unit_ptr = reinterpret_cast<const int32_t*>(ws + L.off_unit_ptr);
-    prm.segments = reinterpret_cast<const mla::Segment*>(ws + L.off_segments);
-    prm.kv_indices = kv_indices;
-    prm.kv_indptr = kv_indptr;
-    prm.ckv = static_cast<const uint8_t*>(ckv_cache);
-    prm.kpe = static_cast<const uint8_t*>(kpe_cache);
-    prm.out = out;
-    prm.lse = lse;
-    prm.part_o = reinterpret_cast<float*>(ws + L.off_part_o);
-    prm.part_lse = reinterpret_cast<float*>(ws + L.off_part_lse);
-    prm.counters = reinterpret_cast<int32_t*>(ws + L.off_counters);
-    prm.status = reinterpret_cast<uint32_t*>(ws + L.off_status);
-    prm.trace = nullptr;
-    prm.scale_log2 = sm_scale * 1.4426950408889634f;
-    prm.h_q = d.h_q;
-    prm.page_size = d.page_size;
-    prm.head_groups = d.head_groups;
-    cudaError_t e;
-    if (d.narrow)
-        e = d.h_q == 16 ? launch_narrow<16>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream)
-                        : launch_narrow<32>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream);
-    else
-        e = launch_attention<32>(plan, mc.m_ckv, mc.m_kpe, mc.m_qn, mc.m_qp, prm, stream);
-    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+    if (plan->d.segments.empty()) return MLA_OK;
+    return run_checked(plan, q_nope, q_pe, ckv_cache, ckv_scale, kpe_cache, num_pages, kv_indices, kv_indptr,
+                       sm_scale, out, lse, ws, stream, nullptr);
 }

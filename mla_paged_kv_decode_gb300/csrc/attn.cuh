@@ -82,6 +82,7 @@ struct AttnParams {
     float* lse;                   // [B, h_q]
     float* part_o;                // [num_partials, h_q, 512]
     float* part_lse;              // [num_partials, h_q]
+    const float* ckv_scale;       // e4m3 cache: fp32 scale per token [num_pages * page_size], else null
     int32_t* counters;            // arrivals per (split request, 16- or 32-head block)
     uint32_t* status;
     uint64_t* trace;              // per-tile event timestamps when built with MLA_TRACE, else unused

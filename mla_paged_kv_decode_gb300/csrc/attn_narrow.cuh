@@ -39,6 +39,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "attn.cuh"
 #include "plan.h"
@@ -48,36 +49,43 @@ namespace mla {
 
 constexpr int kNarrowTile = 32;        // tokens per tile (= one ring stage)
 constexpr int kNarrowStageTok = 32;    // tokens per ring stage
-constexpr int kNarrowPrefetchTiles = 0; // L2 prefetch distance in tiles (0: off; the bulk prefetch shares the TMA engine with the stage loads and measured slower)
 
-template <int HG>
+template <int HG, bool F8>
 struct NarrowCfg {
     static_assert(HG == 16 || HG == 32, "heads per CTA");
     static constexpr int kHeadGroups = HG / 16;               // 16-head groups
     static constexpr int kTokenGroups = (HG == 16) ? 2 : 1;   // groups taking alternate tiles
     static constexpr int kGroups = kHeadGroups * kTokenGroups; // 4-warp compute groups
     static constexpr int kComputeWarps = 4 * kGroups;          // 8 in both cases: 2 warps per SM sub-partition
-    // warpgroup 0: the TMA producer (warp 0) and three helper warps; warpgroups 1 and 2: the
-    // compute groups.  Launched at 168 registers a thread (65536 / 384); warpgroup 0 gives
-    // registers back and the compute warpgroups take them (128 x 80 + 256 x 208 <= 384 x 168).
+    // warpgroup 0: the TMA producer (warp 0; warps 1-3 idle); warpgroups 1 and 2: the compute
+    // groups.  Launched at 168 registers a thread (65536 / 384); warpgroup 0 gives registers
+    // back and the compute warpgroups take them (128 x 80 + 256 x 208 <= 384 x 168).
     static constexpr int kProducerWarps = 4;
     static constexpr int kThreads = 32 * (kProducerWarps + kComputeWarps);
     static constexpr uint32_t kProducerRegs = 80;
     static constexpr uint32_t kComputeRegs = 208;
     static_assert(128 * kProducerRegs + 32 * kComputeWarps * kComputeRegs <= 65536 / kThreads / 8 * 8 * kThreads,
                   "register split");
-    static constexpr int kChunkBytes = kNarrowStageTok * 128;  // 64 dims x 32 tokens = 4 KB
-    static constexpr int kStageBytes = 9 * kChunkBytes;        // 8 ckv chunks + kpe = 36 KB
-    static constexpr int kStages = 5;
+    // ring stages, filled by TMA.  bf16 cache: 8 value chunks (64 dims x 32 tokens, 128-byte
+    // swizzle) + the kpe chunk = 36 KB.  e4m3 cache: 4 code chunks (128 dims x 32 tokens, one
+    // byte each, 128-byte swizzle) + kpe (bf16, same layout as above) + 32 fp32 scales = 20.1 KB,
+    // padded to the 1 KB swizzle alignment; the compute warps read the codes directly.
+    static constexpr int kChunkBytes = kNarrowStageTok * 128;  // 4 KB: 32 rows of 128 B
+    static constexpr int kKpeOff = F8 ? 4 * kChunkBytes : 8 * kChunkBytes;
+    static constexpr int kScaleOff = kKpeOff + kChunkBytes;    // e4m3 cache only
+    static constexpr int kStageBytes = F8 ? 21 * 1024 : 9 * kChunkBytes;
+    static constexpr int kStages = F8 ? 9 : 5;
+    static constexpr int kStageLoadBytes = kNarrowStageTok * (F8 ? 512 + 128 + 4 : 1152);
     static constexpr int kPartBytes = 4 * 32 * 16 * 4;         // per group: 4 warps x 32 lanes x 16 floats = 8 KB
-    static constexpr int kPRowBytes = 80;                       // P row: 32 bf16 tokens + 16 B pad (conflict-free ldmatrix)
+    static constexpr int kPRowBytes = 80;                       // P row: 32 16-bit tokens + 16 B pad (conflict-free ldmatrix)
     static constexpr int kGroupScratch = 16 * kPRowBytes + 4 * 16 * 4;   // P tile + per-warp row maxima
     static constexpr int kOffStage = 0;
     static constexpr int kOffPart = kOffStage + kStages * kStageBytes;
     static constexpr int kOffScratch = kOffPart + kGroups * kPartBytes;
     static constexpr int kOffMisc = kOffScratch + kGroups * kGroupScratch;
-    static constexpr int kMiscBytes = 2048;
+    static constexpr int kMiscBytes = 3072;
     static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;
+    static_assert((!F8 || kScaleOff + kNarrowStageTok * 4 <= kStageBytes) && kStageBytes % 1024 == 0, "stage layout");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     // the token-group merge passes one group's O (16 heads x 512 dims fp32) in two halves
     // through the partial-score buffers of both groups
@@ -85,7 +93,7 @@ struct NarrowCfg {
 };
 
 struct NarrowMisc {
-    uint64_t full[5], empty[5];
+    uint64_t full[9], empty[9];
     int abort_flag;
     int merge_flag[2];
     float mrg_max[2][16];
@@ -104,6 +112,13 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                  : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_f16_16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ void mma_bf16_16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
@@ -125,18 +140,39 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// two bf16 (low half first) -> two f16, rounded to nearest (exact for values in the f16
+// normal range, which holds for the query entries of the e4m3 path)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+    return pack_f16(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+}
+
+// two e4m3 codes in the low 16 bits (lower byte first) -> two f16 (lower byte in the low half);
+// exact, every e4m3 value being an f16 value
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<uint16_t>(codes & 0xffffu)));
+    return r;
+}
+
 // Address of the 16-byte unit holding (row, dims 8u..8u+7) of a 64-dim chunk stored as
 // rows of 128 bytes with the 128-byte swizzle (unit index XOR row % 8).
 __device__ __forceinline__ uint32_t sw_unit(uint32_t chunk_base, uint32_t row, uint32_t unit) {
     return chunk_base + row * 128 + ((unit ^ (row & 7)) << 4);
 }
 
-template <int HG>
-__global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
+// F8: the cache's ckv holds e4m3 codes with an fp32 scale per token (tm_ckv then maps the
+// codes as bytes, prm.ckv_scale the scales).
+template <int HG, bool F8>
+__global__ void __launch_bounds__(NarrowCfg<HG, F8>::kThreads, 1)
     mla_decode_narrow_kernel(const __grid_constant__ CUtensorMap tm_ckv, const __grid_constant__ CUtensorMap tm_kpe,
                              const AttnParams prm, const uint16_t* __restrict__ q_nope,
                              const uint16_t* __restrict__ q_pe) {
-    using C = NarrowCfg<HG>;
+    using C = NarrowCfg<HG, F8>;
     static_assert(sizeof(NarrowMisc) <= C::kMiscBytes, "misc region");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -189,35 +225,7 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
         bool new_seg = true;
         int win_base = -(1 << 30), win_page = 0;
         const int32_t* pages = nullptr;
-        TileCursorT<kNarrowTile> pf;
-        bool pf_more = pf.init(prm.segments, seg_begin, seg_end);
-        bool pf_new = true;
-        int pf_win_base = -(1 << 30), pf_win_page = 0;
-        const int32_t* pf_pages = nullptr;
-        auto prefetch_next_tile = [&]() {
-            if (!pf_more) return;
-            if (pf_new) {
-                pf_pages = prm.kv_indices + prm.kv_indptr[pf.sg.b];
-                pf_win_base = -(1 << 30);
-            }
-            const int fp = pf.t0 / P;
-            const int np = (pf.ntok() + P - 1) / P;
-            if (fp + np > pf_win_base + 32) {
-                const int last_page = (pf.sg.t_end - 1) / P;
-                pf_win_base = fp;
-                pf_win_page = (pf_win_base + lane <= last_page) ? pf_pages[pf_win_base + lane] : 0;
-            }
-            const int pg = __shfl_sync(0xffffffffu, pf_win_page, (fp - pf_win_base + lane) & 31);
-            if (lane < np) {
-                // whole pages: a tile's pages may extend past it; prefetching them early is harmless
-                l2_prefetch(prm.ckv + static_cast<size_t>(pg) * P * (kDimCkv * 2), static_cast<uint32_t>(P * kDimCkv * 2));
-                l2_prefetch(prm.kpe + static_cast<size_t>(pg) * P * (kDimKpe * 2), static_cast<uint32_t>(P * kDimKpe * 2));
-            }
-            pf_more = pf.advance(pf_new);
-        };
-        for (int d = 0; d < kNarrowPrefetchTiles; ++d) prefetch_next_tile();
         while (more && ok) {
-            if (kNarrowPrefetchTiles > 0) prefetch_next_tile();
             if (new_seg) {
                 pages = prm.kv_indices + prm.kv_indptr[cur.sg.b];
                 win_base = -(1 << 30);
@@ -236,16 +244,32 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                     win_page = (win_base + lane <= seg_last_page) ? pages[win_base + lane] : 0;
                 }
                 const uint32_t s = scount % C::kStages, use = scount / C::kStages;
+                uint64_t* bar_full = &misc->full[s];
                 if (lane == 0 && use > 0) ok = wait_phase_flag(&misc->empty[s], (use - 1) & 1, &misc->abort_flag, prm.status, 21);
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) break;
                 uint8_t* dst = stage_base + s * C::kStageBytes;
-                if (lane == 0) mbar_arrive_expect_tx(&misc->full[s], static_cast<uint32_t>(nbox * box_rows * 128 * 9));
+                // bytes per token: bf16 ckv + kpe = 1152; e4m3 codes + kpe + scale = 644
+                if (lane == 0)
+                    mbar_arrive_expect_tx(bar_full, static_cast<uint32_t>(nbox * box_rows * (C::kStageLoadBytes / kNarrowStageTok)));
                 if (lane == 0) MLA_TRACE_EVENT(st == 0 ? 0 : 1, tile_idx);
                 for (int bx = 0; bx < nbox; ++bx) {
                     const int t = t_st + bx * box_rows;
                     const int pg = __shfl_sync(0xffffffffu, win_page, (t / P - win_base) & 31);
-                    if (lane == 0) {
+                    if (lane == 0 && F8) {
+                        const int y = pg * P + (t % P);
+                        if (box_rows == kNarrowStageTok) {
+                            // all 4 code chunks (128 dims each) in one 3-D box -> [chunk][row][128 B]
+                            tma_load_3d(dst, &tm_ckv, bar_full, 0, y, 0);
+                        } else {
+                            for (int c = 0; c < 4; ++c)
+                                tma_load_2d(dst + c * (kNarrowStageTok * 128) + bx * box_rows * 128, &tm_ckv, bar_full,
+                                            c * 128, y);
+                        }
+                        tma_load_2d(dst + C::kKpeOff + bx * box_rows * 128, &tm_kpe, bar_full, 0, y);
+                        bulk_load(dst + C::kScaleOff + bx * box_rows * 4, prm.ckv_scale + static_cast<size_t>(y),
+                                  static_cast<uint32_t>(box_rows * 4), bar_full);
+                    } else if (lane == 0) {
                         const int y = pg * P + (t % P);
                         if (box_rows == kNarrowStageTok) {
                             // all 8 ckv chunks in one 3-D box (64 dims, 32 rows, 8 chunks), which lands as
@@ -300,10 +324,18 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
                     const int row = g + ((r & 1) ? 8 : 0);
-                    const int dim = kd + 2 * c4 + ((r & 2) ? 8 : 0);
+                    // fragment k index 2 c4 + {0, 1} (+ 8): the bf16 layout.  e4m3 latent dims: a
+                    // thread's four codes of a 16-dim step are adjacent bytes (4 c4 .. 4 c4 + 3), so
+                    // the step's k order is permuted to match: k 2 c4 + j <-> dim 4 c4 + j and
+                    // k 2 c4 + 8 + j <-> dim 4 c4 + 2 + j
+                    const int dim = (F8 && kd < kDimCkv) ? kd + 4 * c4 + ((r & 2) ? 2 : 0)
+                                                         : kd + 2 * c4 + ((r & 2) ? 8 : 0);
                     const uint16_t* src = dim < kDimCkv ? q_nope + (qrow0 + row) * kDimCkv + dim
                                                         : q_pe + (qrow0 + row) * kDimKpe + (dim - kDimCkv);
                     qa[ks][r] = *reinterpret_cast<const uint32_t*>(src);
+                    // e4m3 cache: the latent part of the score runs on f16 operands (the cache
+                    // expands exactly to f16), the rope part stays bf16
+                    if (F8 && kd < kDimCkv) qa[ks][r] = bf16x2_to_f16x2(qa[ks][r]);
                 }
             }
         };
@@ -323,6 +355,10 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
             for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
             float m_run[2] = {-INFINITY, -INFINITY};   // rows g and g + 8 (log2 domain)
             float l_part[2] = {0.f, 0.f};
+            // e4m3 cache: O accumulates p * (scale_t / r) * code_t with r the largest scale of
+            // this group's first tile of the segment, which keeps the f16 P operand near 1
+            float r_scale = 1.f, inv_r = 1.f;
+            bool first_tile = true;
             int tile_in_seg = 0;
             for (int t0 = sg.t_begin; t0 < sg.t_end; t0 += kNarrowTile, ++tile_in_seg) {
                 const int ntok = min(kNarrowTile, sg.t_end - t0);
@@ -351,28 +387,70 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                 ok = !named_barrier_or(named_bar, 128, !ok || *reinterpret_cast<volatile int*>(&misc->abort_flag));
                 if (!ok) break;
                 if (cw == 0 && lane == 0) MLA_TRACE_EVENT(2, (uint32_t)tile_in_seg);
+                // e4m3 cache: the stage's per-token scales, 0 past the tile's last token (those slots
+                // may hold anything, NaN included)
+                const float* stage_scale = reinterpret_cast<const float*>(stage_base + sl * C::kStageBytes + C::kScaleOff);
+                auto tok_scale = [&](int t) { return t < ntok ? stage_scale[t] : 0.f; };
+                if (F8 && first_tile) {
+                    const float mx = warp_max(tok_scale(lane));
+                    r_scale = mx > 0.f ? mx : 1.f;
+                    inv_r = 1.f / r_scale;
+                }
+                first_tile = false;
                 // ---- partial scores over this warp's 144 dims for the 4 n8 token tiles
-                float sc[4][4];
+                float sc[4][4], sc_pe[4][4];   // sc_pe: the rope dims (e4m3 cache only, warp 3)
 #pragma unroll
-                for (int n = 0; n < 4; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+                for (int n = 0; n < 4; ++n) {
+                    sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+                    sc_pe[n][0] = sc_pe[n][1] = sc_pe[n][2] = sc_pe[n][3] = 0.f;
+                }
 #pragma unroll
                 for (int ks = 0; ks < 9; ++ks) {
                     const int kd = kr * 144 + ks * 16;
-                    const int chunk = kd >> 6;                 // 0..7 ckv, 8 kpe
+                    if (F8 && kd < kDimCkv) {
+                        // e4m3 latent dims: one 16-byte code unit (16 dims) of 32 tokens; matrix j of
+                        // the x4 load is tokens 8j .. 8j + 7, read as 8 x 8 16-bit elements, so each
+                        // thread gets token 8j + g's codes for dims kd + 4 c4 .. + 3
+                        uint32_t rc[4];
+                        ldsm_x4(sw_unit(st_addr + (kd >> 7) * C::kChunkBytes, lane, (kd & 127) >> 4), rc[0], rc[1],
+                                rc[2], rc[3]);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            if (j * 8 < ntok)
+                                mma_f16_16816(sc[j], qa[ks], e4m3x2_to_f16x2(rc[j]), e4m3x2_to_f16x2(rc[j] >> 16));
+                        }
+                        continue;
+                    }
+                    // bf16 16-dim step: latent (bf16 cache) or rope (both caches)
+                    const uint32_t chunk_base = kd < kDimCkv ? st_addr + (kd >> 6) * C::kChunkBytes
+                                                             : st_addr + C::kKpeOff;
                     const int unit0 = (kd & 63) >> 3;          // 16-byte unit of the k-step's first 8 dims
                     uint32_t bf[2][4];
 #pragma unroll
                     for (int np = 0; np < 2; ++np) {           // pairs of n8 tiles = 16 tokens
                         const int tok = np * 16 + (lane & 7) + ((lane & 16) ? 8 : 0);
-                        ldsm_x4(sw_unit(st_addr + chunk * C::kChunkBytes, tok, unit0 + ((lane & 8) ? 1 : 0)),
+                        ldsm_x4(sw_unit(chunk_base, tok, unit0 + ((lane & 8) ? 1 : 0)),
                                 bf[np][0], bf[np][1], bf[np][2], bf[np][3]);
                     }
 #pragma unroll
                     for (int np = 0; np < 2; ++np) {
                         if (np * 16 < ntok) {
-                            mma_bf16_16816(sc[2 * np], qa[ks], bf[np][0], bf[np][1]);
-                            mma_bf16_16816(sc[2 * np + 1], qa[ks], bf[np][2], bf[np][3]);
+                            float* c0 = F8 ? sc_pe[2 * np] : sc[2 * np];
+                            float* c1 = F8 ? sc_pe[2 * np + 1] : sc[2 * np + 1];
+                            mma_bf16_16816(c0, qa[ks], bf[np][0], bf[np][1]);
+                            mma_bf16_16816(c1, qa[ks], bf[np][2], bf[np][3]);
                         }
+                    }
+                }
+                if (F8) {
+                    // latent part times the token's scale, plus the rope part
+#pragma unroll
+                    for (int n = 0; n < 4; ++n) {
+                        const float s0 = tok_scale(8 * n + 2 * c4), s1 = tok_scale(8 * n + 2 * c4 + 1);
+                        sc[n][0] = fmaf(sc[n][0], s0, sc_pe[n][0]);
+                        sc[n][1] = fmaf(sc[n][1], s1, sc_pe[n][1]);
+                        sc[n][2] = fmaf(sc[n][2], s0, sc_pe[n][2]);
+                        sc[n][3] = fmaf(sc[n][3], s1, sc_pe[n][3]);
                     }
                 }
                 // ---- exchange partials within the group; warp kr finishes the scores of n8 tile kr
@@ -381,12 +459,17 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 4; ++i) dst[i * 32 + lane] = make_float4(sc[i][0], sc[i][1], sc[i][2], sc[i][3]);
                 }
-                // zero the value rows of a partial 16-token step (stale or NaN bytes past the last token)
+                // zero the value rows of a partial 16-token step (stale or NaN bytes past the last
+                // token): 8 bf16 chunks or 4 code chunks of 128 B per row
                 if (ntok < kNarrowTile && (ntok & 15)) {
                     const int r_end = (ntok + 15) & ~15;
                     for (int tok = ntok + kr; tok < r_end; tok += 4) {
                         uint4* rowp = reinterpret_cast<uint4*>(stage_base + (st_addr - stage0) + tok * 128);
-                        for (int c = 0; c < 8; ++c) rowp[c * (C::kChunkBytes / 16) + (lane & 7)] = make_uint4(0, 0, 0, 0);
+                        if (F8) {
+                            rowp[(lane >> 3) * (C::kChunkBytes / 16) + (lane & 7)] = make_uint4(0, 0, 0, 0);
+                        } else {
+                            for (int c = 0; c < 8; ++c) rowp[c * (C::kChunkBytes / 16) + (lane & 7)] = make_uint4(0, 0, 0, 0);
+                        }
                     }
                 }
                 named_barrier_sync(named_bar, 128);
@@ -443,8 +526,19 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                     const float p3 = fast_exp2(fmaf(s4[3], prm.scale_log2, -m_run[1]));
                     l_part[0] += p0 + p1;
                     l_part[1] += p2 + p3;
-                    *reinterpret_cast<uint32_t*>(pbuf + g * C::kPRowBytes + (kr * 8 + 2 * c4) * 2) = pack_bf16(p0, p1);
-                    *reinterpret_cast<uint32_t*>(pbuf + (g + 8) * C::kPRowBytes + (kr * 8 + 2 * c4) * 2) = pack_bf16(p2, p3);
+                    uint32_t w0, w1;
+                    if (F8) {
+                        // P operand: p * scale_t / r (f16); the row sums above use p itself
+                        const float s0 = tok_scale(kr * 8 + 2 * c4) * inv_r;
+                        const float s1 = tok_scale(kr * 8 + 2 * c4 + 1) * inv_r;
+                        w0 = pack_f16(p0 * s0, p1 * s1);
+                        w1 = pack_f16(p2 * s0, p3 * s1);
+                    } else {
+                        w0 = pack_bf16(p0, p1);
+                        w1 = pack_bf16(p2, p3);
+                    }
+                    *reinterpret_cast<uint32_t*>(pbuf + g * C::kPRowBytes + (kr * 8 + 2 * c4) * 2) = w0;
+                    *reinterpret_cast<uint32_t*>(pbuf + (g + 8) * C::kPRowBytes + (kr * 8 + 2 * c4) * 2) = w1;
                 }
                 named_barrier_sync(named_bar, 128);
                 uint32_t pa[2][4];   // P as the A operand of the 2 k16 token steps
@@ -460,6 +554,29 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                 for (int kt = 0; kt < 2; ++kt) {
                     if (kt * 16 >= ntok) break;
                     const int tok = kt * 16 + (lane & 7) + ((lane & 8) ? 8 : 0);
+                    if (F8) {
+                        // e4m3 codes of this warp's 128 dims = code chunk kr.  Read as 16-bit elements
+                        // (pairs of dims) with the transposing load: matrix (unit U, token half h)
+                        // gives each thread tokens 2 c4, 2 c4 + 1 of the half and dims 2g, 2g + 1 of
+                        // the unit's 16, split by byte into an even-dim and an odd-dim B fragment.
+                        // O tile 2p holds dims 16p + 2n of the warp's 128, tile 2p + 1 dims 16p + 2n + 1.
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {         // 32 dims: units 2q, 2q + 1
+                            uint32_t r[4];
+                            ldsm_x4_t(sw_unit(st_addr + kr * C::kChunkBytes, tok, 2 * q + ((lane & 16) ? 1 : 0)), r[0],
+                                      r[1], r[2], r[3]);
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {     // unit 2q + h: matrices 2h (tokens 0-7), 2h + 1 (8-15)
+                                const uint32_t lo = r[2 * h], hi = r[2 * h + 1];
+                                const int p = 2 * q + h;
+                                mma_f16_16816(o[2 * p], pa[kt], e4m3x2_to_f16x2(__byte_perm(lo, 0, 0x4420)),
+                                              e4m3x2_to_f16x2(__byte_perm(hi, 0, 0x4420)));
+                                mma_f16_16816(o[2 * p + 1], pa[kt], e4m3x2_to_f16x2(__byte_perm(lo, 0, 0x4431)),
+                                              e4m3x2_to_f16x2(__byte_perm(hi, 0, 0x4431)));
+                            }
+                        }
+                        continue;
+                    }
                     uint32_t vf[8][4];
 #pragma unroll
                     for (int dp = 0; dp < 8; ++dp) {          // pairs of n8 dim tiles = 16 dims
@@ -487,6 +604,15 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
             }
             if (!ok) break;
             if (kr == 0 && lane == 0) MLA_TRACE_CTA(2 + grp);
+            if (F8) {
+#pragma unroll
+                for (int n = 0; n < 16; ++n) {
+                    o[n][0] *= r_scale;
+                    o[n][1] *= r_scale;
+                    o[n][2] *= r_scale;
+                    o[n][3] *= r_scale;
+                }
+            }
             // ---- row sums: quad, then the 4 warps of the group (each summed its own 8 tokens per tile)
             float l[2];
 #pragma unroll
@@ -565,13 +691,28 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                 obase = prm.part_o + (static_cast<size_t>(sg.slot) * prm.h_q + head0) * kDimCkv;
                 lbase = prm.part_lse + static_cast<size_t>(sg.slot) * prm.h_q + head0;
             }
+            if (F8) {
+                // tiles 2p / 2p + 1 hold the even / odd dims of 16-dim block p: this thread's four
+                // values per row are dims 16p + 4 c4 .. + 3 of the warp's 128
 #pragma unroll
-            for (int n = 0; n < 16; ++n) {
-                const int d = kr * 128 + n * 8 + 2 * c4;
-                *reinterpret_cast<float2*>(obase + static_cast<size_t>(g) * kDimCkv + d) =
-                    make_float2(o[n][0] * inv0, o[n][1] * inv0);
-                *reinterpret_cast<float2*>(obase + static_cast<size_t>(g + 8) * kDimCkv + d) =
-                    make_float2(o[n][2] * inv1, o[n][3] * inv1);
+                for (int p = 0; p < 8; ++p) {
+                    const int d = kr * 128 + p * 16 + 4 * c4;
+                    *reinterpret_cast<float4*>(obase + static_cast<size_t>(g) * kDimCkv + d) =
+                        make_float4(o[2 * p][0] * inv0, o[2 * p + 1][0] * inv0, o[2 * p][1] * inv0,
+                                    o[2 * p + 1][1] * inv0);
+                    *reinterpret_cast<float4*>(obase + static_cast<size_t>(g + 8) * kDimCkv + d) =
+                        make_float4(o[2 * p][2] * inv1, o[2 * p + 1][2] * inv1, o[2 * p][3] * inv1,
+                                    o[2 * p + 1][3] * inv1);
+                }
+            } else {
+#pragma unroll
+                for (int n = 0; n < 16; ++n) {
+                    const int d = kr * 128 + n * 8 + 2 * c4;
+                    *reinterpret_cast<float2*>(obase + static_cast<size_t>(g) * kDimCkv + d) =
+                        make_float2(o[n][0] * inv0, o[n][1] * inv0);
+                    *reinterpret_cast<float2*>(obase + static_cast<size_t>(g + 8) * kDimCkv + d) =
+                        make_float2(o[n][2] * inv1, o[n][3] * inv1);
+                }
             }
             if (kr == 0 && c4 == 0) {
                 lbase[g] = (m_run[0] + log2f(l[0])) * 0.69314718055994530942f;

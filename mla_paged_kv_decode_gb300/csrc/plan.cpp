@@ -40,6 +40,7 @@ int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int ba
     if (page_size != 16 && page_size != 32 && page_size != 64) return 2;
     const int hg = heads_per_cta_for(h_q, kv_dtype);
     if (hg == 0) return 2;
+    if (kv_dtype == 1 && h_q > 32) return 2;   // the e4m3 cache is served by the narrow-head kernel only
     if (kv_indptr[0] != 0) return 1;
 
     const bool narrow = h_q <= 32;

@@ -97,3 +97,23 @@ def test_run_and_commit_reject_bad_arguments_without_touching_a_gpu(lib):
     assert rc == mla.MLA_ERR_INVALID_ARG
     assert lib.mla_decode_plan_workspace_bytes(None) == 0
     assert lib.mla_plan_num_ctas(None) == 0
+
+
+def test_fp8_plan_and_run_checks(lib):
+    # the e4m3 cache is served for 16 and 32 heads; 64/128 heads are refused at plan time
+    assert _plan_rc([0, 1], [5], 1, h_q=16, dtype=mla.MLA_KV_FP8_E4M3) == mla.MLA_OK
+    assert _plan_rc([0, 1], [5], 1, h_q=32, dtype=mla.MLA_KV_FP8_E4M3) == mla.MLA_OK
+    assert _plan_rc([0, 1], [5], 1, h_q=64, dtype=mla.MLA_KV_FP8_E4M3) == mla.MLA_ERR_UNSUPPORTED
+    assert _plan_rc([0, 1], [5], 1, h_q=128, dtype=mla.MLA_KV_FP8_E4M3) == mla.MLA_ERR_UNSUPPORTED
+    vp = ctypes.c_void_p
+    fake = vp(1 << 20)
+    plan = mla.mla_decode_plan(torch.tensor([0, 2]), torch.tensor([7]), 1, 16, 16, 152, mla.MLA_KV_FP8_E4M3)
+    # an 8-bit plan needs the scales, 16-byte aligned; a bf16 plan must not get any
+    for scale in (None, vp((1 << 20) + 4)):
+        rc = lib.mla_decode_run(plan.handle, fake, fake, fake, scale, fake, 4, fake, fake, fake, ctypes.c_float(0.1),
+                                fake, fake, vp(1 << 21), None)
+        assert rc == mla.MLA_ERR_INVALID_ARG
+    plan16 = mla.mla_decode_plan(torch.tensor([0, 2]), torch.tensor([7]), 1, 16, 16, 152)
+    rc = lib.mla_decode_run(plan16.handle, fake, fake, fake, fake, fake, 4, fake, fake, fake, ctypes.c_float(0.1),
+                            fake, fake, vp(1 << 21), None)
+    assert rc == mla.MLA_ERR_INVALID_ARG

@@ -1,0 +1,128 @@
+"""Parity of the 8-bit (e4m3 + per-token fp32 scale) cache path with the fp64 oracle.
+
+Two references, as the 8-bit cache is an approximation of the bf16 one (FlashMLA
+PR #233, "Correctness": worst cosine distance 2.4e-3 for FP8 on synthetic caches):
+
+* the oracle on the dequantised cache (scale_t * e4m3(code)), held to the bf16
+  tolerances: this checks the kernel's arithmetic;
+* the oracle on the original bf16 cache, cosine distance <= 3e-3: this checks the
+  quantisation end to end.
+
+Cases: ragged lengths over page sizes 16/32/64 and 16/32 heads, splits over 1, 3
+and every SM, reruns (bit-identical), a request whose tokens span six orders of
+magnitude (the per-token scale must not underflow or overflow the kernel's f16
+operands), NaN codes and scales in every unused slot, and the full-size 8-bit
+workload on sampled requests.
+"""
+import pytest
+import torch
+
+import mla_paged_kv_decode_gb300 as mla
+import oracle
+from gpu_helpers import COS_DIST_FP8, assert_parity, cos_dist, oracle_subset, run_gpu
+from workloads import WORKLOADS, make_inputs, quantize_e4m3_per_token
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mla_paged_kv_decode_gb300 import build as lib_build
+    if lib_build.needs_build():
+        lib_build.build()
+    mla.load()
+
+
+def _small_fp8(kv_lens, H, P, seed, pool=None):
+    return make_inputs(WORKLOADS["tiny"], kv_lens=list(kv_lens), batch=len(kv_lens), h_q=H, page_size=P,
+                       pool_pages=pool, seed=seed, fp8=True)
+
+
+def _check_both(inp, out, lse, requests=None):
+    """Dequantised-cache oracle at bf16 tolerances; bf16-cache oracle by cosine distance."""
+    if requests is None:
+        ref = oracle.decode_inputs(inp)
+        ref16 = oracle.decode_inputs(inp, use_bf16_cache=True)
+        o, l = out, lse
+    else:
+        ref = oracle_subset(inp, requests)
+        ref16 = oracle_subset(inp, requests, use_bf16_cache=True)
+        idx = torch.tensor(requests)
+        o, l = out[idx], lse[idx]
+    assert_parity(o, l, *ref)
+    cd = cos_dist(o.double(), ref16[0])
+    assert cd <= COS_DIST_FP8, f"cosine distance to the bf16-cache oracle {cd:.3e}"
+
+
+@pytest.mark.parametrize("H", [16, 32])
+@pytest.mark.parametrize("P", [16, 32, 64])
+def test_fp8_small_ragged(H, P):
+    lens = [1, 17, P, P + 1, 127, 128, 129, 300, 1000, 2049]
+    inp = _small_fp8(lens, H, P, seed=20 + H + P)
+    assert inp.ckv.dtype == torch.uint8 and inp.ckv_scale is not None
+    out, lse, _, _ = run_gpu(inp)
+    _check_both(inp, out, lse)
+
+
+def test_fp8_tiny_workload():
+    inp = make_inputs(WORKLOADS["tiny"], fp8=True)
+    out, lse, _, _ = run_gpu(inp)
+    _check_both(inp, out, lse)
+
+
+@pytest.mark.parametrize("sms", [1, 3, 152])
+def test_fp8_split_patterns(sms):
+    inp = _small_fp8([3000, 5, 700, 4096, 129], 16, 64, seed=31)
+    out, lse, _, _ = run_gpu(inp, sms=sms)
+    _check_both(inp, out, lse)
+
+
+def test_fp8_reruns_are_bit_identical():
+    inp = _small_fp8([2500, 40, 900], 16, 32, seed=32)
+    out0, lse0, dec, d = run_gpu(inp)
+    for _ in range(3):
+        o, l = dec.run(d.q_nope, d.q_pe, d.ckv, d.kpe, d.kv_indices, d.kv_indptr, d.kv_last_page_len, inp.sm_scale,
+                       ckv_scale=d.ckv_scale)
+        torch.cuda.synchronize()
+        assert torch.equal(o.cpu(), out0) and torch.equal(l.cpu(), lse0)
+
+
+def test_fp8_scale_extremes():
+    """Tokens of one request scaled by 1e-3 .. 1e3 before quantisation: the kernel keeps
+    P * scale / r in f16 with r the first tile's largest scale, so this spans both ends."""
+    inp = _small_fp8([1500, 700], 16, 64, seed=33)
+    g = torch.Generator().manual_seed(5)
+    fin = torch.nan_to_num(inp.ckv_bf16.float(), nan=0.0)
+    mag = 10.0 ** (torch.randint(-3, 4, (fin.shape[0], fin.shape[1], 1), generator=g).float())
+    scaled = (fin * mag).to(torch.bfloat16)
+    codes, scale = quantize_e4m3_per_token(scaled)
+    bad = ~torch.isfinite(inp.ckv_scale)
+    codes[bad] = 0x7F
+    scale[bad] = float("nan")
+    inp.ckv_bf16 = scaled
+    inp.ckv = codes
+    inp.ckv_scale = scale
+    out, lse, _, _ = run_gpu(inp)
+    assert torch.isfinite(out).all() and torch.isfinite(lse).all()
+    ref_out, ref_lse = oracle.decode_inputs(inp)
+    # outputs and scores here reach ~1e3 and ~1e4: the bf16 tolerances, taken relative to each
+    # request's largest output and to |lse|.  Only the dequantised-cache oracle applies: with
+    # scores this large the e4m3 rounding of the cache (3 mantissa bits) moves the softmax
+    # itself, so the distance to the bf16 cache measures the data, not the kernel.
+    for b in range(inp.batch):
+        o = out[b].double()
+        scale_b = max(1.0, float(ref_out[b].abs().max()))
+        err = float((o - ref_out[b]).abs().max())
+        assert err <= 2e-2 * scale_b, (b, err, scale_b)
+        assert cos_dist(o, ref_out[b]) <= 1e-4
+        lerr = float((lse[b].double() - ref_lse[b]).abs().max())
+        assert lerr <= 1e-3 + 2e-6 * float(ref_lse[b].abs().max()), (b, lerr)
+
+
+def test_fp8_full_size_sampled():
+    inp = make_inputs(WORKLOADS["fp8"])
+    out, lse, _, _ = run_gpu(inp)
+    assert torch.isfinite(out).all() and torch.isfinite(lse).all()
+    _check_both(inp, out, lse, requests=[0, 31, 63])
