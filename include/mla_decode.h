@@ -145,6 +145,7 @@ mla_status_t mla_decode_device_status(mla_plan_t plan, void* workspace_dev, void
 
 /* Introspection (host only, for tests and tools). */
 int mla_plan_num_ctas(mla_plan_t plan);       /* attention CTAs launched per run */
+int mla_plan_num_units(mla_plan_t plan);      /* work units (CTA slots, or CTA pairs for 128 heads) */
 int mla_plan_num_segments(mla_plan_t plan);   /* (request, token range) pieces */
 int mla_plan_num_partials(mla_plan_t plan);   /* split pieces that go through the combine */
 int mla_plan_heads_per_cta(mla_plan_t plan);

@@ -18,7 +18,7 @@ from ._binding import (  # noqa: F401
     mla_decode_plan_workspace_bytes, mla_decode_run, mla_plan_get_segments, mla_plan_heads_per_cta,
     mla_plan_num_ctas, mla_plan_num_partials, mla_plan_num_segments, mla_status_string,
     mla_plan_num_launches, mla_decode_run_noalloc, mla_decode_noalloc_max_workspace_bytes,
-    mla_plan_segment_cost_tiles,
+    mla_plan_segment_cost_tiles, mla_plan_num_units,
 )
 
 

@@ -32,7 +32,7 @@ EXPORTED = (
     "mla_decode_device_status", "mla_plan_num_ctas", "mla_plan_num_segments", "mla_plan_num_partials",
     "mla_plan_heads_per_cta", "mla_plan_get_segments", "mla_plan_destroy", "mla_status_string",
     "mla_plan_num_launches", "mla_decode_run_noalloc", "mla_decode_noalloc_max_workspace_bytes",
-    "mla_plan_segment_cost_tiles",
+    "mla_plan_segment_cost_tiles", "mla_plan_num_units",
 )
 
 _lib = None
@@ -79,7 +79,7 @@ def load(path: Optional[str] = None):
     lib.mla_decode_device_status.restype = ctypes.c_int
     lib.mla_decode_device_status.argtypes = [vp, vp, vp]
     for name in ("mla_plan_num_ctas", "mla_plan_num_segments", "mla_plan_num_partials", "mla_plan_heads_per_cta",
-                 "mla_plan_segment_cost_tiles"):
+                 "mla_plan_segment_cost_tiles", "mla_plan_num_units"):
         getattr(lib, name).restype = ctypes.c_int
         getattr(lib, name).argtypes = [vp]
     lib.mla_plan_get_segments.restype = ctypes.c_int
@@ -202,6 +202,10 @@ def mla_plan_heads_per_cta(plan: Plan) -> int:
     return int(load().mla_plan_heads_per_cta(plan.handle))
 
 
+def mla_plan_num_units(plan: Plan) -> int:
+    return int(load().mla_plan_num_units(plan.handle))
+
+
 def mla_plan_segment_cost_tiles(plan: Plan) -> int:
     return int(load().mla_plan_segment_cost_tiles(plan.handle))
 
@@ -210,7 +214,7 @@ def mla_plan_get_segments(plan: Plan):
     """-> (segments int32 [n, 4] = (request, token_begin, token_end, slot), unit_ptr int32 [units + 1])"""
     lib = load()
     n = lib.mla_plan_num_segments(plan.handle)
-    units = lib.mla_plan_num_ctas(plan.handle) // max(1, plan.h_q // lib.mla_plan_heads_per_cta(plan.handle))
+    units = lib.mla_plan_num_units(plan.handle)
     seg = np.zeros((max(n, 1), 4), dtype=np.int32)
     uptr = np.zeros(units + 1, dtype=np.int32)
     lib.mla_plan_get_segments(plan.handle, seg.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),

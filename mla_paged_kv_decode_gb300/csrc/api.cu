@@ -14,6 +14,7 @@
 #include "mla_decode.h"
 #include "attn.cuh"
 #include "attn_narrow.cuh"
+#include "attn_pair.cuh"
 #include "plan.h"
 
 // Tensor maps of the last run's buffers (re-encoded when an address changes).
@@ -21,7 +22,7 @@ struct MapCache {
     bool valid = false;
     const void *ckv = nullptr, *kpe = nullptr, *qn = nullptr, *qp = nullptr;
     int num_pages = 0;
-    CUtensorMap m_ckv, m_kpe, m_qn, m_qp;
+    CUtensorMap m_ckv, m_kpe, m_qn, m_qp, m_v;
 };
 
 struct mla_plan_s {
@@ -78,6 +79,21 @@ bool make_map_ckv_chunked(CUtensorMap* map, const void* base, uint64_t rows, uin
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Value view of the ckv cache for the 128-head kernel: dims (64 dims, rows, 8 chunks) with
+// strides (2 B, 1024 B, 128 B); a box (64, box_rows, 4) copies box_rows rows of 256 dims as
+// [4 chunks][box_rows][128 B] with the 128-byte swizzle (the MN-major value operand).
+bool make_map_v_half(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {64, rows, 8};
+    cuuint64_t strides[2] = {mla::kDimCkv * 2, 128};
+    cuuint32_t box[3] = {64, box_rows, 4};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // e4m3 codes of the ckv cache ([rows, 512] bytes) for the narrow kernel: with whole 32-token
 // stages a 3-D view (128 code columns, rows, 4 chunks; strides 512 B, 128 B) whose box lands
 // as [chunk][row][128 B]; otherwise a 2-D view with 128-column boxes, one per chunk.  Both
@@ -126,6 +142,18 @@ cudaError_t launch_narrow(const mla_plan_s* p, const CUtensorMap& ckv, const CUt
     return cudaGetLastError();
 }
 
+cudaError_t launch_pair(const mla_plan_s* p, const MapCache& mc, const mla::AttnParams& prm, const void* q_nope,
+                        cudaStream_t stream) {
+    using C = mla::PairCfg;
+    cudaError_t e = cudaFuncSetAttribute(mla::mla_decode_pair_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int grid = 2 * p->d.num_units;   // clusters of two CTAs (the kernel's cluster dimensions)
+    mla::mla_decode_pair_kernel<0><<<grid, C::kThreads, C::kSmemBytes, stream>>>(
+        mc.m_ckv, mc.m_kpe, mc.m_qp, mc.m_v, prm, static_cast<const uint16_t*>(q_nope));
+    return cudaGetLastError();
+}
+
 template <int HG>
 cudaError_t launch_attention(const mla_plan_s* p, const CUtensorMap& ckv, const CUtensorMap& kpe,
                              const CUtensorMap& qn, const CUtensorMap& qp, const mla::AttnParams& prm,
@@ -168,7 +196,8 @@ mla_status_t run_checked(mla_plan_t plan, const void* q_nope, const void* q_pe, 
                              : make_map_bf16(&mc.m_ckv, ckv_cache, mla::kDimCkv, rows, box);
         mc.valid = ok_ckv && make_map_bf16(&mc.m_kpe, kpe_cache, mla::kDimKpe, rows, box) &&
                    make_map_bf16(&mc.m_qn, q_nope, mla::kDimCkv, qrows, hg) &&
-                   make_map_bf16(&mc.m_qp, q_pe, mla::kDimKpe, qrows, hg);
+                   make_map_bf16(&mc.m_qp, q_pe, mla::kDimKpe, qrows, hg) &&
+                   (!d.pair || make_map_v_half(&mc.m_v, ckv_cache, rows, std::min(d.page_size, 32)));
         if (!mc.valid) return MLA_ERR_CUDA;
         mc.ckv = ckv_cache;
         mc.kpe = kpe_cache;
@@ -203,6 +232,8 @@ mla_status_t run_checked(mla_plan_t plan, const void* q_nope, const void* q_pe, 
         else
             e = d.h_q == 16 ? launch_narrow<16, false>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream)
                             : launch_narrow<32, false>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream);
+    } else if (d.pair) {
+        e = launch_pair(plan, mc, prm, q_nope, stream);
     } else {
         e = launch_attention<32>(plan, mc.m_ckv, mc.m_kpe, mc.m_qn, mc.m_qp, prm, stream);
     }
@@ -312,7 +343,10 @@ mla_status_t mla_decode_device_status(mla_plan_t plan, void* workspace_dev, void
     return MLA_ERR_DEVICE_TIMEOUT;
 }
 
-int mla_plan_num_ctas(mla_plan_t plan) { return plan ? plan->d.num_units * plan->d.head_groups : 0; }
+int mla_plan_num_ctas(mla_plan_t plan) {
+    return plan ? plan->d.num_units * plan->d.head_groups * (plan->d.pair ? 2 : 1) : 0;
+}
+int mla_plan_num_units(mla_plan_t plan) { return plan ? plan->d.num_units : 0; }
 int mla_plan_num_segments(mla_plan_t plan) { return plan ? static_cast<int>(plan->d.segments.size()) : 0; }
 int mla_plan_num_partials(mla_plan_t plan) { return plan ? plan->d.num_partials : 0; }
 int mla_plan_heads_per_cta(mla_plan_t plan) { return plan ? plan->d.heads_per_cta : 0; }

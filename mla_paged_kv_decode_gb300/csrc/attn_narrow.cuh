@@ -575,8 +575,7 @@ __global__ void __launch_bounds__(NarrowCfg<HG, F8>::kThreads, 1)
                                               e4m3x2_to_f16x2(__byte_perm(hi, 0, 0x4431)));
                             }
                         }
-                        continue;
-                    }
+                    } else {
                     uint32_t vf[8][4];
 #pragma unroll
                     for (int dp = 0; dp < 8; ++dp) {          // pairs of n8 dim tiles = 16 dims
@@ -589,6 +588,7 @@ __global__ void __launch_bounds__(NarrowCfg<HG, F8>::kThreads, 1)
                     for (int dp = 0; dp < 8; ++dp) {
                         mma_bf16_16816(o[2 * dp], pa[kt], vf[dp][0], vf[dp][1]);
                         mma_bf16_16816(o[2 * dp + 1], pa[kt], vf[dp][2], vf[dp][3]);
+                    }
                     }
                 }
                 __syncwarp();

@@ -1,0 +1,659 @@
+// MLA paged decode attention for 128 query heads on sm_103a: a cluster of two CTAs per
+// work unit, tcgen05 MMAs with M = 128 heads.
+//
+// Absorbed MLA decode is MQA with one KV head: key [ckv | kpe] (576), value ckv (512)
+// ("Benchmarking MLA", FlashInfer issue #700).  With the heads on the MMA's M axis every
+// softmax row is one TMEM lane, so each softmax thread owns one head and needs no
+// cross-thread reduction -- but S (128 heads x 128 tokens fp32) and O (128 heads x 512
+// dims fp32) together need 640 TMEM columns and an SM has 512.  The two CTAs of a cluster
+// therefore split the work by role:
+//
+//   rank 0 ("S CTA"):  q_nope sits in TMEM (256 columns, the A operand), q_pe in shared
+//     memory; S = Q K^T is accumulated into one of two 128-column TMEM buffers by
+//     36 MMAs (M 128, N 128, K 16) per 128-token tile from a ring of 16 KB K chunks.
+//     The softmax warpgroup (thread = head) reads S, keeps the running max and sum, and
+//     writes P (bf16) and the rescale factors into rank 1's shared memory.
+//   rank 1 ("O CTA"):  O (128 x 512 fp32) fills its TMEM; O += P V is 16 MMAs (M 128,
+//     N 256, K 16) per tile, V streamed as [4 dim chunks][32 tokens] slots.  A correction
+//     warpgroup rescales O rows when rank 0 raised a head's running max (lazily, by more
+//     than 2^8), zeroes value rows past the last token of a partial tile, and writes the
+//     normalised output (or a split piece's partial) at the end of a segment.
+//
+// The split-KV partition, the partials and the last-arriver merge are those of the other
+// kernels (FlashMLA PR #233, "balanced scheduler, deterministic combine").  Every wait is
+// bounded; a wait that runs out raises the abort flag of both CTAs.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "attn.cuh"
+#include "plan.h"
+#include "ptx.cuh"
+
+namespace mla {
+
+struct PairCfg {
+    static constexpr int kThreads = 256;          // 8 warps: producer, MMA, 2 idle, one warpgroup (4-7)
+    static constexpr int kTile = kTileTokens;     // 128 tokens
+    static constexpr int kChunkBytes = 128 * 128; // 128 rows x 128 B (64 bf16)
+    // rank 0
+    static constexpr int kKSlots = 12;
+    static constexpr int kOffQpe = 0;                                  // [128 heads][128 B] SW128
+    static constexpr int kOffK = kOffQpe + kChunkBytes;                // K ring
+    static constexpr int kSEnd = kOffK + kKSlots * kChunkBytes;        // 208 KB
+    // rank 1
+    static constexpr int kPBufBytes = 2 * kChunkBytes;                 // [2 token chunks][128 heads][128 B]
+    static constexpr int kOffP = 0;
+    static constexpr int kVSlotBytes = 4 * 32 * 128;                   // [boxes][4 dim chunks][rows][128 B] = 32 tokens x 256 dims
+    static constexpr int kVSlots = 9;
+    static constexpr int kOffV = kOffP + 2 * kPBufBytes;
+    static constexpr int kOEnd = kOffV + kVSlots * kVSlotBytes;        // 208 KB
+    static constexpr int kOffMisc = kSEnd > kOEnd ? kSEnd : kOEnd;
+    static constexpr int kMiscBytes = 12 * 1024;
+    static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+    static constexpr uint32_t kTmemQ = 0;      // rank 0: q_nope, 256 columns
+    static constexpr uint32_t kTmemS = 256;    // rank 0: S buffers at 256, 384
+    static constexpr uint32_t kIdescS = idesc_bf16(128, 128, false, false);
+    static constexpr uint32_t kIdescPV = idesc_bf16(128, 256, false, true);
+};
+
+// Same layout in both CTAs, so mapa_shared of a field's address reaches the partner's copy.
+struct PairMisc {
+    // rank 0
+    uint64_t k_full[PairCfg::kKSlots], k_empty[PairCfg::kKSlots];
+    uint64_t s_full[2], s_empty[2];
+    uint64_t q_full, q_empty;
+    uint64_t p_empty[2];
+    // rank 1
+    uint64_t v_full[PairCfg::kVSlots], v_empty[PairCfg::kVSlots];
+    uint64_t p_full[2];
+    uint64_t pv_done[2];
+    uint64_t corr_done, vz_done, epi_done;
+    uint32_t tmem_base;
+    int abort_flag;
+    int merge_flag;
+    int rescale[2];                 // written by rank 0 per P buffer: some head's max moved
+    float alpha[2][128];            // ... the factor for each head (1 if unchanged)
+    float fin_m[2][128];            // ... at a segment's last tile: running max (log2 units)
+    float fin_l[2][128];            // ... and row sum
+    float mrg_max[128], mrg_inv[128], mrg_w[8 * 128];
+};
+
+// Debug builds (-DMLA_TRACE): each role's progress counter, readable by the host while the
+// kernel runs when the trace buffer is mapped host memory.
+#ifdef MLA_TRACE
+#define PAIR_PROGRESS(k, v)                                                                                    \
+    do {                                                                                                      \
+        if (prm.trace)                                                                                        \
+            reinterpret_cast<volatile uint64_t*>(prm.trace)[4 * 8 * 256 + blockIdx.x * 8 + (k)] = (uint64_t)(v); \
+    } while (0)
+#else
+#define PAIR_PROGRESS(k, v) \
+    do {                    \
+    } while (0)
+#endif
+
+// Bounded wait on a local mbarrier phase with cluster-scope acquire.  On a timeout it raises
+// both CTAs' abort flags and records `site`.
+__device__ __forceinline__ bool pair_wait(uint64_t* bar, uint32_t parity, PairMisc* misc, uint32_t partner_abort,
+                                          uint32_t* status, uint32_t site) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (*reinterpret_cast<volatile int*>(&misc->abort_flag)) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            *reinterpret_cast<volatile int*>(&misc->abort_flag) = 1;
+            st_cluster_u32(partner_abort, 1u);
+            atomicCAS(status, 0u, kStatusTimeout | site);
+            return false;
+        }
+    }
+}
+
+template <int DUMMY = 0>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1)
+    mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tm_ckv, const __grid_constant__ CUtensorMap tm_kpe,
+                           const __grid_constant__ CUtensorMap tm_qpe, const __grid_constant__ CUtensorMap tm_v,
+                           const AttnParams prm, const uint16_t* __restrict__ q_nope) {
+    using C = PairCfg;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    PairMisc* misc = reinterpret_cast<PairMisc*>(smem + C::kOffMisc);
+    static_assert(sizeof(PairMisc) <= C::kMiscBytes, "misc region");
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t partner = rank ^ 1u;
+    const int unit = blockIdx.x / 2;
+    const int seg_begin = prm.unit_ptr[unit];
+    const int seg_end = prm.unit_ptr[unit + 1];
+    const int P = prm.page_size;
+    const uint32_t partner_abort = mapa_shared(smem_u32(&misc->abort_flag), partner);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::kKSlots; ++i) {
+            mbar_init(&misc->k_full[i], 1);
+            mbar_init(&misc->k_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&misc->s_full[i], 1);
+            mbar_init(&misc->s_empty[i], 4);
+            mbar_init(&misc->p_empty[i], 1);
+            mbar_init(&misc->p_full[i], 128);
+            mbar_init(&misc->pv_done[i], 1);
+        }
+        mbar_init(&misc->q_full, 2);
+        mbar_init(&misc->q_empty, 1);
+        for (int i = 0; i < C::kVSlots; ++i) {
+            mbar_init(&misc->v_full[i], 1);
+            mbar_init(&misc->v_empty[i], 1);
+        }
+        mbar_init(&misc->corr_done, 1);
+        mbar_init(&misc->vz_done, 1);
+        mbar_init(&misc->epi_done, 1);
+        misc->abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&misc->tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();   // both CTAs' barriers exist before any remote arrive
+    tc_fence_after();
+    const uint32_t tmem = misc->tmem_base;
+    auto aborted = [&]() { return *reinterpret_cast<volatile int*>(&misc->abort_flag) != 0; };
+
+    if (rank == 0) {
+        // ================================================================== S CTA
+        if (warp == 0) {
+            // ---------------------------------------------------------- TMA producer: q_pe, K chunks
+            if (lane == 0) {
+                prefetch_tensormap(&tm_ckv);
+                prefetch_tensormap(&tm_kpe);
+                prefetch_tensormap(&tm_qpe);
+            }
+            uint32_t kcount = 0, segc = 0;
+            bool ok = true;
+            TileCursorT<C::kTile> cur;
+            bool more = cur.init(prm.segments, seg_begin, seg_end);
+            bool new_seg = true;
+            int win_base = -(1 << 30), win_page = 0;
+            const int32_t* pages = nullptr;
+            while (more && ok) {
+                if (new_seg) {
+                    if (lane == 0 && segc > 0)
+                        ok = pair_wait(&misc->q_empty, (segc - 1) & 1, misc, partner_abort, prm.status, 41);
+                    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                    if (!ok) break;
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&misc->q_full, 128 * 128);
+                        tma_load_2d(smem + C::kOffQpe, &tm_qpe, &misc->q_full, 0, cur.sg.b * 128);
+                    }
+                    ++segc;
+                    pages = prm.kv_indices + prm.kv_indptr[cur.sg.b];
+                    win_base = -(1 << 30);
+                }
+                const int ntok = cur.ntok();
+                const int nbox = (ntok + P - 1) / P;
+                const int first_page = cur.t0 / P;
+                if (first_page + nbox > win_base + 32 || first_page < win_base) {
+                    const int seg_last_page = (cur.sg.t_end - 1) / P;
+                    win_base = first_page;
+                    win_page = (win_base + lane <= seg_last_page) ? pages[win_base + lane] : 0;
+                }
+                for (int c = 0; c < 9 && ok; ++c) {   // 8 ckv chunks of 64 dims, then kpe
+                    const uint32_t s = kcount % C::kKSlots, use = kcount / C::kKSlots;
+                    if (lane == 0 && use > 0)
+                        ok = pair_wait(&misc->k_empty[s], (use - 1) & 1, misc, partner_abort, prm.status, 42);
+                    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                    if (!ok) break;
+                    uint8_t* dst = smem + C::kOffK + s * C::kChunkBytes;
+                    if (lane == 0) mbar_arrive_expect_tx(&misc->k_full[s], static_cast<uint32_t>(nbox * P * 128));
+                    for (int bx = 0; bx < nbox; ++bx) {
+                        const int pg = __shfl_sync(0xffffffffu, win_page, (first_page + bx - win_base) & 31);
+                        if (lane == 0) {
+                            if (c < 8)
+                                tma_load_2d(dst + bx * P * 128, &tm_ckv, &misc->k_full[s], c * 64, pg * P);
+                            else
+                                tma_load_2d(dst + bx * P * 128, &tm_kpe, &misc->k_full[s], 0, pg * P);
+                        }
+                    }
+                    ++kcount;
+                }
+                if (lane == 0) PAIR_PROGRESS(0, kcount);
+                more = cur.advance(new_seg);
+            }
+            if (lane == 0) {   // let every copy land before the CTA can exit
+                const uint64_t t0 = global_timer_ns();
+                for (int s = 0; s < C::kKSlots; ++s) {
+                    const uint32_t uses = kcount / C::kKSlots + (static_cast<uint32_t>(s) < kcount % C::kKSlots ? 1 : 0);
+                    if (uses == 0) continue;
+                    while (!mbar_try_wait(&misc->k_full[s], (uses - 1) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {}
+                }
+            }
+        } else if (warp == 1) {
+            // ---------------------------------------------------------- MMA issuer: S = Q K^T
+            if (lane == 0) {
+                uint32_t tcount = 0, kcount = 0, segc = 0;
+                bool ok = true;
+                TileCursorT<C::kTile> cur;
+                bool more = cur.init(prm.segments, seg_begin, seg_end);
+                bool new_seg = true;
+                const uint32_t qpe = smem_u32(smem + C::kOffQpe);
+                const uint32_t kbase = smem_u32(smem + C::kOffK);
+                while (more && ok) {
+                    const bool last = cur.last();
+                    if (new_seg) {
+                        ok = pair_wait(&misc->q_full, segc & 1, misc, partner_abort, prm.status, 43);
+                        ++segc;
+                    }
+                    const uint32_t buf = tcount & 1, ub = tcount >> 1;
+                    if (ok && ub > 0) ok = pair_wait(&misc->s_empty[buf], (ub - 1) & 1, misc, partner_abort, prm.status, 44);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t d = tmem + C::kTmemS + buf * 128;
+                    for (int c = 0; c < 9 && ok; ++c) {
+                        const uint32_t s = kcount % C::kKSlots;
+                        ok = pair_wait(&misc->k_full[s], (kcount / C::kKSlots) & 1, misc, partner_abort, prm.status, 45);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint32_t kb = kbase + s * C::kChunkBytes;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint64_t bd = umma_desc_sw128(kb + k * 32, 16, 1024);
+                            if (c < 8)
+                                umma_bf16_ts(d, tmem + C::kTmemQ + c * 32 + k * 8, bd, C::kIdescS, (c | k) != 0);
+                            else
+                                umma_bf16(d, umma_desc_sw128(qpe + k * 32, 16, 1024), bd, C::kIdescS, 1);
+                        }
+                        umma_commit(&misc->k_empty[s]);
+                        ++kcount;
+                    }
+                    if (!ok) break;
+                    umma_commit(&misc->s_full[buf]);
+                    if (last) umma_commit(&misc->q_empty);
+                    ++tcount;
+                    PAIR_PROGRESS(1, tcount);
+                    more = cur.advance(new_seg);
+                }
+            }
+        } else if (warp >= 4) {
+            // ---------------------------------------------------------- softmax warpgroup: thread = head
+            const int h = threadIdx.x - 128;
+            const uint32_t lane_base = static_cast<uint32_t>(warp - 4) * 32;
+            const uint32_t o_p = mapa_shared(smem_u32(smem + C::kOffP), partner);
+            const uint32_t o_pfull = mapa_shared(smem_u32(&misc->p_full[0]), partner);
+            const uint32_t o_alpha = mapa_shared(smem_u32(&misc->alpha[0][0]), partner);
+            const uint32_t o_finm = mapa_shared(smem_u32(&misc->fin_m[0][0]), partner);
+            const uint32_t o_finl = mapa_shared(smem_u32(&misc->fin_l[0][0]), partner);
+            const uint32_t o_resc = mapa_shared(smem_u32(&misc->rescale[0]), partner);
+            uint32_t tcount = 0, segc = 0;
+            bool ok = true;
+            for (int si = seg_begin; si < seg_end && ok; ++si) {
+                const Segment sg = prm.segments[si];
+                if (sg.t_end <= sg.t_begin) continue;
+                // q_nope row of head h -> TMEM columns [0, 256) of lane h, once the previous
+                // segment's score MMAs are done with it
+                if (segc > 0) ok = pair_wait(&misc->q_empty, (segc - 1) & 1, misc, partner_abort, prm.status, 46);
+                ok = !named_barrier_or(1, 128, !ok);
+                if (!ok) break;
+                {
+                    const uint4* qrow =
+                        reinterpret_cast<const uint4*>(q_nope + (static_cast<size_t>(sg.b) * 128 + h) * kDimCkv);
+#pragma unroll 1
+                    for (int c0 = 0; c0 < 256; c0 += 32) {
+                        uint32_t r[32];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const uint4 v = qrow[c0 / 4 + j];
+                            r[4 * j] = v.x;
+                            r[4 * j + 1] = v.y;
+                            r[4 * j + 2] = v.z;
+                            r[4 * j + 3] = v.w;
+                        }
+                        tmem_st32(tmem_addr(tmem, lane_base, C::kTmemQ + c0), r);
+                    }
+                    tmem_wait_st();
+                }
+                tc_fence_before();
+                named_barrier_sync(1, 128);
+                if (h == 0) mbar_arrive(&misc->q_full);
+                ++segc;
+                float m_run = -INFINITY, l = 0.f;
+                bool first = true;
+                for (int t0 = sg.t_begin; t0 < sg.t_end && ok; t0 += C::kTile) {
+                    const int ntok = min(C::kTile, sg.t_end - t0);
+                    const bool last = t0 + C::kTile >= sg.t_end;
+                    const uint32_t buf = tcount & 1, ub = tcount >> 1;
+                    ok = pair_wait(&misc->s_full[buf], ub & 1, misc, partner_abort, prm.status, 47);
+                    if (ok && ub > 0) ok = pair_wait(&misc->p_empty[buf], (ub - 1) & 1, misc, partner_abort, prm.status, 48);
+                    ok = !named_barrier_or(1, 128, !ok || aborted());
+                    if (!ok) break;
+                    tc_fence_after();
+                    float s[128];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t r[32];
+                        tmem_ld32(tmem_addr(tmem, lane_base, C::kTmemS + buf * 128 + 32 * j), r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) s[32 * j + i] = __uint_as_float(r[i]);
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&misc->s_empty[buf]);
+                    float mt = -INFINITY;
+#pragma unroll
+                    for (int i = 0; i < 128; ++i) {
+                        if (i >= ntok) s[i] = -INFINITY;
+                        mt = fmaxf(mt, s[i]);
+                    }
+                    // lazy running max (log2 units): move it only when the tile max exceeds it by 8
+                    const float ms = mt * prm.scale_log2;
+                    float alpha = 1.f;
+                    bool resc = false;
+                    if (ms > m_run + 8.f) {
+                        alpha = first ? 0.f : exp2f(m_run - ms);
+                        resc = !first;
+                        m_run = ms;
+                        l *= alpha;
+                    }
+                    // P row of head h -> rank 1's P buffer, K-major with the 128-byte swizzle
+                    const uint32_t prow = o_p + buf * C::kPBufBytes + h * 128;
+#pragma unroll
+                    for (int ck = 0; ck < 2; ++ck) {
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int t = 64 * ck + 8 * u + 2 * e;
+                                const float p0 = exp2f(fmaf(s[t], prm.scale_log2, -m_run));
+                                const float p1 = exp2f(fmaf(s[t + 1], prm.scale_log2, -m_run));
+                                l += p0 + p1;
+                                __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
+                                w[e] = *reinterpret_cast<uint32_t*>(&v);
+                            }
+                            st_cluster_v4(prow + ck * C::kChunkBytes + ((u ^ (h & 7)) << 4), w[0], w[1], w[2], w[3]);
+                        }
+                    }
+                    st_cluster_u32(o_alpha + (buf * 128 + h) * 4, __float_as_uint(alpha));
+                    if (last) {
+                        st_cluster_u32(o_finm + (buf * 128 + h) * 4, __float_as_uint(m_run));
+                        st_cluster_u32(o_finl + (buf * 128 + h) * 4, __float_as_uint(l));
+                    }
+                    const bool any = named_barrier_or(2, 128, resc);
+                    if (h == 0) st_cluster_u32(o_resc + buf * 4, any ? 1u : 0u);
+                    fence_proxy_async_cluster();
+                    mbar_arrive_cluster(o_pfull + buf * 8);
+                    first = false;
+                    ++tcount;
+                    if (h == 0) PAIR_PROGRESS(2, tcount);
+                }
+            }
+        }
+    } else {
+        // ================================================================== O CTA
+        if (warp == 0) {
+            // ---------------------------------------------------------- TMA producer: V slots
+            if (lane == 0) prefetch_tensormap(&tm_v);
+            const int box_rows = P < 32 ? P : 32;
+            uint32_t vcount = 0;
+            bool ok = true;
+            TileCursorT<C::kTile> cur;
+            bool more = cur.init(prm.segments, seg_begin, seg_end);
+            bool new_seg = true;
+            int win_base = -(1 << 30), win_page = 0;
+            const int32_t* pages = nullptr;
+            while (more && ok) {
+                if (new_seg) {
+                    pages = prm.kv_indices + prm.kv_indptr[cur.sg.b];
+                    win_base = -(1 << 30);
+                }
+                const int ntok = cur.ntok();
+                const int nq = (ntok + 31) / 32;
+                const int first_page = cur.t0 / P;
+                const int last_page = (cur.t0 + nq * 32 - 1) / P;
+                if (last_page + 1 > win_base + 32 || first_page < win_base) {
+                    const int seg_last_page = (cur.sg.t_end - 1) / P;
+                    win_base = first_page;
+                    win_page = (win_base + lane <= seg_last_page) ? pages[win_base + lane] : 0;
+                }
+                for (int half = 0; half < 2 && ok; ++half) {
+                    for (int q = 0; q < nq && ok; ++q) {
+                        const uint32_t s = vcount % C::kVSlots, use = vcount / C::kVSlots;
+                        if (lane == 0 && use > 0)
+                            ok = pair_wait(&misc->v_empty[s], (use - 1) & 1, misc, partner_abort, prm.status, 51);
+                        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                        if (!ok) break;
+                        uint8_t* dst = smem + C::kOffV + s * C::kVSlotBytes;
+                        if (lane == 0) mbar_arrive_expect_tx(&misc->v_full[s], C::kVSlotBytes);
+                        for (int bx = 0; bx < 32 / box_rows; ++bx) {
+                            const int t = cur.t0 + q * 32 + bx * box_rows;
+                            const int pg = __shfl_sync(0xffffffffu, win_page, (t / P - win_base) & 31);
+                            if (lane == 0)
+                                tma_load_3d(dst + bx * 4 * box_rows * 128, &tm_v, &misc->v_full[s], 0, pg * P + (t % P),
+                                            4 * half);
+                        }
+                        ++vcount;
+                    }
+                }
+                if (lane == 0) PAIR_PROGRESS(3, vcount);
+                more = cur.advance(new_seg);
+            }
+            if (lane == 0) {
+                const uint64_t t0 = global_timer_ns();
+                for (int s = 0; s < C::kVSlots; ++s) {
+                    const uint32_t uses = vcount / C::kVSlots + (static_cast<uint32_t>(s) < vcount % C::kVSlots ? 1 : 0);
+                    if (uses == 0) continue;
+                    while (!mbar_try_wait(&misc->v_full[s], (uses - 1) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {}
+                }
+            }
+        } else if (warp == 1) {
+            // ---------------------------------------------------------- MMA issuer: O += P V
+            if (lane == 0) {
+                const int box_rows = P < 32 ? P : 32;
+                const uint32_t lbo = static_cast<uint32_t>(box_rows) * 128;
+                uint32_t tcount = 0, vcount = 0, segc = 0, rcount = 0, zcount = 0;
+                bool ok = true;
+                TileCursorT<C::kTile> cur;
+                bool more = cur.init(prm.segments, seg_begin, seg_end);
+                bool new_seg = true;
+                const uint32_t pbase = smem_u32(smem + C::kOffP);
+                const uint32_t vbase = smem_u32(smem + C::kOffV);
+                while (more && ok) {
+                    const bool first = cur.first();
+                    const int ntok = cur.ntok();
+                    const uint32_t buf = tcount & 1, ub = tcount >> 1;
+                    ok = pair_wait(&misc->p_full[buf], ub & 1, misc, partner_abort, prm.status, 52);
+                    if (ok && new_seg && segc > 0)
+                        ok = pair_wait(&misc->epi_done, (segc - 1) & 1, misc, partner_abort, prm.status, 53);
+                    if (new_seg) ++segc;
+                    if (ok && !first && *reinterpret_cast<volatile int*>(&misc->rescale[buf])) {
+                        ok = pair_wait(&misc->corr_done, rcount & 1, misc, partner_abort, prm.status, 54);
+                        ++rcount;
+                    }
+                    if (ok && (ntok & 15)) {
+                        ok = pair_wait(&misc->vz_done, zcount & 1, misc, partner_abort, prm.status, 55);
+                        ++zcount;
+                    }
+                    if (!ok) break;
+                    fence_proxy_async_smem();
+                    tc_fence_after();
+                    const int nq = (ntok + 31) / 32;
+                    for (int half = 0; half < 2 && ok; ++half) {
+                        for (int q = 0; q < nq && ok; ++q) {
+                            const uint32_t s = vcount % C::kVSlots;
+                            ok = pair_wait(&misc->v_full[s], (vcount / C::kVSlots) & 1, misc, partner_abort, prm.status, 56);
+                            if (!ok) break;
+                            tc_fence_after();
+                            for (int k2 = 0; k2 < 2; ++k2) {
+                                const int kk = 2 * q + k2;   // 16-token step within the tile
+                                if (16 * kk >= ntok) break;
+                                const uint32_t a = pbase + buf * C::kPBufBytes + (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+                                const int r0 = 16 * k2;
+                                const uint32_t b = vbase + s * C::kVSlotBytes + (r0 / box_rows) * 4 * lbo + (r0 % box_rows) * 128;
+                                umma_bf16(tmem + 256 * half, umma_desc_sw128(a, 16, 1024), umma_desc_sw128(b, lbo, 1024),
+                                          C::kIdescPV, (first && kk == 0) ? 0u : 1u);
+                            }
+                            umma_commit(&misc->v_empty[s]);
+                            ++vcount;
+                        }
+                    }
+                    if (!ok) break;
+                    umma_commit(&misc->pv_done[buf]);
+                    ++tcount;
+                    PAIR_PROGRESS(4, tcount);
+                    more = cur.advance(new_seg);
+                }
+            }
+        } else if (warp >= 4) {
+            // ---------------------------------------------------------- correction / epilogue warpgroup
+            const int h = threadIdx.x - 128;
+            const uint32_t lane_base = static_cast<uint32_t>(warp - 4) * 32;
+            const uint32_t s_pempty = mapa_shared(smem_u32(&misc->p_empty[0]), partner);
+            const int box_rows = P < 32 ? P : 32;
+            // requests with no tokens: out = 0, lse = -inf
+            for (int si = seg_begin; si < seg_end; ++si) {
+                const Segment sg = prm.segments[si];
+                if (sg.t_end > sg.t_begin) continue;
+                float4* o = reinterpret_cast<float4*>(prm.out + static_cast<size_t>(sg.b) * 128 * kDimCkv);
+                for (int i = h; i < 128 * kDimCkv / 4; i += 128) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                prm.lse[static_cast<size_t>(sg.b) * 128 + h] = -INFINITY;
+            }
+            uint32_t tcount = 0, vcount = 0;
+            bool ok = true;
+            for (int si = seg_begin; si < seg_end && ok; ++si) {
+                const Segment sg = prm.segments[si];
+                if (sg.t_end <= sg.t_begin) continue;
+                for (int t0 = sg.t_begin; t0 < sg.t_end && ok; t0 += C::kTile) {
+                    const int ntok = min(C::kTile, sg.t_end - t0);
+                    const bool first = t0 == sg.t_begin, last = t0 + C::kTile >= sg.t_end;
+                    const int nq = (ntok + 31) / 32;
+                    const uint32_t buf = tcount & 1, ub = tcount >> 1;
+                    ok = pair_wait(&misc->p_full[buf], ub & 1, misc, partner_abort, prm.status, 61);
+                    ok = !named_barrier_or(1, 128, !ok || aborted());
+                    if (!ok) break;
+                    // everything rank 0 left with this P buffer is read before the buffer goes back
+                    const bool resc = !first && *reinterpret_cast<volatile int*>(&misc->rescale[buf]);
+                    const float alpha = misc->alpha[buf][h];
+                    const float fin_m = last ? misc->fin_m[buf][h] : 0.f;
+                    const float fin_l = last ? misc->fin_l[buf][h] : 1.f;
+                    if (ntok & 15) {
+                        // value rows [ntok, next multiple of 16) of the partial 32-token quarter, both
+                        // halves: stale or NaN page tails the step's MMA would otherwise read
+                        const int qz = ntok >> 5, r_lo = ntok & 31, r_hi = (r_lo + 15) & ~15;
+                        for (int half = 0; half < 2 && ok; ++half) {
+                            const uint32_t vi = vcount + half * nq + qz;
+                            ok = pair_wait(&misc->v_full[vi % C::kVSlots], (vi / C::kVSlots) & 1, misc, partner_abort,
+                                           prm.status, 62);
+                            if (!ok) break;
+                            uint8_t* slot = smem + C::kOffV + (vi % C::kVSlots) * C::kVSlotBytes;
+                            for (int i = h; i < (r_hi - r_lo) * 32; i += 128) {
+                                const int r = r_lo + i / 32, c = (i / 8) & 3, u = i & 7;
+                                *reinterpret_cast<uint4*>(slot + (r / box_rows) * 4 * box_rows * 128 + c * box_rows * 128 +
+                                                          (r % box_rows) * 128 + u * 16) = make_uint4(0, 0, 0, 0);
+                            }
+                        }
+                        fence_proxy_async_smem();
+                        ok = !named_barrier_or(1, 128, !ok || aborted());
+                        if (!ok) break;
+                        if (h == 0) mbar_arrive(&misc->vz_done);
+                    }
+                    if (resc) {
+                        // O row *= alpha once the previous tile's O += P V has completed.  The TMEM
+                        // accesses are warp-collective: a warp takes the branch when any of its
+                        // heads moved, each lane scaling by its own factor (1 if unchanged).
+                        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                            tc_fence_after();
+#pragma unroll 1
+                            for (int c = 0; c < 512; c += 32) {
+                                uint32_t r[32];
+                                tmem_ld32(tmem_addr(tmem, lane_base, c), r);
+                                tmem_wait_ld();
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                                tmem_st32(tmem_addr(tmem, lane_base, c), r);
+                            }
+                            tmem_wait_st();
+                        }
+                        tc_fence_before();
+                        named_barrier_sync(1, 128);
+                        if (h == 0) mbar_arrive(&misc->corr_done);
+                    }
+                    vcount += 2 * nq;
+                    // this tile's O += P V done: its P buffer goes back to rank 0
+                    ok = pair_wait(&misc->pv_done[buf], ub & 1, misc, partner_abort, prm.status, 63);
+                    ok = !named_barrier_or(1, 128, !ok || aborted());
+                    if (!ok) break;
+                    if (h == 0) mbar_arrive_cluster(s_pempty + buf * 8);
+                    ++tcount;
+                    if (h == 0) PAIR_PROGRESS(5, tcount);
+                    if (!last) continue;
+                    // ---- epilogue: O / l -> out (or the piece's partial), lse
+                    tc_fence_after();
+                    const float inv = 1.f / fin_l;
+                    const float lse_h = (fin_m + log2f(fin_l)) * 0.69314718055994530942f;
+                    float* obase;
+                    float* lbase;
+                    if (sg.slot < 0) {
+                        obase = prm.out + static_cast<size_t>(sg.b) * 128 * kDimCkv;
+                        lbase = prm.lse + static_cast<size_t>(sg.b) * 128;
+                    } else {
+                        obase = prm.part_o + static_cast<size_t>(sg.slot) * 128 * kDimCkv;
+                        lbase = prm.part_lse + static_cast<size_t>(sg.slot) * 128;
+                    }
+                    float4* orow = reinterpret_cast<float4*>(obase + static_cast<size_t>(h) * kDimCkv);
+#pragma unroll 1
+                    for (int c = 0; c < 512; c += 32) {
+                        uint32_t r[32];
+                        tmem_ld32(tmem_addr(tmem, lane_base, c), r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            orow[c / 4 + i] = make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
+                                                          __uint_as_float(r[4 * i + 2]) * inv,
+                                                          __uint_as_float(r[4 * i + 3]) * inv);
+                    }
+                    lbase[h] = lse_h;
+                    tc_fence_before();
+                    named_barrier_sync(1, 128);
+                    if (h == 0) mbar_arrive(&misc->epi_done);
+                    if (sg.slot >= 0) {
+                        // split request: the last piece to arrive merges all of them in slot order
+                        __threadfence();
+                        named_barrier_sync(1, 128);
+                        if (h == 0) misc->merge_flag = (atomicAdd(&prm.counters[sg.item], 1) == sg.n_slots - 1);
+                        named_barrier_sync(1, 128);
+                        if (misc->merge_flag) {
+                            __threadfence();
+                            merge_split_pieces<128, 128>(prm, sg.b, sg.slot_begin, sg.n_slots, 0, h, 1, misc->mrg_max,
+                                                         misc->mrg_inv, misc->mrg_w);
+                            if (h == 0) prm.counters[sg.item] = 0;
+                        }
+                        named_barrier_sync(1, 128);
+                    }
+                }
+            }
+        }
+    }
+
+    if (threadIdx.x == 0) PAIR_PROGRESS(6, 1000000 + misc->abort_flag);
+    tc_fence_before();
+    __syncwarp();
+    __syncthreads();
+    cluster_sync();   // no CTA leaves while its partner may still write into its shared memory
+    if (threadIdx.x == 0) PAIR_PROGRESS(7, 1);
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace mla

@@ -37,8 +37,10 @@ def _check_plan(lens, h_q, P, sms):
     hg = mla.mla_plan_heads_per_cta(plan)
     groups = h_q // hg
     units = len(uptr) - 1
-    assert mla.mla_plan_num_ctas(plan) == units * groups
-    assert units <= max(1, sms // groups)
+    assert units == mla.mla_plan_num_units(plan)
+    pair = 2 if h_q == 128 else 1            # 128 heads: a cluster of two CTAs per unit
+    assert mla.mla_plan_num_ctas(plan) == units * groups * pair
+    assert units <= max(1, sms // (groups * pair))
     # coverage: each request's tokens exactly once, pieces in token order
     covered = {b: [] for b in range(len(lens))}
     empties = []
@@ -100,7 +102,9 @@ def test_uniform_batch():
 
 def test_compute_shape_groups():
     segs, uptr = _check_plan([8192] * 128, 128, 64, 152)
-    assert len(uptr) - 1 == 152 // 4
+    assert len(uptr) - 1 == 152 // 2          # one unit per pair of SMs
+    segs, uptr = _check_plan([8192] * 128, 64, 64, 152)
+    assert len(uptr) - 1 == 152 // 2          # two 32-head groups per unit
 
 
 def test_tiny_and_edge_lengths():
