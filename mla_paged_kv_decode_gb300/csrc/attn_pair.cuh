@@ -45,10 +45,11 @@ struct PairCfg {
     static constexpr int kSEnd = kOffK + kKSlots * kChunkBytes;        // 208 KB
     // rank 1
     static constexpr int kPBufBytes = 2 * kChunkBytes;                 // [2 token chunks][128 heads][128 B]
+    static constexpr int kPBufs = 3;
     static constexpr int kOffP = 0;
     static constexpr int kVSlotBytes = 4 * 32 * 128;                   // [boxes][4 dim chunks][rows][128 B] = 32 tokens x 256 dims
-    static constexpr int kVSlots = 9;
-    static constexpr int kOffV = kOffP + 2 * kPBufBytes;
+    static constexpr int kVSlots = 7;
+    static constexpr int kOffV = kOffP + kPBufs * kPBufBytes;
     static constexpr int kOEnd = kOffV + kVSlots * kVSlotBytes;        // 208 KB
     static constexpr int kOffMisc = kSEnd > kOEnd ? kSEnd : kOEnd;
     static constexpr int kMiscBytes = 12 * 1024;
@@ -66,19 +67,19 @@ struct PairMisc {
     uint64_t k_full[PairCfg::kKSlots], k_empty[PairCfg::kKSlots];
     uint64_t s_full[2], s_empty[2];
     uint64_t q_full, q_empty;
-    uint64_t p_empty[2];
+    uint64_t p_empty[PairCfg::kPBufs];
     // rank 1
     uint64_t v_full[PairCfg::kVSlots], v_empty[PairCfg::kVSlots];
-    uint64_t p_full[2];
-    uint64_t pv_done[2];
+    uint64_t p_full[PairCfg::kPBufs];
+    uint64_t pv_done[PairCfg::kPBufs];
     uint64_t corr_done, vz_done, epi_done;
     uint32_t tmem_base;
     int abort_flag;
     int merge_flag;
-    int rescale[2];                 // written by rank 0 per P buffer: some head's max moved
-    float alpha[2][128];            // ... the factor for each head (1 if unchanged)
-    float fin_m[2][128];            // ... at a segment's last tile: running max (log2 units)
-    float fin_l[2][128];            // ... and row sum
+    int rescale[PairCfg::kPBufs];           // written by rank 0 per P buffer: some head's max moved
+    float alpha[PairCfg::kPBufs][128];      // ... the factor for each head (1 if unchanged)
+    float fin_m[PairCfg::kPBufs][128];      // ... at a segment's last tile: running max (log2 units)
+    float fin_l[PairCfg::kPBufs][128];      // ... and row sum
     float mrg_max[128], mrg_inv[128], mrg_w[8 * 128];
 };
 
@@ -144,6 +145,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
         for (int i = 0; i < 2; ++i) {
             mbar_init(&misc->s_full[i], 1);
             mbar_init(&misc->s_empty[i], 4);
+        }
+        for (int i = 0; i < C::kPBufs; ++i) {
             mbar_init(&misc->p_empty[i], 1);
             mbar_init(&misc->p_full[i], 128);
             mbar_init(&misc->pv_done[i], 1);
@@ -211,6 +214,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                 }
                 for (int c = 0; c < 9 && ok; ++c) {   // 8 ckv chunks of 64 dims, then kpe
                     const uint32_t s = kcount % C::kKSlots, use = kcount / C::kKSlots;
+                    if (lane == 0 && c == 8) MLA_TRACE_EVENT(0, kcount / 9);
                     if (lane == 0 && use > 0)
                         ok = pair_wait(&misc->k_empty[s], (use - 1) & 1, misc, partner_abort, prm.status, 42);
                     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -258,6 +262,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                     const uint32_t buf = tcount & 1, ub = tcount >> 1;
                     if (ok && ub > 0) ok = pair_wait(&misc->s_empty[buf], (ub - 1) & 1, misc, partner_abort, prm.status, 44);
                     if (!ok) break;
+                    MLA_TRACE_EVENT(1, tcount);
                     tc_fence_after();
                     const uint32_t d = tmem + C::kTmemS + buf * 128;
                     for (int c = 0; c < 9 && ok; ++c) {
@@ -280,6 +285,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                     if (!ok) break;
                     umma_commit(&misc->s_full[buf]);
                     if (last) umma_commit(&misc->q_empty);
+                    MLA_TRACE_EVENT(2, tcount);
                     ++tcount;
                     PAIR_PROGRESS(1, tcount);
                     more = cur.advance(new_seg);
@@ -332,11 +338,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                 for (int t0 = sg.t_begin; t0 < sg.t_end && ok; t0 += C::kTile) {
                     const int ntok = min(C::kTile, sg.t_end - t0);
                     const bool last = t0 + C::kTile >= sg.t_end;
-                    const uint32_t buf = tcount & 1, ub = tcount >> 1;
+                    const uint32_t buf = tcount & 1, ub = tcount >> 1;                  // S buffer
+                    const uint32_t pb = tcount % C::kPBufs, up = tcount / C::kPBufs;   // P buffer
                     ok = pair_wait(&misc->s_full[buf], ub & 1, misc, partner_abort, prm.status, 47);
-                    if (ok && ub > 0) ok = pair_wait(&misc->p_empty[buf], (ub - 1) & 1, misc, partner_abort, prm.status, 48);
+                    if (ok && up > 0) ok = pair_wait(&misc->p_empty[pb], (up - 1) & 1, misc, partner_abort, prm.status, 48);
                     ok = !named_barrier_or(1, 128, !ok || aborted());
                     if (!ok) break;
+                    if (h == 0) MLA_TRACE_EVENT(3, tcount);
                     tc_fence_after();
                     float s[128];
 #pragma unroll
@@ -367,7 +375,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                         l *= alpha;
                     }
                     // P row of head h -> rank 1's P buffer, K-major with the 128-byte swizzle
-                    const uint32_t prow = o_p + buf * C::kPBufBytes + h * 128;
+                    const uint32_t prow = o_p + pb * C::kPBufBytes + h * 128;
 #pragma unroll
                     for (int ck = 0; ck < 2; ++ck) {
 #pragma unroll
@@ -376,8 +384,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 const int t = 64 * ck + 8 * u + 2 * e;
-                                const float p0 = exp2f(fmaf(s[t], prm.scale_log2, -m_run));
-                                const float p1 = exp2f(fmaf(s[t + 1], prm.scale_log2, -m_run));
+                                const float p0 = fast_exp2(fmaf(s[t], prm.scale_log2, -m_run));
+                                const float p1 = fast_exp2(fmaf(s[t + 1], prm.scale_log2, -m_run));
                                 l += p0 + p1;
                                 __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
                                 w[e] = *reinterpret_cast<uint32_t*>(&v);
@@ -385,15 +393,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                             st_cluster_v4(prow + ck * C::kChunkBytes + ((u ^ (h & 7)) << 4), w[0], w[1], w[2], w[3]);
                         }
                     }
-                    st_cluster_u32(o_alpha + (buf * 128 + h) * 4, __float_as_uint(alpha));
+                    st_cluster_u32(o_alpha + (pb * 128 + h) * 4, __float_as_uint(alpha));
                     if (last) {
-                        st_cluster_u32(o_finm + (buf * 128 + h) * 4, __float_as_uint(m_run));
-                        st_cluster_u32(o_finl + (buf * 128 + h) * 4, __float_as_uint(l));
+                        st_cluster_u32(o_finm + (pb * 128 + h) * 4, __float_as_uint(m_run));
+                        st_cluster_u32(o_finl + (pb * 128 + h) * 4, __float_as_uint(l));
                     }
                     const bool any = named_barrier_or(2, 128, resc);
-                    if (h == 0) st_cluster_u32(o_resc + buf * 4, any ? 1u : 0u);
+                    if (h == 0) st_cluster_u32(o_resc + pb * 4, any ? 1u : 0u);
                     fence_proxy_async_cluster();
-                    mbar_arrive_cluster(o_pfull + buf * 8);
+                    if (h == 0) MLA_TRACE_EVENT(4, tcount);
+                    mbar_arrive_cluster(o_pfull + pb * 8);
                     first = false;
                     ++tcount;
                     if (h == 0) PAIR_PROGRESS(2, tcount);
@@ -472,7 +481,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                 while (more && ok) {
                     const bool first = cur.first();
                     const int ntok = cur.ntok();
-                    const uint32_t buf = tcount & 1, ub = tcount >> 1;
+                    const uint32_t buf = tcount % C::kPBufs, ub = tcount / C::kPBufs;
                     ok = pair_wait(&misc->p_full[buf], ub & 1, misc, partner_abort, prm.status, 52);
                     if (ok && new_seg && segc > 0)
                         ok = pair_wait(&misc->epi_done, (segc - 1) & 1, misc, partner_abort, prm.status, 53);
@@ -481,15 +490,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                         ok = pair_wait(&misc->corr_done, rcount & 1, misc, partner_abort, prm.status, 54);
                         ++rcount;
                     }
-                    if (ok && (ntok & 15)) {
-                        ok = pair_wait(&misc->vz_done, zcount & 1, misc, partner_abort, prm.status, 55);
-                        ++zcount;
-                    }
                     if (!ok) break;
+                    MLA_TRACE_EVENT(5, tcount);
                     fence_proxy_async_smem();
                     tc_fence_after();
                     const int nq = (ntok + 31) / 32;
                     for (int half = 0; half < 2 && ok; ++half) {
+                        if (ntok & 15) {   // partial tile: this half's tail rows zeroed first
+                            ok = pair_wait(&misc->vz_done, zcount & 1, misc, partner_abort, prm.status, 55);
+                            ++zcount;
+                            if (!ok) break;
+                            fence_proxy_async_smem();
+                        }
                         for (int q = 0; q < nq && ok; ++q) {
                             const uint32_t s = vcount % C::kVSlots;
                             ok = pair_wait(&misc->v_full[s], (vcount / C::kVSlots) & 1, misc, partner_abort, prm.status, 56);
@@ -510,6 +522,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                     }
                     if (!ok) break;
                     umma_commit(&misc->pv_done[buf]);
+                    MLA_TRACE_EVENT(6, tcount);
                     ++tcount;
                     PAIR_PROGRESS(4, tcount);
                     more = cur.advance(new_seg);
@@ -538,7 +551,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                     const int ntok = min(C::kTile, sg.t_end - t0);
                     const bool first = t0 == sg.t_begin, last = t0 + C::kTile >= sg.t_end;
                     const int nq = (ntok + 31) / 32;
-                    const uint32_t buf = tcount & 1, ub = tcount >> 1;
+                    const uint32_t buf = tcount % C::kPBufs, ub = tcount / C::kPBufs;
                     ok = pair_wait(&misc->p_full[buf], ub & 1, misc, partner_abort, prm.status, 61);
                     ok = !named_barrier_or(1, 128, !ok || aborted());
                     if (!ok) break;
@@ -547,15 +560,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                     const float alpha = misc->alpha[buf][h];
                     const float fin_m = last ? misc->fin_m[buf][h] : 0.f;
                     const float fin_l = last ? misc->fin_l[buf][h] : 1.f;
-                    if (ntok & 15) {
-                        // value rows [ntok, next multiple of 16) of the partial 32-token quarter, both
-                        // halves: stale or NaN page tails the step's MMA would otherwise read
+                    // value rows [ntok, next multiple of 16) of the partial 32-token quarter of one half:
+                    // stale or NaN page tails the step's MMA would otherwise read.  Each half is
+                    // signalled on its own: the second half's slot is loaded only after the MMA has
+                    // released the first half's.
+                    auto zero_half = [&](int half) {
                         const int qz = ntok >> 5, r_lo = ntok & 31, r_hi = (r_lo + 15) & ~15;
-                        for (int half = 0; half < 2 && ok; ++half) {
-                            const uint32_t vi = vcount + half * nq + qz;
-                            ok = pair_wait(&misc->v_full[vi % C::kVSlots], (vi / C::kVSlots) & 1, misc, partner_abort,
-                                           prm.status, 62);
-                            if (!ok) break;
+                        const uint32_t vi = vcount + half * nq + qz;
+                        ok = pair_wait(&misc->v_full[vi % C::kVSlots], (vi / C::kVSlots) & 1, misc, partner_abort,
+                                       prm.status, 62);
+                        if (ok) {
                             uint8_t* slot = smem + C::kOffV + (vi % C::kVSlots) * C::kVSlotBytes;
                             for (int i = h; i < (r_hi - r_lo) * 32; i += 128) {
                                 const int r = r_lo + i / 32, c = (i / 8) & 3, u = i & 7;
@@ -565,8 +579,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                         }
                         fence_proxy_async_smem();
                         ok = !named_barrier_or(1, 128, !ok || aborted());
+                        if (ok && h == 0) mbar_arrive(&misc->vz_done);
+                    };
+                    if (ntok & 15) {
+                        zero_half(0);
                         if (!ok) break;
-                        if (h == 0) mbar_arrive(&misc->vz_done);
                     }
                     if (resc) {
                         // O row *= alpha once the previous tile's O += P V has completed.  The TMEM
@@ -589,12 +606,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                         named_barrier_sync(1, 128);
                         if (h == 0) mbar_arrive(&misc->corr_done);
                     }
+                    if (ntok & 15) {
+                        zero_half(1);
+                        if (!ok) break;
+                    }
                     vcount += 2 * nq;
                     // this tile's O += P V done: its P buffer goes back to rank 0
                     ok = pair_wait(&misc->pv_done[buf], ub & 1, misc, partner_abort, prm.status, 63);
                     ok = !named_barrier_or(1, 128, !ok || aborted());
                     if (!ok) break;
                     if (h == 0) mbar_arrive_cluster(s_pempty + buf * 8);
+                    if (h == 0) MLA_TRACE_EVENT(7, tcount);
                     ++tcount;
                     if (h == 0) PAIR_PROGRESS(5, tcount);
                     if (!last) continue;
