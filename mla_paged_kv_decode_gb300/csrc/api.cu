@@ -142,14 +142,15 @@ cudaError_t launch_narrow(const mla_plan_s* p, const CUtensorMap& ckv, const CUt
     return cudaGetLastError();
 }
 
+template <int HQ>
 cudaError_t launch_pair(const mla_plan_s* p, const MapCache& mc, const mla::AttnParams& prm, const void* q_nope,
                         cudaStream_t stream) {
     using C = mla::PairCfg;
-    cudaError_t e = cudaFuncSetAttribute(mla::mla_decode_pair_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(mla::mla_decode_pair_kernel<HQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int grid = 2 * p->d.num_units;   // clusters of two CTAs (the kernel's cluster dimensions)
-    mla::mla_decode_pair_kernel<0><<<grid, C::kThreads, C::kSmemBytes, stream>>>(
+    mla::mla_decode_pair_kernel<HQ><<<grid, C::kThreads, C::kSmemBytes, stream>>>(
         mc.m_ckv, mc.m_kpe, mc.m_qp, mc.m_v, prm, static_cast<const uint16_t*>(q_nope));
     return cudaGetLastError();
 }
@@ -196,7 +197,7 @@ mla_status_t run_checked(mla_plan_t plan, const void* q_nope, const void* q_pe, 
                              : make_map_bf16(&mc.m_ckv, ckv_cache, mla::kDimCkv, rows, box);
         mc.valid = ok_ckv && make_map_bf16(&mc.m_kpe, kpe_cache, mla::kDimKpe, rows, box) &&
                    make_map_bf16(&mc.m_qn, q_nope, mla::kDimCkv, qrows, hg) &&
-                   make_map_bf16(&mc.m_qp, q_pe, mla::kDimKpe, qrows, hg) &&
+                   make_map_bf16(&mc.m_qp, q_pe, mla::kDimKpe, qrows, d.pair ? 128 : hg) &&
                    (!d.pair || make_map_v_half(&mc.m_v, ckv_cache, rows, std::min(d.page_size, 32)));
         if (!mc.valid) return MLA_ERR_CUDA;
         mc.ckv = ckv_cache;
@@ -233,7 +234,8 @@ mla_status_t run_checked(mla_plan_t plan, const void* q_nope, const void* q_pe, 
             e = d.h_q == 16 ? launch_narrow<16, false>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream)
                             : launch_narrow<32, false>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream);
     } else if (d.pair) {
-        e = launch_pair(plan, mc, prm, q_nope, stream);
+        e = d.h_q == 128 ? launch_pair<128>(plan, mc, prm, q_nope, stream)
+                         : launch_pair<64>(plan, mc, prm, q_nope, stream);
     } else {
         e = launch_attention<32>(plan, mc.m_ckv, mc.m_kpe, mc.m_qn, mc.m_qp, prm, stream);
     }

@@ -19,6 +19,9 @@
 //     than 2^8), zeroes value rows past the last token of a partial tile, and writes the
 //     normalised output (or a split piece's partial) at the end of a segment.
 //
+// 64-head requests run on the same kernel with the MMAs' M padded to 128: heads 64..127
+// get zero query rows and zero P rows, and nothing is written for them.
+//
 // The split-KV partition, the partials and the last-arriver merge are those of the other
 // kernels (FlashMLA PR #233, "balanced scheduler, deterministic combine").  Every wait is
 // bounded; a wait that runs out raises the abort flag of both CTAs.
@@ -117,7 +120,7 @@ __device__ __forceinline__ bool pair_wait(uint64_t* bar, uint32_t parity, PairMi
     }
 }
 
-template <int DUMMY = 0>
+template <int HQ>   // query heads: 128, or 64 with the MMAs' M padded to 128
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1)
     mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tm_ckv, const __grid_constant__ CUtensorMap tm_kpe,
                            const __grid_constant__ CUtensorMap tm_qpe, const __grid_constant__ CUtensorMap tm_v,
@@ -135,6 +138,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
     const int seg_begin = prm.unit_ptr[unit];
     const int seg_end = prm.unit_ptr[unit + 1];
     const int P = prm.page_size;
+    static_assert(HQ == 64 || HQ == 128, "the two-CTA kernel serves 64 or 128 heads");
+    constexpr int hq = HQ;
     const uint32_t partner_abort = mapa_shared(smem_u32(&misc->abort_flag), partner);
 
     if (threadIdx.x == 0) {
@@ -198,7 +203,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                     if (!ok) break;
                     if (lane == 0) {
                         mbar_arrive_expect_tx(&misc->q_full, 128 * 128);
-                        tma_load_2d(smem + C::kOffQpe, &tm_qpe, &misc->q_full, 0, cur.sg.b * 128);
+                        // 128 rows from the request's first head: for 64 heads the rows past them
+                        // belong to the next request (or lie past the tensor, filled with zeros) and
+                        // only feed score rows that are never used
+                        tma_load_2d(smem + C::kOffQpe, &tm_qpe, &misc->q_full, 0, cur.sg.b * hq);
                     }
                     ++segc;
                     pages = prm.kv_indices + prm.kv_indptr[cur.sg.b];
@@ -313,13 +321,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                 if (!ok) break;
                 {
                     const uint4* qrow =
-                        reinterpret_cast<const uint4*>(q_nope + (static_cast<size_t>(sg.b) * 128 + h) * kDimCkv);
+                        reinterpret_cast<const uint4*>(q_nope + (static_cast<size_t>(sg.b) * hq + h) * kDimCkv);
 #pragma unroll 1
                     for (int c0 = 0; c0 < 256; c0 += 32) {
                         uint32_t r[32];
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
-                            const uint4 v = qrow[c0 / 4 + j];
+                            const uint4 v = h < hq ? qrow[c0 / 4 + j] : make_uint4(0, 0, 0, 0);
                             r[4 * j] = v.x;
                             r[4 * j + 1] = v.y;
                             r[4 * j + 2] = v.z;
@@ -361,9 +369,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                     float mt = -INFINITY;
 #pragma unroll
                     for (int i = 0; i < 128; ++i) {
-                        if (i >= ntok) s[i] = -INFINITY;
+                        if (i >= ntok || h >= hq) s[i] = -INFINITY;   // padded heads: P = 0
                         mt = fmaxf(mt, s[i]);
                     }
+                    if (h >= hq) mt = 0.f;
                     // lazy running max (log2 units): move it only when the tile max exceeds it by 8
                     const float ms = mt * prm.scale_log2;
                     float alpha = 1.f;
@@ -538,9 +547,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
             for (int si = seg_begin; si < seg_end; ++si) {
                 const Segment sg = prm.segments[si];
                 if (sg.t_end > sg.t_begin) continue;
-                float4* o = reinterpret_cast<float4*>(prm.out + static_cast<size_t>(sg.b) * 128 * kDimCkv);
-                for (int i = h; i < 128 * kDimCkv / 4; i += 128) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                prm.lse[static_cast<size_t>(sg.b) * 128 + h] = -INFINITY;
+                float4* o = reinterpret_cast<float4*>(prm.out + static_cast<size_t>(sg.b) * hq * kDimCkv);
+                for (int i = h; i < hq * kDimCkv / 4; i += 128) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (h < hq) prm.lse[static_cast<size_t>(sg.b) * hq + h] = -INFINITY;
             }
             uint32_t tcount = 0, vcount = 0;
             bool ok = true;
@@ -627,25 +636,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                     float* obase;
                     float* lbase;
                     if (sg.slot < 0) {
-                        obase = prm.out + static_cast<size_t>(sg.b) * 128 * kDimCkv;
-                        lbase = prm.lse + static_cast<size_t>(sg.b) * 128;
+                        obase = prm.out + static_cast<size_t>(sg.b) * hq * kDimCkv;
+                        lbase = prm.lse + static_cast<size_t>(sg.b) * hq;
                     } else {
-                        obase = prm.part_o + static_cast<size_t>(sg.slot) * 128 * kDimCkv;
-                        lbase = prm.part_lse + static_cast<size_t>(sg.slot) * 128;
+                        obase = prm.part_o + static_cast<size_t>(sg.slot) * hq * kDimCkv;
+                        lbase = prm.part_lse + static_cast<size_t>(sg.slot) * hq;
                     }
                     float4* orow = reinterpret_cast<float4*>(obase + static_cast<size_t>(h) * kDimCkv);
 #pragma unroll 1
-                    for (int c = 0; c < 512; c += 32) {
+                    for (int c = 0; c < 512; c += 32) {   // the TMEM loads are warp-collective: every lane
                         uint32_t r[32];
                         tmem_ld32(tmem_addr(tmem, lane_base, c), r);
                         tmem_wait_ld();
+                        if (h < hq) {
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            orow[c / 4 + i] = make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
-                                                          __uint_as_float(r[4 * i + 2]) * inv,
-                                                          __uint_as_float(r[4 * i + 3]) * inv);
+                            for (int i = 0; i < 8; ++i)
+                                orow[c / 4 + i] =
+                                    make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
+                                                __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
+                        }
                     }
-                    lbase[h] = lse_h;
+                    if (h < hq) lbase[h] = lse_h;
                     tc_fence_before();
                     named_barrier_sync(1, 128);
                     if (h == 0) mbar_arrive(&misc->epi_done);
@@ -657,8 +668,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                         named_barrier_sync(1, 128);
                         if (misc->merge_flag) {
                             __threadfence();
-                            merge_split_pieces<128, 128>(prm, sg.b, sg.slot_begin, sg.n_slots, 0, h, 1, misc->mrg_max,
-                                                         misc->mrg_inv, misc->mrg_w);
+                            merge_split_pieces<HQ, 128>(prm, sg.b, sg.slot_begin, sg.n_slots, 0, h, 1, misc->mrg_max,
+                                                        misc->mrg_inv, misc->mrg_w);
                             if (h == 0) prm.counters[sg.item] = 0;
                         }
                         named_barrier_sync(1, 128);

@@ -27,8 +27,8 @@ int heads_per_cta_for(int h_q, int kv_dtype) {
     switch (h_q) {
         case 16: return 16;
         case 32: return 32;
-        case 64: return 32;
-        case 128: return kv_dtype == 0 ? 128 : 32;   // bf16: one cluster of two CTAs serves all 128 heads
+        case 64:
+        case 128: return kv_dtype == 0 ? h_q : 32;   // bf16: one cluster of two CTAs serves all heads
         default: return 0;
     }
 }
@@ -72,7 +72,7 @@ int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int ba
     p.head_groups = h_q / hg;
     p.tile_tokens = tile_tok;
     p.narrow = narrow;
-    p.pair = h_q == 128 && kv_dtype == 0;
+    p.pair = h_q >= 64 && kv_dtype == 0;
     const int ctas_per_unit = p.head_groups * (p.pair ? 2 : 1);
     int64_t units = std::max(1, num_sms / ctas_per_unit);
     units = std::min<int64_t>(units, std::max<int64_t>(total_tiles, 1));

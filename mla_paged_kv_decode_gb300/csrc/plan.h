@@ -45,7 +45,7 @@ struct PlanData {
     int heads_per_cta = 0, head_groups = 0, num_units = 0;
     int tile_tokens = 0;              // plan granularity = the kernel's tile
     bool narrow = false;              // h_q <= 32: warp-MMA kernel, else tcgen05 kernel
-    bool pair = false;                // h_q == 128, bf16 cache: two-CTA cluster kernel, 2 CTAs per unit
+    bool pair = false;                // h_q 64/128, bf16 cache: two-CTA cluster kernel, 2 CTAs per unit
     int segment_cost = 0;             // partition cost of a request start, in tiles
     std::vector<int32_t> unit_ptr;
     std::vector<Segment> segments;

@@ -61,6 +61,23 @@ def test_split_patterns(sms):
     assert_parity(out, lse, *oracle.decode_inputs(inp))
 
 
+@pytest.mark.parametrize("H", [64, 128])
+@pytest.mark.parametrize("sms", [3, 152])
+def test_split_patterns_wide_heads(H, sms):
+    """64 and 128 heads on the two-CTA kernel: pieces merged over 64 or 128 heads."""
+    inp = _small([3000, 5, 700, 4096, 129], H, 64, seed=13 + H)
+    out, lse, _, _ = run_gpu(inp, sms=sms)
+    assert_parity(out, lse, *oracle.decode_inputs(inp))
+
+
+@pytest.mark.parametrize("L", [1, 130, 5000])
+def test_single_request_64_heads(L):
+    """One 64-head request: the kernel's 128-row query box runs past the query tensor."""
+    inp = _small([L], 64, 32, seed=14)
+    out, lse, _, _ = run_gpu(inp)
+    assert_parity(out, lse, *oracle.decode_inputs(inp))
+
+
 def test_one_long_request_split_over_every_sm():
     inp = _small([32768], 16, 16, seed=8)
     out, lse, dec, _ = run_gpu(inp)

@@ -38,7 +38,7 @@ def _check_plan(lens, h_q, P, sms):
     groups = h_q // hg
     units = len(uptr) - 1
     assert units == mla.mla_plan_num_units(plan)
-    pair = 2 if h_q == 128 else 1            # 128 heads: a cluster of two CTAs per unit
+    pair = 2 if h_q >= 64 else 1             # 64/128 heads: a cluster of two CTAs per unit
     assert mla.mla_plan_num_ctas(plan) == units * groups * pair
     assert units <= max(1, sms // (groups * pair))
     # coverage: each request's tokens exactly once, pieces in token order
@@ -104,7 +104,7 @@ def test_compute_shape_groups():
     segs, uptr = _check_plan([8192] * 128, 128, 64, 152)
     assert len(uptr) - 1 == 152 // 2          # one unit per pair of SMs
     segs, uptr = _check_plan([8192] * 128, 64, 64, 152)
-    assert len(uptr) - 1 == 152 // 2          # two 32-head groups per unit
+    assert len(uptr) - 1 == 152 // 2          # 64 heads: the same two-CTA unit
 
 
 def test_tiny_and_edge_lengths():
