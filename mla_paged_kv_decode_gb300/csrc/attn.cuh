@@ -173,8 +173,15 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, AttnM
 #ifdef MLA_TRACE
 #define MLA_TRACE_EVENT(ev, idx)                                                              \
     do {                                                                                      \
-        if (prm.trace && blockIdx.x < 4 && (idx) < 256)                                       \
+        if (prm.trace && blockIdx.x < 2 && (idx) < 256)                                       \
             prm.trace[(blockIdx.x * 8 + (ev)) * 256 + (idx)] = global_timer_ns();            \
+    } while (0)
+// CTA 0 only: a timestamp per unit of work (a ring slot fill, ...) in the area of CTAs 2 and 3,
+// lane `ln` (0..3) of 1024 entries each.
+#define MLA_TRACE_UNIT(ln, idx)                                                               \
+    do {                                                                                      \
+        if (prm.trace && blockIdx.x == 0 && (idx) < 1024)                                     \
+            prm.trace[2 * 8 * 256 + (ln) * 1024 + (idx)] = global_timer_ns();                 \
     } while (0)
 // Every CTA also records 8 milestones (entry, producer done, ...) after the per-tile area.
 #define MLA_TRACE_CTA(k)                                                                      \
@@ -187,6 +194,9 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, AttnM
     } while (0)
 #define MLA_TRACE_CTA(k) \
     do {                 \
+    } while (0)
+#define MLA_TRACE_UNIT(ln, idx) \
+    do {                        \
     } while (0)
 #endif
 

@@ -12,7 +12,10 @@
 //     memory; S = Q K^T is accumulated into one of two 128-column TMEM buffers by
 //     36 MMAs (M 128, N 128, K 16) per 128-token tile from a ring of 16 KB K chunks.
 //     The softmax warpgroup (thread = head) reads S, keeps the running max and sum, and
-//     writes P (bf16) and the rescale factors into rank 1's shared memory.
+//     writes P (bf16) and the rescale factors into a local staging tile, which one thread
+//     hands to rank 1's shared memory with bulk copies (cp.async.bulk over the cluster).
+//     Per-thread remote stores of P (st.shared::cluster) measured 17 % slower per step:
+//     thousands of 16-byte transactions per tile held up the SM's TMA loads.
 //   rank 1 ("O CTA"):  O (128 x 512 fp32) fills its TMEM; O += P V is 16 MMAs (M 128,
 //     N 256, K 16) per tile, V streamed as [4 dim chunks][32 tokens] slots.  A correction
 //     warpgroup rescales O rows when rank 0 raised a head's running max (lazily, by more
@@ -42,12 +45,13 @@ struct PairCfg {
     static constexpr int kTile = kTileTokens;     // 128 tokens
     static constexpr int kChunkBytes = 128 * 128; // 128 rows x 128 B (64 bf16)
     // rank 0
-    static constexpr int kKSlots = 12;
+    static constexpr int kKSlots = 10;
+    static constexpr int kPBufBytes = 2 * kChunkBytes;                 // [2 token chunks][128 heads][128 B]
     static constexpr int kOffQpe = 0;                                  // [128 heads][128 B] SW128
     static constexpr int kOffK = kOffQpe + kChunkBytes;                // K ring
-    static constexpr int kSEnd = kOffK + kKSlots * kChunkBytes;        // 208 KB
+    static constexpr int kOffPStage = kOffK + kKSlots * kChunkBytes;   // P of one tile, copied to rank 1
+    static constexpr int kSEnd = kOffPStage + kPBufBytes;              // 208 KB
     // rank 1
-    static constexpr int kPBufBytes = 2 * kChunkBytes;                 // [2 token chunks][128 heads][128 B]
     static constexpr int kPBufs = 3;
     static constexpr int kOffP = 0;
     static constexpr int kVSlotBytes = 4 * 32 * 128;                   // [boxes][4 dim chunks][rows][128 B] = 32 tokens x 256 dims
@@ -79,10 +83,11 @@ struct PairMisc {
     uint32_t tmem_base;
     int abort_flag;
     int merge_flag;
-    int rescale[PairCfg::kPBufs];           // written by rank 0 per P buffer: some head's max moved
-    float alpha[PairCfg::kPBufs][128];      // ... the factor for each head (1 if unchanged)
-    float fin_m[PairCfg::kPBufs][128];      // ... at a segment's last tile: running max (log2 units)
-    float fin_l[PairCfg::kPBufs][128];      // ... and row sum
+    // per P buffer, staged in rank 0 and bulk-copied into rank 1 with the P tile:
+    alignas(16) int rescale[PairCfg::kPBufs][4];     // [0]: some head's running max moved
+    alignas(16) float alpha[PairCfg::kPBufs][128];   // the factor for each head (1 if unchanged)
+    alignas(16) float fin_m[PairCfg::kPBufs][128];   // at a segment's last tile: running max (log2 units)
+    alignas(16) float fin_l[PairCfg::kPBufs][128];   // ... and row sum
     float mrg_max[128], mrg_inv[128], mrg_w[8 * 128];
 };
 
@@ -100,16 +105,20 @@ struct PairMisc {
     } while (0)
 #endif
 
-// Bounded wait on a local mbarrier phase with cluster-scope acquire.  On a timeout it raises
-// both CTAs' abort flags and records `site`.
+// Bounded wait on a local mbarrier phase.  kCluster: the phase is completed by arrivals from
+// the partner CTA, whose writes the wait acquires (cluster scope); otherwise by this CTA's
+// threads, its TMA copies or its tensor-core commits (CTA scope).  On a timeout it raises both
+// CTAs' abort flags and records `site`.
+template <bool kCluster = false>
 __device__ __forceinline__ bool pair_wait(uint64_t* bar, uint32_t parity, PairMisc* misc, uint32_t partner_abort,
                                           uint32_t* status, uint32_t site) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
+    auto probe = [&]() { return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+    if (probe()) return true;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
 #pragma unroll 1
         for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait_cluster(bar, parity)) return true;
+            if (probe()) return true;
         if (*reinterpret_cast<volatile int*>(&misc->abort_flag)) return false;
         if (global_timer_ns() - t0 > kWaitLimitNs) {
             *reinterpret_cast<volatile int*>(&misc->abort_flag) = 1;
@@ -153,7 +162,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
         }
         for (int i = 0; i < C::kPBufs; ++i) {
             mbar_init(&misc->p_empty[i], 1);
-            mbar_init(&misc->p_full[i], 128);
+            mbar_init(&misc->p_full[i], 1);   // rank 0's issuing thread; the copies add bytes
             mbar_init(&misc->pv_done[i], 1);
         }
         mbar_init(&misc->q_full, 2);
@@ -227,6 +236,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                         ok = pair_wait(&misc->k_empty[s], (use - 1) & 1, misc, partner_abort, prm.status, 42);
                     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                     if (!ok) break;
+                    if (lane == 0) MLA_TRACE_UNIT(0, kcount);
                     uint8_t* dst = smem + C::kOffK + s * C::kChunkBytes;
                     if (lane == 0) mbar_arrive_expect_tx(&misc->k_full[s], static_cast<uint32_t>(nbox * P * 128));
                     for (int bx = 0; bx < nbox; ++bx) {
@@ -238,6 +248,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                                 tma_load_2d(dst + bx * P * 128, &tm_kpe, &misc->k_full[s], 0, pg * P);
                         }
                     }
+                    if (lane == 0 && c == 0) MLA_TRACE_EVENT(5, kcount / 9);
+                    if (lane == 0) MLA_TRACE_UNIT(1, kcount);
                     ++kcount;
                 }
                 if (lane == 0) PAIR_PROGRESS(0, kcount);
@@ -277,6 +289,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                         const uint32_t s = kcount % C::kKSlots;
                         ok = pair_wait(&misc->k_full[s], (kcount / C::kKSlots) & 1, misc, partner_abort, prm.status, 45);
                         if (!ok) break;
+                        MLA_TRACE_UNIT(2, kcount);
                         tc_fence_after();
                         const uint32_t kb = kbase + s * C::kChunkBytes;
 #pragma unroll
@@ -288,6 +301,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                                 umma_bf16(d, umma_desc_sw128(qpe + k * 32, 16, 1024), bd, C::kIdescS, 1);
                         }
                         umma_commit(&misc->k_empty[s]);
+                        MLA_TRACE_UNIT(3, kcount);
                         ++kcount;
                     }
                     if (!ok) break;
@@ -308,7 +322,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
             const uint32_t o_alpha = mapa_shared(smem_u32(&misc->alpha[0][0]), partner);
             const uint32_t o_finm = mapa_shared(smem_u32(&misc->fin_m[0][0]), partner);
             const uint32_t o_finl = mapa_shared(smem_u32(&misc->fin_l[0][0]), partner);
-            const uint32_t o_resc = mapa_shared(smem_u32(&misc->rescale[0]), partner);
+            const uint32_t o_resc = mapa_shared(smem_u32(&misc->rescale[0][0]), partner);
+            uint8_t* pstage = smem + C::kOffPStage;
+            const uint32_t pstage_row = smem_u32(pstage) + h * 128;
+            // bytes one tile hands to rank 1: P, then alpha, fin_m, fin_l rows and the rescale word
+            constexpr uint32_t kHandBytes = C::kPBufBytes + 3 * 128 * 4 + 16;
             uint32_t tcount = 0, segc = 0;
             bool ok = true;
             for (int si = seg_begin; si < seg_end && ok; ++si) {
@@ -345,11 +363,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                 bool first = true;
                 for (int t0 = sg.t_begin; t0 < sg.t_end && ok; t0 += C::kTile) {
                     const int ntok = min(C::kTile, sg.t_end - t0);
-                    const bool last = t0 + C::kTile >= sg.t_end;
                     const uint32_t buf = tcount & 1, ub = tcount >> 1;                  // S buffer
                     const uint32_t pb = tcount % C::kPBufs, up = tcount / C::kPBufs;   // P buffer
                     ok = pair_wait(&misc->s_full[buf], ub & 1, misc, partner_abort, prm.status, 47);
-                    if (ok && up > 0) ok = pair_wait(&misc->p_empty[pb], (up - 1) & 1, misc, partner_abort, prm.status, 48);
+                    if (ok && up > 0) ok = pair_wait<true>(&misc->p_empty[pb], (up - 1) & 1, misc, partner_abort, prm.status, 48);
+                    if (h == 0) bulk_wait_read_all();   // the previous tile's copies have left the staging
                     ok = !named_barrier_or(1, 128, !ok || aborted());
                     if (!ok) break;
                     if (h == 0) MLA_TRACE_EVENT(3, tcount);
@@ -366,6 +384,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&misc->s_empty[buf]);
+                    if (h == 0) MLA_TRACE_EVENT(6, tcount);
                     float mt = -INFINITY;
 #pragma unroll
                     for (int i = 0; i < 128; ++i) {
@@ -383,8 +402,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                         m_run = ms;
                         l *= alpha;
                     }
-                    // P row of head h -> rank 1's P buffer, K-major with the 128-byte swizzle
-                    const uint32_t prow = o_p + pb * C::kPBufBytes + h * 128;
+                    // P row of head h -> the staging tile, K-major with the 128-byte swizzle
 #pragma unroll
                     for (int ck = 0; ck < 2; ++ck) {
 #pragma unroll
@@ -399,24 +417,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                                 __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
                                 w[e] = *reinterpret_cast<uint32_t*>(&v);
                             }
-                            st_cluster_v4(prow + ck * C::kChunkBytes + ((u ^ (h & 7)) << 4), w[0], w[1], w[2], w[3]);
+                            st_shared_v4(pstage_row + ck * C::kChunkBytes + ((u ^ (h & 7)) << 4), w[0], w[1], w[2], w[3]);
                         }
                     }
-                    st_cluster_u32(o_alpha + (pb * 128 + h) * 4, __float_as_uint(alpha));
-                    if (last) {
-                        st_cluster_u32(o_finm + (pb * 128 + h) * 4, __float_as_uint(m_run));
-                        st_cluster_u32(o_finl + (pb * 128 + h) * 4, __float_as_uint(l));
-                    }
+                    misc->alpha[pb][h] = alpha;
+                    misc->fin_m[pb][h] = m_run;
+                    misc->fin_l[pb][h] = l;
+                    fence_proxy_async_smem();   // this thread's staging writes -> the copy engine
+                    if (h == 0) MLA_TRACE_EVENT(7, tcount);
                     const bool any = named_barrier_or(2, 128, resc);
-                    if (h == 0) st_cluster_u32(o_resc + pb * 4, any ? 1u : 0u);
-                    fence_proxy_async_cluster();
-                    if (h == 0) MLA_TRACE_EVENT(4, tcount);
-                    mbar_arrive_cluster(o_pfull + pb * 8);
+                    if (h == 0) {
+                        misc->rescale[pb][0] = any ? 1 : 0;
+                        fence_proxy_async_smem();
+                        const uint32_t bar = o_pfull + pb * 8;
+                        mbar_arrive_expect_tx_cluster(bar, kHandBytes);
+                        bulk_copy_to_cluster(o_p + pb * C::kPBufBytes, pstage, C::kPBufBytes, bar);
+                        bulk_copy_to_cluster(o_alpha + pb * 512, &misc->alpha[pb][0], 512, bar);
+                        bulk_copy_to_cluster(o_finm + pb * 512, &misc->fin_m[pb][0], 512, bar);
+                        bulk_copy_to_cluster(o_finl + pb * 512, &misc->fin_l[pb][0], 512, bar);
+                        bulk_copy_to_cluster(o_resc + pb * 16, &misc->rescale[pb][0], 16, bar);
+                        bulk_commit_group();
+                        MLA_TRACE_EVENT(4, tcount);
+                    }
                     first = false;
                     ++tcount;
                     if (h == 0) PAIR_PROGRESS(2, tcount);
                 }
             }
+            if (h == 0) bulk_wait_read_all();
         }
     } else {
         // ================================================================== O CTA
@@ -454,6 +482,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                         if (!ok) break;
                         uint8_t* dst = smem + C::kOffV + s * C::kVSlotBytes;
                         if (lane == 0) mbar_arrive_expect_tx(&misc->v_full[s], C::kVSlotBytes);
+                        if (lane == 0 && half == 0 && q == 0) MLA_TRACE_EVENT(0, vcount / (2 * nq));
+                        if (lane == 0 && half == 1 && q == nq - 1) MLA_TRACE_EVENT(1, vcount / (2 * nq));
                         for (int bx = 0; bx < 32 / box_rows; ++bx) {
                             const int t = cur.t0 + q * 32 + bx * box_rows;
                             const int pg = __shfl_sync(0xffffffffu, win_page, (t / P - win_base) & 31);
@@ -491,11 +521,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                     const bool first = cur.first();
                     const int ntok = cur.ntok();
                     const uint32_t buf = tcount % C::kPBufs, ub = tcount / C::kPBufs;
-                    ok = pair_wait(&misc->p_full[buf], ub & 1, misc, partner_abort, prm.status, 52);
+                    ok = pair_wait<true>(&misc->p_full[buf], ub & 1, misc, partner_abort, prm.status, 52);
                     if (ok && new_seg && segc > 0)
                         ok = pair_wait(&misc->epi_done, (segc - 1) & 1, misc, partner_abort, prm.status, 53);
                     if (new_seg) ++segc;
-                    if (ok && !first && *reinterpret_cast<volatile int*>(&misc->rescale[buf])) {
+                    if (ok && !first && *reinterpret_cast<volatile int*>(&misc->rescale[buf][0])) {
                         ok = pair_wait(&misc->corr_done, rcount & 1, misc, partner_abort, prm.status, 54);
                         ++rcount;
                     }
@@ -528,6 +558,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                             umma_commit(&misc->v_empty[s]);
                             ++vcount;
                         }
+                        if (half == 0) MLA_TRACE_EVENT(2, tcount);
                     }
                     if (!ok) break;
                     umma_commit(&misc->pv_done[buf]);
@@ -561,11 +592,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                     const bool first = t0 == sg.t_begin, last = t0 + C::kTile >= sg.t_end;
                     const int nq = (ntok + 31) / 32;
                     const uint32_t buf = tcount % C::kPBufs, ub = tcount / C::kPBufs;
-                    ok = pair_wait(&misc->p_full[buf], ub & 1, misc, partner_abort, prm.status, 61);
+                    ok = pair_wait<true>(&misc->p_full[buf], ub & 1, misc, partner_abort, prm.status, 61);
                     ok = !named_barrier_or(1, 128, !ok || aborted());
                     if (!ok) break;
+                    if (h == 0) MLA_TRACE_EVENT(3, tcount);
                     // everything rank 0 left with this P buffer is read before the buffer goes back
-                    const bool resc = !first && *reinterpret_cast<volatile int*>(&misc->rescale[buf]);
+                    const bool resc = !first && *reinterpret_cast<volatile int*>(&misc->rescale[buf][0]);
                     const float alpha = misc->alpha[buf][h];
                     const float fin_m = last ? misc->fin_m[buf][h] : 0.f;
                     const float fin_l = last ? misc->fin_l[buf][h] : 1.f;

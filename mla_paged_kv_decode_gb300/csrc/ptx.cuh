@@ -322,6 +322,10 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
     return r;
 }
 
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
 __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                  : "memory");
@@ -359,5 +363,28 @@ __device__ __forceinline__ void cluster_sync() {
 __device__ __forceinline__ void fence_proxy_async_cluster() {
     asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
 }
+
+// Arrive on a cluster CTA's mbarrier (address from mapa_shared) and raise its expected
+// transaction bytes, releasing this thread's earlier writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t remote_bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(remote_bar),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// Bulk copy from this CTA's shared memory into a cluster CTA's (destination and mbarrier
+// addresses from mapa_shared; 16-byte aligned, bytes % 16 == 0).  Completes on the
+// destination's mbarrier; the source may be reused after bulk_wait_read_all().
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst),
+                 "r"(smem_u32(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// every bulk copy this thread committed has finished reading its source
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 }  // namespace mla
