@@ -22,7 +22,7 @@ struct MapCache {
     bool valid = false;
     const void *ckv = nullptr, *kpe = nullptr, *qn = nullptr, *qp = nullptr;
     int num_pages = 0;
-    CUtensorMap m_ckv, m_kpe, m_qn, m_qp, m_v;
+    CUtensorMap m_ckv, m_kpe, m_qp, m_v;
 };
 
 struct mla_plan_s {
@@ -155,20 +155,6 @@ cudaError_t launch_pair(const mla_plan_s* p, const MapCache& mc, const mla::Attn
     return cudaGetLastError();
 }
 
-template <int HG>
-cudaError_t launch_attention(const mla_plan_s* p, const CUtensorMap& ckv, const CUtensorMap& kpe,
-                             const CUtensorMap& qn, const CUtensorMap& qp, const mla::AttnParams& prm,
-                             cudaStream_t stream) {
-    using C = mla::AttnCfg<HG>;
-    cudaError_t e = cudaFuncSetAttribute(mla::mla_decode_attn_kernel<HG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    static_assert(sizeof(mla::AttnParams) % 8 == 0, "kernel parameter block");
-    const int grid = p->d.num_units * p->d.head_groups;
-    mla::mla_decode_attn_kernel<HG><<<grid, C::kThreads, C::kSmemBytes, stream>>>(ckv, kpe, qn, qp, prm);
-    return cudaGetLastError();
-}
-
 // Argument checks, tensor maps and the launch shared by mla_decode_run and
 // mla_decode_run_noalloc; `ws` is the committed workspace (device).
 mla_status_t run_checked(mla_plan_t plan, const void* q_nope, const void* q_pe, const void* ckv_cache,
@@ -196,7 +182,6 @@ mla_status_t run_checked(mla_plan_t plan, const void* q_nope, const void* q_pe, 
             ok_ckv = chunked ? make_map_ckv_chunked(&mc.m_ckv, ckv_cache, rows, box)
                              : make_map_bf16(&mc.m_ckv, ckv_cache, mla::kDimCkv, rows, box);
         mc.valid = ok_ckv && make_map_bf16(&mc.m_kpe, kpe_cache, mla::kDimKpe, rows, box) &&
-                   make_map_bf16(&mc.m_qn, q_nope, mla::kDimCkv, qrows, hg) &&
                    make_map_bf16(&mc.m_qp, q_pe, mla::kDimKpe, qrows, d.pair ? 128 : hg) &&
                    (!d.pair || make_map_v_half(&mc.m_v, ckv_cache, rows, std::min(d.page_size, 32)));
         if (!mc.valid) return MLA_ERR_CUDA;
@@ -237,7 +222,7 @@ mla_status_t run_checked(mla_plan_t plan, const void* q_nope, const void* q_pe, 
         e = d.h_q == 128 ? launch_pair<128>(plan, mc, prm, q_nope, stream)
                          : launch_pair<64>(plan, mc, prm, q_nope, stream);
     } else {
-        e = launch_attention<32>(plan, mc.m_ckv, mc.m_kpe, mc.m_qn, mc.m_qp, prm, stream);
+        return MLA_ERR_UNSUPPORTED;   // the plan admits no other head count
     }
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
