@@ -79,7 +79,11 @@ struct PairMisc {
     uint64_t v_full[PairCfg::kVSlots], v_empty[PairCfg::kVSlots];
     uint64_t p_full[PairCfg::kPBufs];
     uint64_t pv_done[PairCfg::kPBufs];
-    uint64_t corr_done, vz_done, epi_done;
+    // Zeroing the value rows past the last token of a partial tile, per half: the MMA thread
+    // (the V ring's consumer) raises vz_go once the slot has landed, the correction warps zero
+    // the rows and raise vz_done.  One barrier pair per half, so that no barrier can run two
+    // phases ahead of its waiter.
+    uint64_t corr_done, vz_go[2], vz_done[2], epi_done;
     uint32_t tmem_base;
     int abort_flag;
     int merge_flag;
@@ -172,7 +176,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
             mbar_init(&misc->v_empty[i], 1);
         }
         mbar_init(&misc->corr_done, 1);
-        mbar_init(&misc->vz_done, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&misc->vz_go[i], 1);
+            mbar_init(&misc->vz_done[i], 1);
+        }
         mbar_init(&misc->epi_done, 1);
         misc->abort_flag = 0;
         fence_mbarrier_init();
@@ -534,17 +541,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                     fence_proxy_async_smem();
                     tc_fence_after();
                     const int nq = (ntok + 31) / 32;
+                    const bool partial = (ntok & 15) != 0;
                     for (int half = 0; half < 2 && ok; ++half) {
-                        if (ntok & 15) {   // partial tile: this half's tail rows zeroed first
-                            ok = pair_wait(&misc->vz_done, zcount & 1, misc, partner_abort, prm.status, 55);
-                            ++zcount;
-                            if (!ok) break;
-                            fence_proxy_async_smem();
-                        }
                         for (int q = 0; q < nq && ok; ++q) {
                             const uint32_t s = vcount % C::kVSlots;
                             ok = pair_wait(&misc->v_full[s], (vcount / C::kVSlots) & 1, misc, partner_abort, prm.status, 56);
                             if (!ok) break;
+                            if (partial && q == nq - 1) {
+                                // the slot with the tile's last token: its rows past it are zeroed first
+                                mbar_arrive(&misc->vz_go[half]);
+                                ok = pair_wait(&misc->vz_done[half], zcount & 1, misc, partner_abort, prm.status, 55);
+                                if (!ok) break;
+                                fence_proxy_async_smem();
+                            }
                             tc_fence_after();
                             for (int k2 = 0; k2 < 2; ++k2) {
                                 const int kk = 2 * q + k2;   // 16-token step within the tile
@@ -561,6 +570,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                         if (half == 0) MLA_TRACE_EVENT(2, tcount);
                     }
                     if (!ok) break;
+                    if (partial) ++zcount;   // partial tiles seen
                     umma_commit(&misc->pv_done[buf]);
                     MLA_TRACE_EVENT(6, tcount);
                     ++tcount;
@@ -582,7 +592,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                 for (int i = h; i < hq * kDimCkv / 4; i += 128) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (h < hq) prm.lse[static_cast<size_t>(sg.b) * hq + h] = -INFINITY;
             }
-            uint32_t tcount = 0, vcount = 0;
+            uint32_t tcount = 0, vcount = 0, zcount = 0;
             bool ok = true;
             for (int si = seg_begin; si < seg_end && ok; ++si) {
                 const Segment sg = prm.segments[si];
@@ -602,14 +612,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                     const float fin_m = last ? misc->fin_m[buf][h] : 0.f;
                     const float fin_l = last ? misc->fin_l[buf][h] : 1.f;
                     // value rows [ntok, next multiple of 16) of the partial 32-token quarter of one half:
-                    // stale or NaN page tails the step's MMA would otherwise read.  Each half is
-                    // signalled on its own: the second half's slot is loaded only after the MMA has
-                    // released the first half's.
+                    // stale or NaN page tails the step's MMA would otherwise read.  The MMA thread
+                    // raises vz_go[half] once that slot has landed (it is the ring's consumer; these
+                    // warps could not tell the slot's phase apart from its previous use's).
                     auto zero_half = [&](int half) {
                         const int qz = ntok >> 5, r_lo = ntok & 31, r_hi = (r_lo + 15) & ~15;
                         const uint32_t vi = vcount + half * nq + qz;
-                        ok = pair_wait(&misc->v_full[vi % C::kVSlots], (vi / C::kVSlots) & 1, misc, partner_abort,
-                                       prm.status, 62);
+                        ok = pair_wait(&misc->vz_go[half], zcount & 1, misc, partner_abort, prm.status, 62);
                         if (ok) {
                             uint8_t* slot = smem + C::kOffV + (vi % C::kVSlots) * C::kVSlotBytes;
                             for (int i = h; i < (r_hi - r_lo) * 32; i += 128) {
@@ -620,12 +629,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                         }
                         fence_proxy_async_smem();
                         ok = !named_barrier_or(1, 128, !ok || aborted());
-                        if (ok && h == 0) mbar_arrive(&misc->vz_done);
+                        if (ok && h == 0) mbar_arrive(&misc->vz_done[half]);
                     };
-                    if (ntok & 15) {
-                        zero_half(0);
-                        if (!ok) break;
-                    }
                     if (resc) {
                         // O row *= alpha once the previous tile's O += P V has completed.  The TMEM
                         // accesses are warp-collective: a warp takes the branch when any of its
@@ -647,9 +652,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                         named_barrier_sync(1, 128);
                         if (h == 0) mbar_arrive(&misc->corr_done);
                     }
-                    if (ntok & 15) {
-                        zero_half(1);
+                    if (ntok & 15) {   // after the rescale: the MMA thread signals only once past corr_done
+                        zero_half(0);
+                        if (ok) zero_half(1);
                         if (!ok) break;
+                        ++zcount;
                     }
                     vcount += 2 * nq;
                     // this tile's O += P V done: its P buffer goes back to rank 0

@@ -31,7 +31,8 @@ def run_gpu(inp, sms=None, stream=None):
     out, lse = dec.run(d.q_nope, d.q_pe, d.ckv, d.kpe, d.kv_indices, d.kv_indptr, d.kv_last_page_len,
                        inp.sm_scale, ckv_scale=d.ckv_scale, stream=stream)
     torch.cuda.synchronize()
-    assert dec.device_status() == mla.MLA_OK
+    word = int(dec.workspace[:4].view(torch.int32).item())   # status word: 0x100 | site of a timed-out wait
+    assert dec.device_status() == mla.MLA_OK, f"device status word {word:#x}"
     return out.cpu(), lse.cpu(), dec, d
 
 
