@@ -349,7 +349,7 @@ def main():
         secondary = {"workload": args.secondary, "desc": WORKLOADS[args.secondary].description,
                      "us_per_step": s2 * 1e6, "tflops": f2 / s2 / 1e12, "kv_gbs": b2 / s2 / 1e9,
                      "tensor_frac": f2 / s2 / 1e12 / bf16_tf, "hbm_frac": b2 / s2 / 1e9 / hbm_gbs,
-                     "alg_flops": f2, "alg_bytes": b2}
+                     "alg_flops": f2, "alg_bytes": b2, "traffic": recorded_traffic(args.secondary)}
         del inp2
         torch.cuda.empty_cache()
 
@@ -370,7 +370,8 @@ def main():
         fp8 = {"workload": "fp8", "desc": WORKLOADS["fp8"].description, "us_per_step": t8 * 1e6,
                "gbs": b8 / t8 / 1e9, "hbm_frac": b8 / t8 / 1e9 / hbm_gbs, "tokens_per_s": tok / t8,
                "bf16_us_per_step": t16 * 1e6, "bf16_gbs": b16 / t16 / 1e9,
-               "speedup_vs_bf16": t16 / t8, "bytes_per_token": {"fp8": 644, "bf16": 1152}}
+               "speedup_vs_bf16": t16 / t8, "bytes_per_token": {"fp8": 644, "bf16": 1152},
+               "traffic": recorded_traffic("fp8")}
 
     # ---- cpu baseline: the oracle on a bounded sample, host cores, rank 0 at N=1
     cpu = None
