@@ -122,11 +122,14 @@ __device__ __forceinline__ float warp_sum(float v) {
 // give identical bits.  The loads are issued in batches (all heads of a piece at once) so
 // the merge costs a few memory round trips rather than one per (piece, head).
 // NTHR threads (tid 0..NTHR-1) call it together and synchronise on named barrier `bar`.
-// Scratch in shared memory: s_max[NH], s_inv[NH], s_w[NTHR] (NTHR >= 8 * 16).
+// Scratch in shared memory: s_max[NH], s_inv[NH], s_w[8 * NH] (and NTHR >= 8 * 16).
+//
+// This general form takes five or more dependent rounds of L2 loads (the lse, the weights,
+// then each piece); merge_split_pieces below serves up to 8 pieces in two or three.
 template <int NH, int NTHR>
-__device__ __forceinline__ void merge_split_pieces(const AttnParams& prm, int b, int slot_begin, int n_slots,
-                                                   int head0, int tid, uint32_t bar, float* s_max, float* s_inv,
-                                                   float* s_w) {
+__device__ __forceinline__ void merge_split_pieces_chunked(const AttnParams& prm, int b, int slot_begin, int n_slots,
+                                                           int head0, int tid, uint32_t bar, float* s_max,
+                                                           float* s_inv, float* s_w) {
     static_assert(NTHR == 128 && NH % 16 == 0 && NTHR % NH == 0, "merge layout");
     constexpr int kTph = NTHR / NH;    // threads per head in the lse pass
     constexpr int kChunk = NTHR / 16;  // pieces whose weights are staged at a time (8)
@@ -200,6 +203,95 @@ __device__ __forceinline__ void merge_split_pieces(const AttnParams& prm, int b,
         }
 #pragma unroll
         for (int h = 0; h < 16; ++h) out4[(hb + h) * (kDimCkv / 4)] = acc[h];
+    }
+}
+
+// The same merge for up to 8 pieces: every thread loads the lse of its pieces once and
+// computes their weights itself, and the outputs go by blocks of 8 heads x 4 pieces whose
+// loads are all in flight together.  The first block's loads are issued before the lse
+// reduction.  Same sums, same fixed orders (pieces in slot order) as the general form.
+template <int NH, int NTHR>
+__device__ __forceinline__ void merge_split_pieces(const AttnParams& prm, int b, int slot_begin, int n_slots,
+                                                   int head0, int tid, uint32_t bar, float* s_max, float* s_inv,
+                                                   float* s_w) {
+    static_assert(NTHR == 128 && NH % 16 == 0 && NTHR % NH == 0, "merge layout");
+    constexpr int kMax = 8;            // pieces served here
+    constexpr int kTph = NTHR / NH;    // threads per head in the lse pass
+    constexpr int kPer = kMax / kTph;  // pieces per thread in the lse pass
+    constexpr int kHB = 8, kPB = 4;    // output block: heads x pieces with their loads in flight together
+    if (n_slots > kMax) {
+        merge_split_pieces_chunked<NH, NTHR>(prm, b, slot_begin, n_slots, head0, tid, bar, s_max, s_inv, s_w);
+        return;
+    }
+    const size_t hq = static_cast<size_t>(prm.h_q);
+    auto piece_o = [&](int i, int h) {   // this thread's 4 dims of head h, piece i
+        return reinterpret_cast<const float4*>(prm.part_o + ((slot_begin + i) * hq + head0 + h) * kDimCkv) + tid;
+    };
+    float4 v[kPB][kHB];
+    auto load_block = [&](int hb, int p0) {
+#pragma unroll
+        for (int i = 0; i < kPB; ++i)
+#pragma unroll
+            for (int h = 0; h < kHB; ++h)
+                v[i][h] = (p0 + i < n_slots) ? __ldcg(piece_o(p0 + i, hb + h)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    load_block(0, 0);   // in flight during the lse pass
+    {
+        const int h = tid / kTph, sub = tid % kTph;
+        float x[kPer];
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int i = sub + kTph * j;
+            x[j] = i < n_slots ? __ldcg(prm.part_lse + (slot_begin + i) * hq + head0 + h) : -INFINITY;
+        }
+        float m = x[0];
+#pragma unroll
+        for (int j = 1; j < kPer; ++j) m = fmaxf(m, x[j]);
+#pragma unroll
+        for (int o = kTph / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        // every piece has a finite lse (a non-empty token range), so m is finite
+        float sum = 0.f;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) sum += (sub + kTph * j < n_slots) ? expf(x[j] - m) : 0.f;
+#pragma unroll
+        for (int o = kTph / 2; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        const float inv = 1.f / sum;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int i = sub + kTph * j;
+            if (i < n_slots) s_w[i * NH + h] = expf(x[j] - m) * inv;
+        }
+        if (sub == 0) {
+            s_max[h] = m;
+            s_inv[h] = inv;
+            prm.lse[static_cast<size_t>(b) * hq + head0 + h] = m + logf(sum);
+        }
+    }
+    named_barrier_sync(bar, NTHR);
+    float4* out4 = reinterpret_cast<float4*>(prm.out + (static_cast<size_t>(b) * hq + head0) * kDimCkv) + tid;
+#pragma unroll 1
+    for (int hb = 0; hb < NH; hb += kHB) {
+        float4 acc[kHB];
+#pragma unroll
+        for (int h = 0; h < kHB; ++h) acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+        for (int p0 = 0; p0 < n_slots; p0 += kPB) {
+            if (hb != 0 || p0 != 0) load_block(hb, p0);
+#pragma unroll
+            for (int i = 0; i < kPB; ++i) {
+                if (p0 + i >= n_slots) break;
+#pragma unroll
+                for (int h = 0; h < kHB; ++h) {
+                    const float w = s_w[(p0 + i) * NH + hb + h];
+                    acc[h].x = fmaf(w, v[i][h].x, acc[h].x);
+                    acc[h].y = fmaf(w, v[i][h].y, acc[h].y);
+                    acc[h].z = fmaf(w, v[i][h].z, acc[h].z);
+                    acc[h].w = fmaf(w, v[i][h].w, acc[h].w);
+                }
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < kHB; ++h) out4[(hb + h) * (kDimCkv / 4)] = acc[h];
     }
 }
 
