@@ -13,6 +13,7 @@
 
 #include "mla_decode.h"
 #include "attn.cuh"
+#include "attn_e4m3.cuh"
 #include "attn_narrow.cuh"
 #include "attn_pair.cuh"
 #include "plan.h"
@@ -20,9 +21,9 @@
 // Tensor maps of the last run's buffers (re-encoded when an address changes).
 struct MapCache {
     bool valid = false;
-    const void *ckv = nullptr, *kpe = nullptr, *qn = nullptr, *qp = nullptr;
+    const void *ckv = nullptr, *kpe = nullptr, *qn = nullptr, *qp = nullptr, *scale = nullptr;
     int num_pages = 0;
-    CUtensorMap m_ckv, m_kpe, m_qp, m_v;
+    CUtensorMap m_ckv, m_kpe, m_qp, m_v, m_scale;
 };
 
 struct mla_plan_s {
@@ -118,6 +119,20 @@ bool make_map_codes(CUtensorMap* map, const void* base, uint64_t rows, uint32_t 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 1-D fp32 view of the per-token scales of an e4m3 cache ([num_pages * page_size]), box of one
+// page; coordinates past either end read zeros.
+bool make_map_scale(CUtensorMap* map, const float* base, uint64_t n, uint32_t box) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[1] = {n};
+    cuuint64_t strides[1] = {n * 4};   // unused for a 1-D map
+    cuuint32_t bx[1] = {box};
+    cuuint32_t es[1] = {1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, const_cast<float*>(base), dims, strides, bx, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 void build_image(mla_plan_s* p) {
@@ -139,6 +154,18 @@ cudaError_t launch_narrow(const mla_plan_s* p, const CUtensorMap& ckv, const CUt
     const int grid = p->d.num_units * p->d.head_groups;
     mla::mla_decode_narrow_kernel<HG, F8><<<grid, C::kThreads, C::kSmemBytes, stream>>>(
         ckv, kpe, prm, static_cast<const uint16_t*>(q_nope), static_cast<const uint16_t*>(q_pe));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_e4m3(const mla_plan_s* p, const MapCache& mc, const mla::AttnParams& prm, const void* q_nope,
+                        const void* q_pe, cudaStream_t stream) {
+    using C = mla::E4m3Cfg;
+    cudaError_t e = cudaFuncSetAttribute(mla::mla_decode_e4m3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int grid = p->d.num_units * p->d.head_groups;
+    mla::mla_decode_e4m3_kernel<<<grid, C::kThreads, C::kSmemBytes, stream>>>(
+        mc.m_ckv, mc.m_kpe, mc.m_scale, prm, static_cast<const uint16_t*>(q_nope), static_cast<const uint16_t*>(q_pe));
     return cudaGetLastError();
 }
 
@@ -167,7 +194,7 @@ mla_status_t run_checked(mla_plan_t plan, const void* q_nope, const void* q_pe, 
     // tensor maps depend only on the buffer addresses: re-encode when they change
     MapCache& mc = plan->maps;
     if (!mc.valid || mc.ckv != ckv_cache || mc.kpe != kpe_cache || mc.qn != q_nope || mc.qp != q_pe ||
-        mc.num_pages != num_pages) {
+        mc.scale != ckv_scale || mc.num_pages != num_pages) {
         const uint64_t rows = static_cast<uint64_t>(num_pages) * d.page_size;
         const uint64_t qrows = static_cast<uint64_t>(d.batch) * d.h_q;
         const uint32_t hg = static_cast<uint32_t>(d.heads_per_cta);
@@ -183,12 +210,14 @@ mla_status_t run_checked(mla_plan_t plan, const void* q_nope, const void* q_pe, 
                              : make_map_bf16(&mc.m_ckv, ckv_cache, mla::kDimCkv, rows, box);
         mc.valid = ok_ckv && make_map_bf16(&mc.m_kpe, kpe_cache, mla::kDimKpe, rows, box) &&
                    make_map_bf16(&mc.m_qp, q_pe, mla::kDimKpe, qrows, d.pair ? 128 : hg) &&
-                   (!d.pair || make_map_v_half(&mc.m_v, ckv_cache, rows, std::min(d.page_size, 32)));
+                   (!d.pair || make_map_v_half(&mc.m_v, ckv_cache, rows, std::min(d.page_size, 32))) &&
+                   (!d.e4m3 || make_map_scale(&mc.m_scale, ckv_scale, rows, static_cast<uint32_t>(d.page_size)));
         if (!mc.valid) return MLA_ERR_CUDA;
         mc.ckv = ckv_cache;
         mc.kpe = kpe_cache;
         mc.qn = q_nope;
         mc.qp = q_pe;
+        mc.scale = ckv_scale;
         mc.num_pages = num_pages;
     }
     mla::AttnParams prm;
@@ -210,14 +239,13 @@ mla_status_t run_checked(mla_plan_t plan, const void* q_nope, const void* q_pe, 
     prm.h_q = d.h_q;
     prm.page_size = d.page_size;
     prm.head_groups = d.head_groups;
+    prm.num_pages = num_pages;
     cudaError_t e;
-    if (d.narrow) {
-        if (f8)
-            e = d.h_q == 16 ? launch_narrow<16, true>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream)
-                            : launch_narrow<32, true>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream);
-        else
-            e = d.h_q == 16 ? launch_narrow<16, false>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream)
-                            : launch_narrow<32, false>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream);
+    if (d.e4m3) {
+        e = launch_e4m3(plan, mc, prm, q_nope, q_pe, stream);
+    } else if (d.narrow) {
+        e = d.h_q == 16 ? launch_narrow<16, false>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream)
+                        : launch_narrow<32, false>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream);
     } else if (d.pair) {
         e = d.h_q == 128 ? launch_pair<128>(plan, mc, prm, q_nope, stream)
                          : launch_pair<64>(plan, mc, prm, q_nope, stream);

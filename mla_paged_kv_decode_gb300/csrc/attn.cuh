@@ -47,6 +47,7 @@ struct AttnParams {
     int h_q;
     int page_size;
     int head_groups;
+    int num_pages;                // pages in the cache buffers
 };
 
 // Bounded wait on an mbarrier phase.  Returns false if the kernel is aborting

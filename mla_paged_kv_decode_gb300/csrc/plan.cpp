@@ -4,7 +4,7 @@
 // for its decode kernel without spelling out the partition; the reading used
 // here is the plainest one that balances SMs: lay every request's tokens end
 // to end in request order, cut the sequence into tiles of the kernel's tile size
-// (32 tokens for 16/32 heads, 128 for 64/128 heads; a request's last tile may
+// (32 tokens for the bf16 cache with 16/32 heads, 128 otherwise; a request's last tile may
 // be short), and cut the sequence into U contiguous ranges of equal cost, one
 // per CTA slot.  A tile costs 1; every request start after the first also costs
 // kSegmentCost tiles, because a CTA that crosses into a new request pays a second
@@ -23,12 +23,12 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 }  // namespace
 
 int heads_per_cta_for(int h_q, int kv_dtype) {
-    (void)kv_dtype;
+    if (kv_dtype == 1) return (h_q == 16 || h_q == 32) ? 16 : 0;
     switch (h_q) {
-        case 16: return 16;
-        case 32: return 32;
+        case 16:
+        case 32:
         case 64:
-        case 128: return kv_dtype == 0 ? h_q : 32;   // bf16: one cluster of two CTAs serves all heads
+        case 128: return h_q;
         default: return 0;
     }
 }
@@ -40,10 +40,10 @@ int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int ba
     if (page_size != 16 && page_size != 32 && page_size != 64) return 2;
     const int hg = heads_per_cta_for(h_q, kv_dtype);
     if (hg == 0) return 2;
-    if (kv_dtype == 1 && h_q > 32) return 2;   // the e4m3 cache is served by the narrow-head kernel only
     if (kv_indptr[0] != 0) return 1;
 
-    const bool narrow = h_q <= 32;
+    const bool e4m3 = kv_dtype == 1;
+    const bool narrow = h_q <= 32 && !e4m3;
     const int tile_tok = narrow ? kNarrowTileTokens : kTileTokens;
     std::vector<int64_t> len(batch), tiles(batch);
     int64_t total_tiles = 0;
@@ -72,7 +72,8 @@ int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int ba
     p.head_groups = h_q / hg;
     p.tile_tokens = tile_tok;
     p.narrow = narrow;
-    p.pair = h_q >= 64 && kv_dtype == 0;
+    p.pair = h_q >= 64 && !e4m3;
+    p.e4m3 = e4m3;
     const int ctas_per_unit = p.head_groups * (p.pair ? 2 : 1);
     int64_t units = std::max(1, num_sms / ctas_per_unit);
     units = std::min<int64_t>(units, std::max<int64_t>(total_tiles, 1));

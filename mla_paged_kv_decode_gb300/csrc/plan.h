@@ -46,6 +46,7 @@ struct PlanData {
     int tile_tokens = 0;              // plan granularity = the kernel's tile
     bool narrow = false;              // h_q <= 32: warp-MMA kernel, else tcgen05 kernel
     bool pair = false;                // h_q 64/128, bf16 cache: two-CTA cluster kernel, 2 CTAs per unit
+    bool e4m3 = false;                // e4m3 cache: tcgen05 kind::f8f6f4 kernel, 16 heads per CTA
     int segment_cost = 0;             // partition cost of a request start, in tiles
     std::vector<int32_t> unit_ptr;
     std::vector<Segment> segments;
@@ -58,8 +59,9 @@ struct PlanData {
 int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int batch, int h_q, int page_size,
                int num_sms, int kv_dtype, PlanData* out);
 
-// Heads handled by one CTA for a given h_q (0 if unsupported): all of them for the
-// narrow-head kernel (h_q <= 32), 32-head groups for the tcgen05 kernel.
+// Heads handled by one CTA for a given h_q and cache type (0 if unsupported): bf16 cache, all
+// of them (the narrow-head kernel for h_q <= 32, the two-CTA kernel for 64/128); e4m3 cache,
+// 16 (h_q 16 or 32).
 int heads_per_cta_for(int h_q, int kv_dtype);
 
 }  // namespace mla

@@ -29,16 +29,19 @@ def _lens_to_arrays(lens, P):
     return indptr, last
 
 
-def _check_plan(lens, h_q, P, sms):
-    TILE = 32 if h_q <= 32 else 128          # the kernel's tile: narrow (warp MMA) or tcgen05
+def _check_plan(lens, h_q, P, sms, kv_dtype=mla.MLA_KV_BF16):
+    e4m3 = kv_dtype == mla.MLA_KV_FP8_E4M3
+    # the kernel's tile: 32 tokens for the narrow (warp MMA) bf16 kernel, 128 for the tcgen05 ones
+    TILE = 32 if (h_q <= 32 and not e4m3) else 128
     indptr, last = _lens_to_arrays(lens, P)
-    plan = mla.mla_decode_plan(torch.from_numpy(indptr), torch.from_numpy(last), len(lens), h_q, P, sms)
+    plan = mla.mla_decode_plan(torch.from_numpy(indptr), torch.from_numpy(last), len(lens), h_q, P, sms, kv_dtype)
     segs, uptr = mla.mla_plan_get_segments(plan)
     hg = mla.mla_plan_heads_per_cta(plan)
+    assert hg == (16 if e4m3 else h_q)
     groups = h_q // hg
     units = len(uptr) - 1
     assert units == mla.mla_plan_num_units(plan)
-    pair = 2 if h_q >= 64 else 1             # 64/128 heads: a cluster of two CTAs per unit
+    pair = 2 if (h_q >= 64 and not e4m3) else 1   # bf16 64/128 heads: a cluster of two CTAs per unit
     assert mla.mla_plan_num_ctas(plan) == units * groups * pair
     assert units <= max(1, sms // (groups * pair))
     # coverage: each request's tokens exactly once, pieces in token order
@@ -121,6 +124,25 @@ def test_random_plans():
         B = rng.randint(1, 80)
         lens = [rng.choice([0, 1, rng.randint(1, 300), rng.randint(1, 20000)]) for _ in range(B)]
         _check_plan(lens, rng.choice([16, 32, 64, 128]), rng.choice([16, 32, 64]), rng.choice([1, 7, 64, 152]))
+
+
+def test_e4m3_plans():
+    """The 8-bit cache runs on the tcgen05 kernel: 128-token tiles, 16 heads per CTA."""
+    segs, uptr = _check_plan([16384] * 64, 16, 64, 152, mla.MLA_KV_FP8_E4M3)
+    assert len(uptr) - 1 == 152
+    segs, uptr = _check_plan([4096] * 8, 32, 64, 152, mla.MLA_KV_FP8_E4M3)
+    assert len(uptr) - 1 == 152 // 2          # two 16-head CTAs per unit
+    rng = random.Random(99)
+    for _ in range(20):
+        B = rng.randint(1, 60)
+        lens = [rng.choice([0, 1, rng.randint(1, 300), rng.randint(1, 20000)]) for _ in range(B)]
+        _check_plan(lens, rng.choice([16, 32]), rng.choice([16, 32, 64]), rng.choice([1, 7, 64, 152]),
+                    mla.MLA_KV_FP8_E4M3)
+    indptr, last = _lens_to_arrays([100], 16)
+    for h_q in (64, 128):                     # wider heads have no 8-bit kernel
+        with pytest.raises(RuntimeError):
+            mla.mla_decode_plan(torch.from_numpy(indptr), torch.from_numpy(last), 1, h_q, 16, 152,
+                                mla.MLA_KV_FP8_E4M3)
 
 
 def test_plan_is_deterministic():
