@@ -65,7 +65,8 @@ typedef enum {
 /* Build a balanced split-KV work list (host only, no device call).
  *
  * Work is measured in tokens.  Requests are laid out in order, cut into
- * tiles of 128 tokens, and the tile sequence is partitioned into contiguous
+ * tiles of the kernel's size (32 tokens for a bf16 cache with h_q 16 or 32,
+ * else 128), and the tile sequence is partitioned into contiguous
  * ranges of near-equal cost, one per CTA slot; a request cut across slots
  * becomes several split pieces whose partial (out, lse) are merged after
  * the attention kernel (FlashMLA PR #233, "balanced scheduler").
@@ -149,7 +150,7 @@ int mla_plan_num_units(mla_plan_t plan);      /* work units (CTA slots, or CTA p
 int mla_plan_num_segments(mla_plan_t plan);   /* (request, token range) pieces */
 int mla_plan_num_partials(mla_plan_t plan);   /* split pieces that go through the combine */
 int mla_plan_heads_per_cta(mla_plan_t plan);
-/* Partition cost, in tiles (32 tokens for h_q <= 32, else 128), that the balanced plan
+/* Partition cost, in tiles (32 tokens for a bf16 cache with h_q <= 32, else 128), that the balanced plan
  * charges for each request start after the first: CTA slots are cut so that tiles plus
  * these costs are equal to within one tile. */
 int mla_plan_segment_cost_tiles(mla_plan_t plan);

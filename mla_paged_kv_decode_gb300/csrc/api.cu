@@ -9,6 +9,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <utility>
 #include <vector>
 
 #include "mla_decode.h"
@@ -95,22 +96,12 @@ bool make_map_v_half(CUtensorMap* map, const void* base, uint64_t rows, uint32_t
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// e4m3 codes of the ckv cache ([rows, 512] bytes) for the narrow kernel: with whole 32-token
-// stages a 3-D view (128 code columns, rows, 4 chunks; strides 512 B, 128 B) whose box lands
-// as [chunk][row][128 B]; otherwise a 2-D view with 128-column boxes, one per chunk.  Both
-// with the 128-byte swizzle.
-bool make_map_codes(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows, bool chunked) {
+// e4m3 codes of the ckv cache ([rows, 512] bytes) for the e4m3 kernel: a 2-D view with boxes
+// of 128 code columns (one 128-dim chunk) x box_rows rows, 128-byte swizzle.
+bool make_map_codes(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
-    cuuint32_t es[3] = {1, 1, 1};
-    if (chunked) {
-        cuuint64_t dims[3] = {128, rows, 4};
-        cuuint64_t strides[2] = {mla::kDimCkv, 128};
-        cuuint32_t box[3] = {128, box_rows, 4};
-        return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-    }
+    cuuint32_t es[2] = {1, 1};
     cuuint64_t dims[2] = {mla::kDimCkv, rows};
     cuuint64_t strides[1] = {mla::kDimCkv};
     cuuint32_t box[2] = {128, box_rows};
@@ -144,17 +135,35 @@ void build_image(mla_plan_s* p) {
                     sizeof(mla::Segment) * p->d.segments.size());
 }
 
-template <int HG, bool F8>
+// Launch with programmatic stream serialization: the kernel's prologue (barriers, TMEM, its
+// slice of the plan) may overlap the tail of the previous kernel in the stream; the kernels
+// wait for that kernel (griddepcontrol.wait) before they touch any buffer of the caller.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), int grid, int threads, int smem, cudaStream_t stream,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+template <int HG>
 cudaError_t launch_narrow(const mla_plan_s* p, const CUtensorMap& ckv, const CUtensorMap& kpe, const mla::AttnParams& prm,
                           const void* q_nope, const void* q_pe, cudaStream_t stream) {
-    using C = mla::NarrowCfg<HG, F8>;
-    cudaError_t e = cudaFuncSetAttribute(mla::mla_decode_narrow_kernel<HG, F8>,
+    using C = mla::NarrowCfg<HG>;
+    cudaError_t e = cudaFuncSetAttribute(mla::mla_decode_narrow_kernel<HG>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int grid = p->d.num_units * p->d.head_groups;
-    mla::mla_decode_narrow_kernel<HG, F8><<<grid, C::kThreads, C::kSmemBytes, stream>>>(
-        ckv, kpe, prm, static_cast<const uint16_t*>(q_nope), static_cast<const uint16_t*>(q_pe));
-    return cudaGetLastError();
+    return launch_pdl(mla::mla_decode_narrow_kernel<HG>, grid, C::kThreads, C::kSmemBytes, stream, ckv, kpe, prm,
+                      static_cast<const uint16_t*>(q_nope), static_cast<const uint16_t*>(q_pe));
 }
 
 cudaError_t launch_e4m3(const mla_plan_s* p, const MapCache& mc, const mla::AttnParams& prm, const void* q_nope,
@@ -164,9 +173,8 @@ cudaError_t launch_e4m3(const mla_plan_s* p, const MapCache& mc, const mla::Attn
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int grid = p->d.num_units * p->d.head_groups;
-    mla::mla_decode_e4m3_kernel<<<grid, C::kThreads, C::kSmemBytes, stream>>>(
-        mc.m_ckv, mc.m_kpe, mc.m_scale, prm, static_cast<const uint16_t*>(q_nope), static_cast<const uint16_t*>(q_pe));
-    return cudaGetLastError();
+    return launch_pdl(mla::mla_decode_e4m3_kernel, grid, C::kThreads, C::kSmemBytes, stream, mc.m_ckv, mc.m_kpe,
+                      mc.m_scale, prm, static_cast<const uint16_t*>(q_nope), static_cast<const uint16_t*>(q_pe));
 }
 
 template <int HQ>
@@ -177,9 +185,8 @@ cudaError_t launch_pair(const mla_plan_s* p, const MapCache& mc, const mla::Attn
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int grid = 2 * p->d.num_units;   // clusters of two CTAs (the kernel's cluster dimensions)
-    mla::mla_decode_pair_kernel<HQ><<<grid, C::kThreads, C::kSmemBytes, stream>>>(
-        mc.m_ckv, mc.m_kpe, mc.m_qp, mc.m_v, prm, static_cast<const uint16_t*>(q_nope));
-    return cudaGetLastError();
+    return launch_pdl(mla::mla_decode_pair_kernel<HQ>, grid, C::kThreads, C::kSmemBytes, stream, mc.m_ckv, mc.m_kpe,
+                      mc.m_qp, mc.m_v, prm, static_cast<const uint16_t*>(q_nope));
 }
 
 // Argument checks, tensor maps and the launch shared by mla_decode_run and
@@ -204,7 +211,7 @@ mla_status_t run_checked(mla_plan_t plan, const void* q_nope, const void* q_pe, 
         const bool chunked = d.narrow && box == static_cast<uint32_t>(mla::kNarrowStageTok);
         bool ok_ckv;
         if (f8)
-            ok_ckv = make_map_codes(&mc.m_ckv, ckv_cache, rows, box, chunked);
+            ok_ckv = make_map_codes(&mc.m_ckv, ckv_cache, rows, box);
         else
             ok_ckv = chunked ? make_map_ckv_chunked(&mc.m_ckv, ckv_cache, rows, box)
                              : make_map_bf16(&mc.m_ckv, ckv_cache, mla::kDimCkv, rows, box);
@@ -244,8 +251,8 @@ mla_status_t run_checked(mla_plan_t plan, const void* q_nope, const void* q_pe, 
     if (d.e4m3) {
         e = launch_e4m3(plan, mc, prm, q_nope, q_pe, stream);
     } else if (d.narrow) {
-        e = d.h_q == 16 ? launch_narrow<16, false>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream)
-                        : launch_narrow<32, false>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream);
+        e = d.h_q == 16 ? launch_narrow<16>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream)
+                        : launch_narrow<32>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream);
     } else if (d.pair) {
         e = d.h_q == 128 ? launch_pair<128>(plan, mc, prm, q_nope, stream)
                          : launch_pair<64>(plan, mc, prm, q_nope, stream);

@@ -174,6 +174,10 @@ __global__ void __launch_bounds__(E4m3Cfg::kThreads, 1)
     const int seg_end = prm.unit_ptr[unit + 1];
     const int P = prm.page_size;
 
+    // Prologue before the previous kernel in the stream has finished (programmatic dependent
+    // launch): barriers, TMEM and this CTA's slice of the plan, which only the plan commit
+    // writes.  Every read of the caller's buffers and every write comes after grid_dep_wait.
+    grid_dep_launch();
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kSlots; ++i) {
             mbar_init(&misc->full[i], 1);
@@ -198,6 +202,7 @@ __global__ void __launch_bounds__(E4m3Cfg::kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
+    grid_dep_wait();
     tc_fence_after();
     const uint32_t tmem = misc->tmem_base;
     int* abort_flag = &misc->abort_flag;

@@ -1,45 +1,41 @@
-// MLA paged decode attention for narrow head counts (16 or 32 query heads per
-// CTA) on sm_103a: TMA page staging into an mbarrier ring, tensor-core math
+// MLA paged decode attention over a bf16 latent cache for narrow head counts (16 or 32
+// query heads per CTA) on sm_103a: TMA page staging into an mbarrier ring, tensor-core math
 // with warp-level mma.sync (m16n8k16, bf16 in, fp32 accumulate).
 //
-// Why warp MMA here: the score contraction of a 16-head request has only 16
-// rows per query, and a tcgen05.mma costs 60-150 SM cycles per instruction
-// whatever its N (measured on GB300), so a 16-column tcgen05 tile runs at a
-// small fraction of the tensor pipe and cannot keep up with HBM.  The warp
-// MMA has no such floor: 16 heads x 1088 MACs per cached token is ~17 cycles
-// per token per SM, against the ~49 cycles per token an SM may spend at full
-// HBM bandwidth.  The wide-head path (64/128 heads) uses tcgen05 (attn.cuh).
+// Why warp MMA here: the score contraction of a 16-head request has 16 rows per query, and a
+// tcgen05.mma costs ~97 SM cycles per instruction whatever its N up to 128 (measured on this
+// GPU), so tcgen05 tiles of 16 heads and 128 tokens would need ~68 instructions per tile of
+// bf16 operands.  The warp MMA has no such floor: 16 heads x 1088 MACs per cached token is
+// ~17 cycles per token per SM, against the ~49 cycles per token an SM may spend at full HBM
+// bandwidth.  The 64/128-head path (attn_pair.cuh) and the e4m3 cache (attn_e4m3.cuh) run
+// on tcgen05.
 //
-// Absorbed MLA decode is MQA with one KV head: key [ckv | kpe] (576), value
-// ckv (512) ("Benchmarking MLA", FlashInfer issue #700).  The layout of the
-// work follows the split-K idea of FlashMLA PR #233's sm86 kernel ("Q in
-// registers, split-K QK inside the CTA, a multi-stage ... KV ring"), rebuilt
-// for TMA and the GB300 memory system:
+// Absorbed MLA decode is MQA with one KV head: key [ckv | kpe] (576), value ckv (512)
+// ("Benchmarking MLA", FlashInfer issue #700).  The layout of the work follows the split-K
+// idea of FlashMLA PR #233's sm86 kernel ("Q in registers, split-K QK inside the CTA, a
+// multi-stage ... KV ring"), rebuilt for TMA and the GB300 memory system:
 //
-//   * a CTA owns HG heads of every segment of its plan slot and walks it in
-//     64-token tiles; a tile is two 32-token ring stages of 36 KB (8 ckv
-//     chunks of 64 dims + kpe, 128-byte swizzle, one TMA box per page piece);
-//   * warp 0 is the TMA producer and also prefetches the pages of the tile two
-//     ahead into L2 (cp.async.bulk.prefetch), so the ring only covers L2
-//     latency;
-//   * 4 compute warps per 16-head group: warp k holds q for dims
-//     [144k, 144k + 144) in registers and computes the partial scores of all
-//     64 tokens over those dims; the 4 partials go through shared memory and
-//     every warp sums them in the same order, so all 4 hold identical scores;
-//   * each warp then runs the same online softmax (row max via quad shuffles)
-//     and keeps P in registers as the A operand of O += P V for its own 128
-//     latent dims (V loaded with ldmatrix.trans).
+//   * a CTA owns HG heads of every segment of its plan slot and walks it in 32-token tiles,
+//     one ring stage each (36 KB: 8 ckv chunks of 64 dims + kpe, 128-byte swizzle; one 3-D
+//     TMA box per stage when a page holds it, else one 2-D box per chunk and page piece);
+//   * warpgroup 0 is the producer (warp 0 issues the copies); two compute groups of 4 warps
+//     take the math.  With 16 heads the groups take alternate tiles of a segment (token
+//     groups) and merge their (m, l, O) at its end; with 32 heads each group takes 16 heads;
+//   * in a group, warp k holds q for dims [144k, 144k + 144) in registers and computes the
+//     partial scores of the tile over those dims; the 4 partials go through shared memory
+//     and warp k finishes the scores of tokens [8k, 8k + 8);
+//   * the online softmax keeps a lazy running max (moved, and O rescaled, only when a tile
+//     exceeds it by more than 2^8), P goes through shared memory as bf16 A fragments, and
+//     warp k accumulates O += P V for its own 128 latent dims (V read with ldmatrix.trans).
 //
-// The running max is updated every tile (rescaling O in registers is cheap
-// here).  A split request's pieces write normalised partials; the last CTA to
-// finish one merges them in slot order (FlashMLA PR #233, "deterministic
-// combine"), as in attn.cuh.  Every mbarrier wait is bounded.
+// A split request's pieces write normalised partials; the last CTA to finish one merges them
+// in slot order (FlashMLA PR #233, "deterministic combine"; attn.cuh).  Every mbarrier wait
+// is bounded.
 #pragma once
 
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
-#include <cuda_fp16.h>
 
 #include "attn.cuh"
 #include "plan.h"
@@ -50,7 +46,7 @@ namespace mla {
 constexpr int kNarrowTile = 32;        // tokens per tile (= one ring stage)
 constexpr int kNarrowStageTok = 32;    // tokens per ring stage
 
-template <int HG, bool F8>
+template <int HG>
 struct NarrowCfg {
     static_assert(HG == 16 || HG == 32, "heads per CTA");
     static constexpr int kHeadGroups = HG / 16;               // 16-head groups
@@ -66,16 +62,13 @@ struct NarrowCfg {
     static constexpr uint32_t kComputeRegs = 208;
     static_assert(128 * kProducerRegs + 32 * kComputeWarps * kComputeRegs <= 65536 / kThreads / 8 * 8 * kThreads,
                   "register split");
-    // ring stages, filled by TMA.  bf16 cache: 8 value chunks (64 dims x 32 tokens, 128-byte
-    // swizzle) + the kpe chunk = 36 KB.  e4m3 cache: 4 code chunks (128 dims x 32 tokens, one
-    // byte each, 128-byte swizzle) + kpe (bf16, same layout as above) + 32 fp32 scales = 20.1 KB,
-    // padded to the 1 KB swizzle alignment; the compute warps read the codes directly.
+    // ring stages, filled by TMA: 8 value chunks (64 dims x 32 tokens, 128-byte swizzle) + the
+    // kpe chunk = 36 KB
     static constexpr int kChunkBytes = kNarrowStageTok * 128;  // 4 KB: 32 rows of 128 B
-    static constexpr int kKpeOff = F8 ? 4 * kChunkBytes : 8 * kChunkBytes;
-    static constexpr int kScaleOff = kKpeOff + kChunkBytes;    // e4m3 cache only
-    static constexpr int kStageBytes = F8 ? 21 * 1024 : 9 * kChunkBytes;
-    static constexpr int kStages = F8 ? 9 : 5;
-    static constexpr int kStageLoadBytes = kNarrowStageTok * (F8 ? 512 + 128 + 4 : 1152);
+    static constexpr int kKpeOff = 8 * kChunkBytes;
+    static constexpr int kStageBytes = 9 * kChunkBytes;
+    static constexpr int kStages = 5;
+    static constexpr int kStageLoadBytes = kNarrowStageTok * 1152;
     static constexpr int kPartBytes = 4 * 32 * 16 * 4;         // per group: 4 warps x 32 lanes x 16 floats = 8 KB
     static constexpr int kPRowBytes = 80;                       // P row: 32 16-bit tokens + 16 B pad (conflict-free ldmatrix)
     static constexpr int kGroupScratch = 16 * kPRowBytes + 4 * 16 * 4;   // P tile + per-warp row maxima
@@ -85,7 +78,7 @@ struct NarrowCfg {
     static constexpr int kOffMisc = kOffScratch + kGroups * kGroupScratch;
     static constexpr int kMiscBytes = 3072;
     static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;
-    static_assert((!F8 || kScaleOff + kNarrowStageTok * 4 <= kStageBytes) && kStageBytes % 1024 == 0, "stage layout");
+    static_assert(kStageBytes % 1024 == 0, "stage layout");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     // the token-group merge passes one group's O (16 heads x 512 dims fp32) in two halves
     // through the partial-score buffers of both groups
@@ -93,7 +86,7 @@ struct NarrowCfg {
 };
 
 struct NarrowMisc {
-    uint64_t full[9], empty[9];
+    uint64_t full[5], empty[5];
     int abort_flag;
     int merge_flag[2];
     float mrg_max[2][16];
@@ -114,13 +107,6 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                  : "r"(addr));
 }
 
-__device__ __forceinline__ void mma_f16_16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 __device__ __forceinline__ void mma_bf16_16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
@@ -134,40 +120,19 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
-    __half2 v = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-}
-
-// two bf16 (low half first) -> two f16, rounded to nearest (exact for values in the f16
-// normal range, which holds for the query entries of the e4m3 path)
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
-    return pack_f16(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
-}
-
-// two e4m3 codes in the low 16 bits (lower byte first) -> two f16 (lower byte in the low half);
-// exact, every e4m3 value being an f16 value
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes) {
-    uint32_t r;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<uint16_t>(codes & 0xffffu)));
-    return r;
-}
-
 // Address of the 16-byte unit holding (row, dims 8u..8u+7) of a 64-dim chunk stored as
 // rows of 128 bytes with the 128-byte swizzle (unit index XOR row % 8).
 __device__ __forceinline__ uint32_t sw_unit(uint32_t chunk_base, uint32_t row, uint32_t unit) {
     return chunk_base + row * 128 + ((unit ^ (row & 7)) << 4);
 }
 
-// F8: the cache's ckv holds e4m3 codes with an fp32 scale per token (tm_ckv then maps the
-// codes as bytes, prm.ckv_scale the scales).
-template <int HG, bool F8>
-__global__ void __launch_bounds__(NarrowCfg<HG, F8>::kThreads, 1)
+template <int HG>
+__global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
     mla_decode_narrow_kernel(const __grid_constant__ CUtensorMap tm_ckv, const __grid_constant__ CUtensorMap tm_kpe,
                              const AttnParams prm, const uint16_t* __restrict__ q_nope,
                              const uint16_t* __restrict__ q_pe) {
-    using C = NarrowCfg<HG, F8>;
-    static_assert(sizeof(NarrowMisc) <= C::kMiscBytes, "misc region");
+    using C = NarrowCfg<HG>;
+    static_assert(sizeof(NarrowMisc) <= C::kMiscBytes && C::kStages <= 5, "misc region");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stage_base = smem + C::kOffStage;
@@ -183,6 +148,10 @@ __global__ void __launch_bounds__(NarrowCfg<HG, F8>::kThreads, 1)
     const int P = prm.page_size;
     const int box_rows = P < kNarrowStageTok ? P : kNarrowStageTok;
 
+    // Prologue before the previous kernel in the stream has finished (programmatic dependent
+    // launch): barrier set-up and this CTA's slice of the plan, which only the plan commit
+    // writes.  Every read of the caller's buffers and every write comes after grid_dep_wait.
+    grid_dep_launch();
     if (threadIdx.x == 0) {
         MLA_TRACE_CTA(0);
 #ifdef MLA_TRACE
@@ -200,18 +169,17 @@ __global__ void __launch_bounds__(NarrowCfg<HG, F8>::kThreads, 1)
         }
         misc->abort_flag = 0;
         fence_mbarrier_init();
+        prefetch_tensormap(&tm_ckv);
+        prefetch_tensormap(&tm_kpe);
     }
     __syncthreads();
+    grid_dep_wait();
 
     if (warp < C::kProducerWarps) regs_dec<C::kProducerRegs>();
     else regs_inc<C::kComputeRegs>();
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            prefetch_tensormap(&tm_ckv);
-            prefetch_tensormap(&tm_kpe);
-        }
         uint32_t scount = 0, tile_idx = 0;
         bool ok = true;
         TileCursorT<kNarrowTile> cur;
@@ -243,27 +211,14 @@ __global__ void __launch_bounds__(NarrowCfg<HG, F8>::kThreads, 1)
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) break;
                 uint8_t* dst = stage_base + s * C::kStageBytes;
-                // bytes per token: bf16 ckv + kpe = 1152; e4m3 codes + kpe + scale = 644
+                // bytes per token: bf16 ckv + kpe = 1152
                 if (lane == 0)
                     mbar_arrive_expect_tx(bar_full, static_cast<uint32_t>(nbox * box_rows * (C::kStageLoadBytes / kNarrowStageTok)));
                 if (lane == 0) MLA_TRACE_EVENT(st == 0 ? 0 : 1, tile_idx);
                 for (int bx = 0; bx < nbox; ++bx) {
                     const int t = t_st + bx * box_rows;
                     const int pg = __shfl_sync(0xffffffffu, win_page, (t / P - win_base) & 31);
-                    if (lane == 0 && F8) {
-                        const int y = pg * P + (t % P);
-                        if (box_rows == kNarrowStageTok) {
-                            // all 4 code chunks (128 dims each) in one 3-D box -> [chunk][row][128 B]
-                            tma_load_3d(dst, &tm_ckv, bar_full, 0, y, 0);
-                        } else {
-                            for (int c = 0; c < 4; ++c)
-                                tma_load_2d(dst + c * (kNarrowStageTok * 128) + bx * box_rows * 128, &tm_ckv, bar_full,
-                                            c * 128, y);
-                        }
-                        tma_load_2d(dst + C::kKpeOff + bx * box_rows * 128, &tm_kpe, bar_full, 0, y);
-                        bulk_load(dst + C::kScaleOff + bx * box_rows * 4, prm.ckv_scale + static_cast<size_t>(y),
-                                  static_cast<uint32_t>(box_rows * 4), bar_full);
-                    } else if (lane == 0) {
+                    if (lane == 0) {
                         const int y = pg * P + (t % P);
                         if (box_rows == kNarrowStageTok) {
                             // all 8 ckv chunks in one 3-D box (64 dims, 32 rows, 8 chunks), which lands as
@@ -318,18 +273,10 @@ __global__ void __launch_bounds__(NarrowCfg<HG, F8>::kThreads, 1)
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
                     const int row = g + ((r & 1) ? 8 : 0);
-                    // fragment k index 2 c4 + {0, 1} (+ 8): the bf16 layout.  e4m3 latent dims: a
-                    // thread's four codes of a 16-dim step are adjacent bytes (4 c4 .. 4 c4 + 3), so
-                    // the step's k order is permuted to match: k 2 c4 + j <-> dim 4 c4 + j and
-                    // k 2 c4 + 8 + j <-> dim 4 c4 + 2 + j
-                    const int dim = (F8 && kd < kDimCkv) ? kd + 4 * c4 + ((r & 2) ? 2 : 0)
-                                                         : kd + 2 * c4 + ((r & 2) ? 8 : 0);
+                    const int dim = kd + 2 * c4 + ((r & 2) ? 8 : 0);   // fragment k index 2 c4 + {0, 1} (+ 8)
                     const uint16_t* src = dim < kDimCkv ? q_nope + (qrow0 + row) * kDimCkv + dim
                                                         : q_pe + (qrow0 + row) * kDimKpe + (dim - kDimCkv);
                     qa[ks][r] = *reinterpret_cast<const uint32_t*>(src);
-                    // e4m3 cache: the latent part of the score runs on f16 operands (the cache
-                    // expands exactly to f16), the rope part stays bf16
-                    if (F8 && kd < kDimCkv) qa[ks][r] = bf16x2_to_f16x2(qa[ks][r]);
                 }
             }
         };
@@ -349,10 +296,6 @@ __global__ void __launch_bounds__(NarrowCfg<HG, F8>::kThreads, 1)
             for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
             float m_run[2] = {-INFINITY, -INFINITY};   // rows g and g + 8 (log2 domain)
             float l_part[2] = {0.f, 0.f};
-            // e4m3 cache: O accumulates p * (scale_t / r) * code_t with r the largest scale of
-            // this group's first tile of the segment, which keeps the f16 P operand near 1
-            float r_scale = 1.f, inv_r = 1.f;
-            bool first_tile = true;
             int tile_in_seg = 0;
             for (int t0 = sg.t_begin; t0 < sg.t_end; t0 += kNarrowTile, ++tile_in_seg) {
                 const int ntok = min(kNarrowTile, sg.t_end - t0);
@@ -381,41 +324,14 @@ __global__ void __launch_bounds__(NarrowCfg<HG, F8>::kThreads, 1)
                 ok = !named_barrier_or(named_bar, 128, !ok || *reinterpret_cast<volatile int*>(&misc->abort_flag));
                 if (!ok) break;
                 if (cw == 0 && lane == 0) MLA_TRACE_EVENT(2, (uint32_t)tile_in_seg);
-                // e4m3 cache: the stage's per-token scales, 0 past the tile's last token (those slots
-                // may hold anything, NaN included)
-                const float* stage_scale = reinterpret_cast<const float*>(stage_base + sl * C::kStageBytes + C::kScaleOff);
-                auto tok_scale = [&](int t) { return t < ntok ? stage_scale[t] : 0.f; };
-                if (F8 && first_tile) {
-                    const float mx = warp_max(tok_scale(lane));
-                    r_scale = mx > 0.f ? mx : 1.f;
-                    inv_r = 1.f / r_scale;
-                }
-                first_tile = false;
                 // ---- partial scores over this warp's 144 dims for the 4 n8 token tiles
-                float sc[4][4], sc_pe[4][4];   // sc_pe: the rope dims (e4m3 cache only, warp 3)
+                float sc[4][4];
 #pragma unroll
-                for (int n = 0; n < 4; ++n) {
-                    sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-                    sc_pe[n][0] = sc_pe[n][1] = sc_pe[n][2] = sc_pe[n][3] = 0.f;
-                }
+                for (int n = 0; n < 4; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
 #pragma unroll
                 for (int ks = 0; ks < 9; ++ks) {
                     const int kd = kr * 144 + ks * 16;
-                    if (F8 && kd < kDimCkv) {
-                        // e4m3 latent dims: one 16-byte code unit (16 dims) of 32 tokens; matrix j of
-                        // the x4 load is tokens 8j .. 8j + 7, read as 8 x 8 16-bit elements, so each
-                        // thread gets token 8j + g's codes for dims kd + 4 c4 .. + 3
-                        uint32_t rc[4];
-                        ldsm_x4(sw_unit(st_addr + (kd >> 7) * C::kChunkBytes, lane, (kd & 127) >> 4), rc[0], rc[1],
-                                rc[2], rc[3]);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            if (j * 8 < ntok)
-                                mma_f16_16816(sc[j], qa[ks], e4m3x2_to_f16x2(rc[j]), e4m3x2_to_f16x2(rc[j] >> 16));
-                        }
-                        continue;
-                    }
-                    // bf16 16-dim step: latent (bf16 cache) or rope (both caches)
+                    // 16-dim step: latent or rope
                     const uint32_t chunk_base = kd < kDimCkv ? st_addr + (kd >> 6) * C::kChunkBytes
                                                              : st_addr + C::kKpeOff;
                     const int unit0 = (kd & 63) >> 3;          // 16-byte unit of the k-step's first 8 dims
@@ -429,22 +345,9 @@ __global__ void __launch_bounds__(NarrowCfg<HG, F8>::kThreads, 1)
 #pragma unroll
                     for (int np = 0; np < 2; ++np) {
                         if (np * 16 < ntok) {
-                            float* c0 = F8 ? sc_pe[2 * np] : sc[2 * np];
-                            float* c1 = F8 ? sc_pe[2 * np + 1] : sc[2 * np + 1];
-                            mma_bf16_16816(c0, qa[ks], bf[np][0], bf[np][1]);
-                            mma_bf16_16816(c1, qa[ks], bf[np][2], bf[np][3]);
+                            mma_bf16_16816(sc[2 * np], qa[ks], bf[np][0], bf[np][1]);
+                            mma_bf16_16816(sc[2 * np + 1], qa[ks], bf[np][2], bf[np][3]);
                         }
-                    }
-                }
-                if (F8) {
-                    // latent part times the token's scale, plus the rope part
-#pragma unroll
-                    for (int n = 0; n < 4; ++n) {
-                        const float s0 = tok_scale(8 * n + 2 * c4), s1 = tok_scale(8 * n + 2 * c4 + 1);
-                        sc[n][0] = fmaf(sc[n][0], s0, sc_pe[n][0]);
-                        sc[n][1] = fmaf(sc[n][1], s1, sc_pe[n][1]);
-                        sc[n][2] = fmaf(sc[n][2], s0, sc_pe[n][2]);
-                        sc[n][3] = fmaf(sc[n][3], s1, sc_pe[n][3]);
                     }
                 }
                 // ---- exchange partials within the group; warp kr finishes the scores of n8 tile kr
@@ -454,16 +357,12 @@ __global__ void __launch_bounds__(NarrowCfg<HG, F8>::kThreads, 1)
                     for (int i = 0; i < 4; ++i) dst[i * 32 + lane] = make_float4(sc[i][0], sc[i][1], sc[i][2], sc[i][3]);
                 }
                 // zero the value rows of a partial 16-token step (stale or NaN bytes past the last
-                // token): 8 bf16 chunks or 4 code chunks of 128 B per row
+                // token): 8 chunks of 128 B per row
                 if (ntok < kNarrowTile && (ntok & 15)) {
                     const int r_end = (ntok + 15) & ~15;
                     for (int tok = ntok + kr; tok < r_end; tok += 4) {
                         uint4* rowp = reinterpret_cast<uint4*>(stage_base + (st_addr - stage0) + tok * 128);
-                        if (F8) {
-                            rowp[(lane >> 3) * (C::kChunkBytes / 16) + (lane & 7)] = make_uint4(0, 0, 0, 0);
-                        } else {
-                            for (int c = 0; c < 8; ++c) rowp[c * (C::kChunkBytes / 16) + (lane & 7)] = make_uint4(0, 0, 0, 0);
-                        }
+                        for (int c = 0; c < 8; ++c) rowp[c * (C::kChunkBytes / 16) + (lane & 7)] = make_uint4(0, 0, 0, 0);
                     }
                 }
                 named_barrier_sync(named_bar, 128);
@@ -520,17 +419,7 @@ __global__ void __launch_bounds__(NarrowCfg<HG, F8>::kThreads, 1)
                     const float p3 = fast_exp2(fmaf(s4[3], prm.scale_log2, -m_run[1]));
                     l_part[0] += p0 + p1;
                     l_part[1] += p2 + p3;
-                    uint32_t w0, w1;
-                    if (F8) {
-                        // P operand: p * scale_t / r (f16); the row sums above use p itself
-                        const float s0 = tok_scale(kr * 8 + 2 * c4) * inv_r;
-                        const float s1 = tok_scale(kr * 8 + 2 * c4 + 1) * inv_r;
-                        w0 = pack_f16(p0 * s0, p1 * s1);
-                        w1 = pack_f16(p2 * s0, p3 * s1);
-                    } else {
-                        w0 = pack_bf16(p0, p1);
-                        w1 = pack_bf16(p2, p3);
-                    }
+                    const uint32_t w0 = pack_bf16(p0, p1), w1 = pack_bf16(p2, p3);
                     *reinterpret_cast<uint32_t*>(pbuf + g * C::kPRowBytes + (kr * 8 + 2 * c4) * 2) = w0;
                     *reinterpret_cast<uint32_t*>(pbuf + (g + 8) * C::kPRowBytes + (kr * 8 + 2 * c4) * 2) = w1;
                 }
@@ -548,28 +437,6 @@ __global__ void __launch_bounds__(NarrowCfg<HG, F8>::kThreads, 1)
                 for (int kt = 0; kt < 2; ++kt) {
                     if (kt * 16 >= ntok) break;
                     const int tok = kt * 16 + (lane & 7) + ((lane & 8) ? 8 : 0);
-                    if (F8) {
-                        // e4m3 codes of this warp's 128 dims = code chunk kr.  Read as 16-bit elements
-                        // (pairs of dims) with the transposing load: matrix (unit U, token half h)
-                        // gives each thread tokens 2 c4, 2 c4 + 1 of the half and dims 2g, 2g + 1 of
-                        // the unit's 16, split by byte into an even-dim and an odd-dim B fragment.
-                        // O tile 2p holds dims 16p + 2n of the warp's 128, tile 2p + 1 dims 16p + 2n + 1.
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {         // 32 dims: units 2q, 2q + 1
-                            uint32_t r[4];
-                            ldsm_x4_t(sw_unit(st_addr + kr * C::kChunkBytes, tok, 2 * q + ((lane & 16) ? 1 : 0)), r[0],
-                                      r[1], r[2], r[3]);
-#pragma unroll
-                            for (int h = 0; h < 2; ++h) {     // unit 2q + h: matrices 2h (tokens 0-7), 2h + 1 (8-15)
-                                const uint32_t lo = r[2 * h], hi = r[2 * h + 1];
-                                const int p = 2 * q + h;
-                                mma_f16_16816(o[2 * p], pa[kt], e4m3x2_to_f16x2(__byte_perm(lo, 0, 0x4420)),
-                                              e4m3x2_to_f16x2(__byte_perm(hi, 0, 0x4420)));
-                                mma_f16_16816(o[2 * p + 1], pa[kt], e4m3x2_to_f16x2(__byte_perm(lo, 0, 0x4431)),
-                                              e4m3x2_to_f16x2(__byte_perm(hi, 0, 0x4431)));
-                            }
-                        }
-                    } else {
                     uint32_t vf[8][4];
 #pragma unroll
                     for (int dp = 0; dp < 8; ++dp) {          // pairs of n8 dim tiles = 16 dims
@@ -582,7 +449,6 @@ __global__ void __launch_bounds__(NarrowCfg<HG, F8>::kThreads, 1)
                     for (int dp = 0; dp < 8; ++dp) {
                         mma_bf16_16816(o[2 * dp], pa[kt], vf[dp][0], vf[dp][1]);
                         mma_bf16_16816(o[2 * dp + 1], pa[kt], vf[dp][2], vf[dp][3]);
-                    }
                     }
                 }
                 __syncwarp();
@@ -598,15 +464,6 @@ __global__ void __launch_bounds__(NarrowCfg<HG, F8>::kThreads, 1)
             }
             if (!ok) break;
             if (kr == 0 && lane == 0) MLA_TRACE_CTA(2 + grp);
-            if (F8) {
-#pragma unroll
-                for (int n = 0; n < 16; ++n) {
-                    o[n][0] *= r_scale;
-                    o[n][1] *= r_scale;
-                    o[n][2] *= r_scale;
-                    o[n][3] *= r_scale;
-                }
-            }
             // ---- row sums: quad, then the 4 warps of the group (each summed its own 8 tokens per tile)
             float l[2];
 #pragma unroll
@@ -685,28 +542,13 @@ __global__ void __launch_bounds__(NarrowCfg<HG, F8>::kThreads, 1)
                 obase = prm.part_o + (static_cast<size_t>(sg.slot) * prm.h_q + head0) * kDimCkv;
                 lbase = prm.part_lse + static_cast<size_t>(sg.slot) * prm.h_q + head0;
             }
-            if (F8) {
-                // tiles 2p / 2p + 1 hold the even / odd dims of 16-dim block p: this thread's four
-                // values per row are dims 16p + 4 c4 .. + 3 of the warp's 128
 #pragma unroll
-                for (int p = 0; p < 8; ++p) {
-                    const int d = kr * 128 + p * 16 + 4 * c4;
-                    *reinterpret_cast<float4*>(obase + static_cast<size_t>(g) * kDimCkv + d) =
-                        make_float4(o[2 * p][0] * inv0, o[2 * p + 1][0] * inv0, o[2 * p][1] * inv0,
-                                    o[2 * p + 1][1] * inv0);
-                    *reinterpret_cast<float4*>(obase + static_cast<size_t>(g + 8) * kDimCkv + d) =
-                        make_float4(o[2 * p][2] * inv1, o[2 * p + 1][2] * inv1, o[2 * p][3] * inv1,
-                                    o[2 * p + 1][3] * inv1);
-                }
-            } else {
-#pragma unroll
-                for (int n = 0; n < 16; ++n) {
-                    const int d = kr * 128 + n * 8 + 2 * c4;
-                    *reinterpret_cast<float2*>(obase + static_cast<size_t>(g) * kDimCkv + d) =
-                        make_float2(o[n][0] * inv0, o[n][1] * inv0);
-                    *reinterpret_cast<float2*>(obase + static_cast<size_t>(g + 8) * kDimCkv + d) =
-                        make_float2(o[n][2] * inv1, o[n][3] * inv1);
-                }
+            for (int n = 0; n < 16; ++n) {
+                const int d = kr * 128 + n * 8 + 2 * c4;
+                *reinterpret_cast<float2*>(obase + static_cast<size_t>(g) * kDimCkv + d) =
+                    make_float2(o[n][0] * inv0, o[n][1] * inv0);
+                *reinterpret_cast<float2*>(obase + static_cast<size_t>(g + 8) * kDimCkv + d) =
+                    make_float2(o[n][2] * inv1, o[n][3] * inv1);
             }
             if (kr == 0 && c4 == 0) {
                 lbase[g] = (m_run[0] + log2f(l[0])) * 0.69314718055994530942f;

@@ -155,6 +155,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
     constexpr int hq = HQ;
     const uint32_t partner_abort = mapa_shared(smem_u32(&misc->abort_flag), partner);
 
+    // Prologue before the previous kernel in the stream has finished (programmatic dependent
+    // launch): barriers, TMEM and this unit's slice of the plan, which only the plan commit
+    // writes.  Every read of the caller's buffers and every write comes after grid_dep_wait.
+    grid_dep_launch();
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kKSlots; ++i) {
             mbar_init(&misc->k_full[i], 1);
@@ -191,6 +195,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
     tc_fence_before();
     __syncthreads();
     cluster_sync();   // both CTAs' barriers exist before any remote arrive
+    grid_dep_wait();
     tc_fence_after();
     const uint32_t tmem = misc->tmem_base;
     auto aborted = [&]() { return *reinterpret_cast<volatile int*>(&misc->abort_flag) != 0; };

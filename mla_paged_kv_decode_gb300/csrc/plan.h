@@ -8,7 +8,7 @@
 
 namespace mla {
 
-constexpr int kTileTokens = 128;   // tokens per tile of the wide-head (tcgen05) kernel
+constexpr int kTileTokens = 128;   // tokens per tile of the tcgen05 kernels (64/128 heads, e4m3 cache)
 constexpr int kNarrowTileTokens = 32;  // tokens per tile of the narrow-head (warp MMA) kernel
 // Partition cost of a request start (after the first), in tiles: what a CTA that crosses
 // into another request pays for the second segment's prologue and epilogue, measured on
@@ -44,7 +44,7 @@ struct PlanData {
     int batch = 0, h_q = 0, page_size = 0, num_sms = 0, kv_dtype = 0;
     int heads_per_cta = 0, head_groups = 0, num_units = 0;
     int tile_tokens = 0;              // plan granularity = the kernel's tile
-    bool narrow = false;              // h_q <= 32: warp-MMA kernel, else tcgen05 kernel
+    bool narrow = false;              // bf16 cache, h_q <= 32: warp-MMA kernel
     bool pair = false;                // h_q 64/128, bf16 cache: two-CTA cluster kernel, 2 CTAs per unit
     bool e4m3 = false;                // e4m3 cache: tcgen05 kind::f8f6f4 kernel, 16 heads per CTA
     int segment_cost = 0;             // partition cost of a request start, in tiles

@@ -55,6 +55,13 @@ __device__ __forceinline__ void regs_inc() {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// Programmatic dependent launch.  grid_dep_launch lets the next kernel in the stream (launched
+// with programmatic stream serialization) start its prologue once every CTA of this grid has
+// issued it or exited; grid_dep_wait blocks until the previous kernel in the stream has
+// completed and its memory is visible (a no-op without such a predecessor).
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // 2^x with the hardware approximation (a few ulp; the kernels call it with x <= 0)
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
