@@ -228,6 +228,25 @@ def bench_device(inp, steps, warmup, stream):
     return dec, step, (out, lse, d)
 
 
+def profile_only(args):
+    """warmup + steps decodes of one workload through the library, checked, for ncu captures."""
+    import mla_paged_kv_decode_gb300 as mla
+    torch.cuda.set_device(0)
+    mla.load()
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w) if args.kv_len is None else make_inputs(w, kv_lens=[args.kv_len] * w.batch, batch=w.batch)
+    stream = torch.cuda.Stream()
+    dec, step, keep = bench_device(inp, args.steps, args.warmup, stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            step()
+    torch.cuda.synchronize()
+    st = mla.mla_decode_device_status(dec.plan, dec.workspace, stream)
+    out = keep[0]
+    assert st == 0 and bool(torch.isfinite(out).all()), f"status {st}"
+    print(f"profile-only: {args.workload} batch {inp.batch} h_q {inp.h_q} launches {args.warmup + args.steps} ok")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -239,8 +258,17 @@ def main():
     ap.add_argument("--sample-requests", type=int, default=16)
     ap.add_argument("--fp8", type=int, default=1, help="also time the 8-bit cache workload against bf16 (1/0)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-only", action="store_true",
+                    help="run warmup + steps decodes of --workload on the device and exit, no timing or JSON "
+                         "(the program the profiles' ncu commands capture)")
+    ap.add_argument("--kv-len", type=int, default=None,
+                    help="with --profile-only: every request's kv_len (a smaller case of the workload)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+
+    if args.profile_only:
+        profile_only(args)
+        return
 
     if args.impl == "reference":
         run_reference(args)

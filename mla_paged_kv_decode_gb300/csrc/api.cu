@@ -422,7 +422,7 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
 constexpr int kMaxDevices = 64;
 
-__device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
 std::mutex g_noalloc_mutex;
 void* g_noalloc_ptr[kMaxDevices] = {};
