@@ -23,7 +23,9 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 }  // namespace
 
 int heads_per_cta_for(int h_q, int kv_dtype) {
-    if (kv_dtype == 1) return (h_q == 16 || h_q == 32) ? 16 : 0;
+    // e4m3 cache: 16 heads per CTA; 32, 64 and 128 heads take 2, 4 or 8 CTAs per unit, each
+    // streaming the unit's pages (the repeats mostly from L2)
+    if (kv_dtype == 1) return (h_q == 16 || h_q == 32 || h_q == 64 || h_q == 128) ? 16 : 0;
     switch (h_q) {
         case 16:
         case 32:

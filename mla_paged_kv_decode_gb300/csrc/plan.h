@@ -61,7 +61,7 @@ int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int ba
 
 // Heads handled by one CTA for a given h_q and cache type (0 if unsupported): bf16 cache, all
 // of them (the narrow-head kernel for h_q <= 32, the two-CTA kernel for 64/128); e4m3 cache,
-// 16 (h_q 16 or 32).
+// 16 (h_q / 16 CTAs per unit).
 int heads_per_cta_for(int h_q, int kv_dtype);
 
 }  // namespace mla

@@ -100,11 +100,11 @@ def test_run_and_commit_reject_bad_arguments_without_touching_a_gpu(lib):
 
 
 def test_fp8_plan_and_run_checks(lib):
-    # the e4m3 cache is served for 16 and 32 heads; 64/128 heads are refused at plan time
-    assert _plan_rc([0, 1], [5], 1, h_q=16, dtype=mla.MLA_KV_FP8_E4M3) == mla.MLA_OK
-    assert _plan_rc([0, 1], [5], 1, h_q=32, dtype=mla.MLA_KV_FP8_E4M3) == mla.MLA_OK
-    assert _plan_rc([0, 1], [5], 1, h_q=64, dtype=mla.MLA_KV_FP8_E4M3) == mla.MLA_ERR_UNSUPPORTED
-    assert _plan_rc([0, 1], [5], 1, h_q=128, dtype=mla.MLA_KV_FP8_E4M3) == mla.MLA_ERR_UNSUPPORTED
+    # the e4m3 cache is served for every supported head count; others are refused at plan time
+    for h_q in (16, 32, 64, 128):
+        assert _plan_rc([0, 1], [5], 1, h_q=h_q, dtype=mla.MLA_KV_FP8_E4M3) == mla.MLA_OK
+    for h_q in (8, 48, 256):
+        assert _plan_rc([0, 1], [5], 1, h_q=h_q, dtype=mla.MLA_KV_FP8_E4M3) == mla.MLA_ERR_UNSUPPORTED
     vp = ctypes.c_void_p
     fake = vp(1 << 20)
     plan = mla.mla_decode_plan(torch.tensor([0, 2]), torch.tensor([7]), 1, 16, 16, 152, mla.MLA_KV_FP8_E4M3)

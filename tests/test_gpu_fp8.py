@@ -8,7 +8,7 @@ PR #233, "Correctness": worst cosine distance 2.4e-3 for FP8 on synthetic caches
 * the oracle on the original bf16 cache, cosine distance <= 3e-3: this checks the
   quantisation end to end.
 
-Cases: ragged lengths over page sizes 16/32/64 and 16/32 heads, splits over 1, 3
+Cases: ragged lengths over page sizes 16/32/64 and 16/32 heads (and 64/128 heads), splits over 1, 3
 and every SM, reruns (bit-identical), a request whose tokens span six orders of
 magnitude (the per-token scale must not underflow or overflow the kernel's f16
 operands), NaN codes and scales in every unused slot, and the full-size 8-bit
@@ -62,6 +62,15 @@ def test_fp8_small_ragged(H, P):
     lens = [1, 17, P, P + 1, 127, 128, 129, 300, 1000, 2049]
     inp = _small_fp8(lens, H, P, seed=20 + H + P)
     assert inp.ckv.dtype == torch.uint8 and inp.ckv_scale is not None
+    out, lse, _, _ = run_gpu(inp)
+    _check_both(inp, out, lse)
+
+
+@pytest.mark.parametrize("H", [64, 128])
+def test_fp8_wide_heads(H):
+    """64 and 128 heads on the 8-bit cache: 16-head CTAs, h_q / 16 of them per unit."""
+    lens = [1, 100, 129, 700, 2049]
+    inp = _small_fp8(lens, H, 64, seed=50 + H)
     out, lse, _, _ = run_gpu(inp)
     _check_both(inp, out, lse)
 

@@ -6,7 +6,8 @@ SM count) are compared on sampled requests, all heads and all 512 dims of
 each.  Edge cases: empty requests, one-token requests, ragged tails inside a
 page and inside a tile, single requests split over every SM, NaN in every
 slot and page the method must not read, page-placement permutations
-(bit-identical), reruns and CUDA-graph replays (bit-identical).
+(bit-identical), reruns and CUDA-graph replays (bit-identical), and stream order across
+back-to-back launches (each kernel's prologue overlaps the previous kernel's tail).
 """
 import pytest
 import torch
@@ -128,6 +129,41 @@ def test_reruns_and_graph_replay_are_bit_identical():
         g.replay()
         torch.cuda.synchronize()
         assert torch.equal(out_g.cpu(), out0) and torch.equal(lse_g.cpu(), lse0)
+
+
+def test_back_to_back_decodes_keep_stream_order():
+    """Every decode is launched with programmatic dependent launch: its prologue may overlap the
+    previous kernel's tail, but its reads of the caller's buffers and all its writes follow that
+    kernel.  Two different decodes alternate into one output buffer with no synchronisation: the
+    buffer must end up holding the last one's result, bit for bit.  A torch kernel that rewrites
+    q between two launches must be seen by the second."""
+    a = _small([3000, 129, 700, 1], 16, 64, seed=31)
+    b = _small([50, 2500, 64, 900], 16, 64, seed=32)
+    ref_a, lse_ref_a, dec_a, da = run_gpu(a)
+    ref_b, lse_ref_b, dec_b, db = run_gpu(b)
+    assert not torch.equal(ref_a, ref_b)
+    out = torch.empty(a.batch, a.h_q, 512, device="cuda")
+    lse = torch.empty(a.batch, a.h_q, device="cuda")
+    args = lambda d, inp: (d.q_nope, d.q_pe, d.ckv, d.kpe, d.kv_indices, d.kv_indptr, d.kv_last_page_len,
+                           inp.sm_scale)
+    for _ in range(20):
+        dec_a.run(*args(da, a), out=out, lse=lse)
+        dec_b.run(*args(db, b), out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.equal(out.cpu(), ref_b) and torch.equal(lse.cpu(), lse_ref_b)
+    # q rewritten by a torch kernel between two launches on the same stream
+    out2 = torch.empty_like(out)
+    lse2 = torch.empty_like(lse)
+    dec_b.run(*args(db, b), out=out, lse=lse)
+    db.q_nope.neg_()
+    dec_b.run(*args(db, b), out=out2, lse=lse2)
+    torch.cuda.synchronize()
+    assert torch.equal(out.cpu(), ref_b)
+    o3, l3 = dec_b.run(*args(db, b))
+    torch.cuda.synchronize()
+    assert torch.equal(out2.cpu(), o3.cpu()) and torch.equal(lse2.cpu(), l3.cpu())
+    assert not torch.equal(out2.cpu(), ref_b)
+    assert dec_a.device_status() == mla.MLA_OK and dec_b.device_status() == mla.MLA_OK
 
 
 def test_page_permutation_is_bit_identical():

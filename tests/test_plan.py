@@ -138,11 +138,9 @@ def test_e4m3_plans():
         lens = [rng.choice([0, 1, rng.randint(1, 300), rng.randint(1, 20000)]) for _ in range(B)]
         _check_plan(lens, rng.choice([16, 32]), rng.choice([16, 32, 64]), rng.choice([1, 7, 64, 152]),
                     mla.MLA_KV_FP8_E4M3)
-    indptr, last = _lens_to_arrays([100], 16)
-    for h_q in (64, 128):                     # wider heads have no 8-bit kernel
-        with pytest.raises(RuntimeError):
-            mla.mla_decode_plan(torch.from_numpy(indptr), torch.from_numpy(last), 1, h_q, 16, 152,
-                                mla.MLA_KV_FP8_E4M3)
+    for h_q, units in ((64, 38), (128, 19)):  # wider heads: h_q / 16 CTAs of 16 heads per unit
+        segs, uptr = _check_plan([8192] * 16, h_q, 64, 152, mla.MLA_KV_FP8_E4M3)
+        assert len(uptr) - 1 == units
 
 
 def test_plan_is_deterministic():
