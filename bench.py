@@ -118,8 +118,10 @@ class ClockSampler:
                 continue
             rows.append((ts, parts))
         inside = [r for r in rows if t0 <= r[0] <= t1]
+        window = "timed region"
         if not inside and rows:  # region shorter than the sampling period: nearest samples
             inside = sorted(rows, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))[:2]
+            window = "nearest to the timed region"
         if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         sm = [float(p[1]) for _, p in inside if p[1].replace(".", "").isdigit()]
@@ -127,7 +129,7 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({n for _, p in inside for n, v in zip(names, p[5:9]) if v.lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": reasons, "samples": len(inside)}
+                "reasons": reasons, "samples": len(inside), "window": window}
 
 
 def dist_env():
@@ -173,6 +175,11 @@ def run_reference(args):
     inp = make_inputs(WORKLOADS[args.workload])
     cores = cpu_cores()
     sample = list(range(min(args.sample_requests, inp.batch)))
+    # the whole --steps/--warmup run stays within about two minutes: halve the sample while a
+    # step would take longer than its share
+    share = 120.0 / max(1, args.steps + args.warmup)
+    while len(sample) > 1 and time_oracle(inp, sample, cores) > share:
+        sample = sample[: len(sample) // 2]
     for _ in range(args.warmup):
         time_oracle(inp, sample, cores)
     ts = [time_oracle(inp, sample, cores) for _ in range(args.steps)]
@@ -250,7 +257,7 @@ def profile_only(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="membound", choices=sorted(WORKLOADS))
