@@ -210,6 +210,64 @@ def time_workload(inp, n, stream):
     return e0.elapsed_time(e1) / n / 1e3
 
 
+def plan_balance(plan, h_q: int, kv_dtype: int) -> dict:
+    """Max / mean unit cost of a plan: a unit's cost is its tiles plus the plan's start cost per
+    request it starts (the measure the planner equalises)."""
+    import mla_paged_kv_decode_gb300 as mla
+    tile = 32 if (h_q <= 32 and kv_dtype == mla.MLA_KV_BF16) else 128
+    segs, uptr = mla.mla_plan_get_segments(plan)
+    c = mla.mla_plan_segment_cost_tiles(plan)
+    cost, tiles = [], []
+    for u in range(len(uptr) - 1):
+        s = segs[uptr[u]:uptr[u + 1]]
+        nt = sum((int(t1) - int(t0) + tile - 1) // tile for _, t0, t1, _ in s if t1 > t0)
+        tiles.append(nt)
+        cost.append(nt + c * sum(1 for _, t0, t1, _ in s if t1 > t0 and t0 == 0))
+    ratio = lambda v: (max(v) * len(v) / sum(v)) if sum(v) else None
+    return {"units": len(cost), "tile": tile, "start_cost_tiles": c, "cost_max_over_mean": ratio(cost),
+            "tiles_max_over_mean": ratio(tiles), "segments": int(len(segs)),
+            "partials": mla.mla_plan_num_partials(plan)}
+
+
+def per_call_medians(name: str, stream, n: int = 100) -> dict:
+    """One workload: the median of n single decodes timed one by one (an event pair around each
+    call on the launching stream), launched eagerly and as replays of a captured CUDA graph."""
+    import mla_paged_kv_decode_gb300 as mla
+    inp = make_inputs(WORKLOADS[name])
+    b, f = algorithmic_bytes(inp), algorithmic_flops(inp)
+    dec, step, keep = bench_device(inp, 0, 5, stream)
+    out, lse, d = keep
+
+    def timed(fn):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):   # replays go to the current stream
+            for e0, e1 in evs:
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+        torch.cuda.synchronize()
+        return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs) * 1e3
+
+    eager = timed(step)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g.replay()
+    graph = timed(lambda: g.replay())
+    st = dec.device_status(stream)
+    kvd = mla.MLA_KV_FP8_E4M3 if inp.ckv_scale is not None else mla.MLA_KV_BF16
+    res = {"desc": WORKLOADS[name].description, "us_eager_median": eager, "us_graph_median": graph,
+           "gbs": b / graph / 1e3, "tflops": f / graph / 1e6, "alg_bytes": b, "alg_flops": f,
+           "tokens": int(inp.kv_lens.sum()), "calls": n, "status": st,
+           "plan": plan_balance(dec.plan, inp.h_q, kvd)}
+    del g, keep, dec, d, out, lse, inp
+    torch.cuda.empty_cache()
+    return res
+
+
 def bench_device(inp, steps, warmup, stream):
     """Device-timed steps with resident inputs.  Returns per-step and per-kernel times (s)."""
     import mla_paged_kv_decode_gb300 as mla
@@ -265,6 +323,8 @@ def main():
     ap.add_argument("--sample-requests", type=int, default=16)
     ap.add_argument("--fp8", type=int, default=1, help="also time the 8-bit cache workload against bf16 (1/0)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--configs", type=int, default=1,
+                    help="also report every workload's per-call median, eager and CUDA-graph replay (1/0)")
     ap.add_argument("--profile-only", action="store_true",
                     help="run warmup + steps decodes of --workload on the device and exit, no timing or JSON "
                          "(the program the profiles' ncu commands capture)")
@@ -408,6 +468,16 @@ def main():
                "speedup_vs_bf16": t16 / t8, "bytes_per_token": {"fp8": 644, "bf16": 1152},
                "traffic": recorded_traffic("fp8")}
 
+    # ---- every workload of the measurement table, one decode at a time: eager and graph replay
+    configs = None
+    if args.configs and rank == 0 and world == 1:
+        configs = {}
+        for name in ("membound", "compute", "b768_kv1024", "b768_kv2048", "ragged", "fp8"):
+            c = per_call_medians(name, stream)
+            c["hbm_frac"] = c["gbs"] / hbm_gbs
+            c["tensor_frac"] = c["tflops"] / bf16_tf
+            configs[name] = c
+
     # ---- cpu baseline: the oracle on a bounded sample, host cores, rank 0 at N=1
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -431,7 +501,7 @@ def main():
                        "tflops": alg_flops * args.steps * world / total_max / 1e12},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
                          "frac": achieved / hbm_gbs, "traffic": recorded_traffic(args.workload),
-                         "kernel": ("mla_decode_narrow_kernel" if inp.h_q <= 32 else "mla_decode_attn_kernel"),
+                         "kernel": ("mla_decode_narrow_kernel" if inp.h_q <= 32 else "mla_decode_pair_kernel"),
                          "peak_source": peak_src,
                          "kernel_us": attn_avg * 1e6},
             "cpu_baseline": cpu,
@@ -441,6 +511,7 @@ def main():
             "clocks": clocks,
             "secondary": secondary,
             "fp8": fp8,
+            "configs": configs,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -296,6 +296,77 @@ __device__ __forceinline__ void merge_split_pieces(const AttnParams& prm, int b,
     }
 }
 
+// The merge of up to 8 pieces of 16 heads by 256 threads: threads [128 k, 128 k + 128) take
+// heads [8 k, 8 k + 8), so the loads of every piece (up to 4) of both head blocks go out in one
+// round, together with the lse loads.  Threads 0..127 run the lse pass of
+// merge_split_pieces<16, 128>, and every output sums the same products in the same order as
+// there: the two forms give identical bits.  More than 8 pieces: threads 0..127 run the
+// general form on the 128-thread barrier `bar128`, the others return.
+__device__ __forceinline__ void merge_split_pieces_wide16(const AttnParams& prm, int b, int slot_begin, int n_slots,
+                                                          int head0, int tid, uint32_t bar256, uint32_t bar128,
+                                                          float* s_max, float* s_inv, float* s_w) {
+    constexpr int NH = 16, kMax = 8, kTph = 8, kHB = 8, kPB = 4;
+    if (n_slots > kMax) {
+        if (tid < 128)
+            merge_split_pieces_chunked<NH, 128>(prm, b, slot_begin, n_slots, head0, tid, bar128, s_max, s_inv, s_w);
+        return;
+    }
+    const size_t hq = static_cast<size_t>(prm.h_q);
+    const int t = tid & 127, hb = (tid >> 7) * kHB;
+    auto piece_o = [&](int i, int h) {   // this thread's 4 dims of head h, piece i
+        return reinterpret_cast<const float4*>(prm.part_o + ((slot_begin + i) * hq + head0 + h) * kDimCkv) + t;
+    };
+    float4 v[kPB][kHB];
+    auto load_block = [&](int p0) {
+#pragma unroll
+        for (int i = 0; i < kPB; ++i)
+#pragma unroll
+            for (int h = 0; h < kHB; ++h)
+                v[i][h] = (p0 + i < n_slots) ? __ldcg(piece_o(p0 + i, hb + h)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    load_block(0);   // in flight during the lse pass
+    if (tid < 128) {
+        const int h = tid / kTph, sub = tid % kTph;
+        const float x = sub < n_slots ? __ldcg(prm.part_lse + (slot_begin + sub) * hq + head0 + h) : -INFINITY;
+        float m = x;
+#pragma unroll
+        for (int o = kTph / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float sum = sub < n_slots ? expf(x - m) : 0.f;
+#pragma unroll
+        for (int o = kTph / 2; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        const float inv = 1.f / sum;
+        if (sub < n_slots) s_w[sub * NH + h] = expf(x - m) * inv;
+        if (sub == 0) {
+            s_max[h] = m;
+            s_inv[h] = inv;
+            prm.lse[static_cast<size_t>(b) * hq + head0 + h] = m + logf(sum);
+        }
+    }
+    named_barrier_sync(bar256, 256);
+    float4 acc[kHB];
+#pragma unroll
+    for (int h = 0; h < kHB; ++h) acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+    for (int p0 = 0; p0 < n_slots; p0 += kPB) {
+        if (p0 != 0) load_block(p0);
+#pragma unroll
+        for (int i = 0; i < kPB; ++i) {
+            if (p0 + i >= n_slots) break;
+#pragma unroll
+            for (int h = 0; h < kHB; ++h) {
+                const float w = s_w[(p0 + i) * NH + hb + h];
+                acc[h].x = fmaf(w, v[i][h].x, acc[h].x);
+                acc[h].y = fmaf(w, v[i][h].y, acc[h].y);
+                acc[h].z = fmaf(w, v[i][h].z, acc[h].z);
+                acc[h].w = fmaf(w, v[i][h].w, acc[h].w);
+            }
+        }
+    }
+    float4* out4 = reinterpret_cast<float4*>(prm.out + (static_cast<size_t>(b) * hq + head0) * kDimCkv) + t;
+#pragma unroll
+    for (int h = 0; h < kHB; ++h) out4[(hb + h) * (kDimCkv / 4)] = acc[h];
+}
+
 // Walks the non-empty segments of one CTA slot tile by tile.
 template <int TILE>
 struct TileCursorT {

@@ -674,24 +674,23 @@ __global__ void __launch_bounds__(E4m3Cfg::kThreads, 1)
                 if (t < 8) lbase[hb + t] = ltt > 0.f ? (mt + log2f(ltt)) * 0.69314718055994530942f : -INFINITY;
             }
             if (sg.slot >= 0) {
-                // ---- split request: the last piece to arrive merges all of them in slot order
+                // ---- split request: the last piece to arrive merges all of them in slot order,
+                // both groups together (256 threads: one round of loads)
                 __threadfence();
                 named_barrier_sync(abar, 256);
-                if (grp == 0) {
-                    const int ctr = sg.item * prm.head_groups + group_cta;
-                    if (t == 0) {
-                        const int old = atomicAdd(&prm.counters[ctr], 1);
-                        misc->merge_flag = (old == sg.n_slots - 1);
-                    }
-                    named_barrier_sync(gbar, 128);
-                    if (misc->merge_flag) {
-                        __threadfence();
-                        merge_split_pieces<16, 128>(prm, sg.b, sg.slot_begin, sg.n_slots, head0, t, gbar,
-                                                    misc->mrg_max, misc->mrg_inv, misc->mrg_w);
-                        if (t == 0) prm.counters[ctr] = 0;
-                    }
-                    named_barrier_sync(gbar, 128);
+                const int ctr = sg.item * prm.head_groups + group_cta;
+                if (grp == 0 && t == 0) {
+                    const int old = atomicAdd(&prm.counters[ctr], 1);
+                    misc->merge_flag = (old == sg.n_slots - 1);
                 }
+                named_barrier_sync(abar, 256);
+                if (misc->merge_flag) {
+                    __threadfence();
+                    merge_split_pieces_wide16(prm, sg.b, sg.slot_begin, sg.n_slots, head0, grp * 128 + t, abar, gbar,
+                                              misc->mrg_max, misc->mrg_inv, misc->mrg_w);
+                    if (grp == 0 && t == 0) prm.counters[ctr] = 0;
+                }
+                named_barrier_sync(abar, 256);
             }
         }
     }

@@ -529,51 +529,63 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                     }
                     named_barrier_sync(merge_bar, 256);   // the buffer is rewritten next
                 }
-                if (tg == 1) continue;
             }
-            // ---- epilogue (token group 0): normalise and store this warp's 128 dims
-            const float inv0 = 1.f / l[0], inv1 = 1.f / l[1];
-            float* obase;
-            float* lbase;
-            if (sg.slot < 0) {
-                obase = prm.out + (static_cast<size_t>(sg.b) * prm.h_q + head0) * kDimCkv;
-                lbase = prm.lse + static_cast<size_t>(sg.b) * prm.h_q + head0;
-            } else {
-                obase = prm.part_o + (static_cast<size_t>(sg.slot) * prm.h_q + head0) * kDimCkv;
-                lbase = prm.part_lse + static_cast<size_t>(sg.slot) * prm.h_q + head0;
-            }
+            // At the unit's last segment token group 1 has no more tiles: if the segment is a
+            // split piece it stays to merge with group 0 (256 threads, one round of loads)
+            const bool wide = C::kTokenGroups == 2 && sg.slot >= 0 && si == seg_end - 1;
+            if (tg == 1 && !wide) continue;
+            if (tg == 0) {
+                // ---- epilogue (token group 0): normalise and store this warp's 128 dims
+                const float inv0 = 1.f / l[0], inv1 = 1.f / l[1];
+                float* obase;
+                float* lbase;
+                if (sg.slot < 0) {
+                    obase = prm.out + (static_cast<size_t>(sg.b) * prm.h_q + head0) * kDimCkv;
+                    lbase = prm.lse + static_cast<size_t>(sg.b) * prm.h_q + head0;
+                } else {
+                    obase = prm.part_o + (static_cast<size_t>(sg.slot) * prm.h_q + head0) * kDimCkv;
+                    lbase = prm.part_lse + static_cast<size_t>(sg.slot) * prm.h_q + head0;
+                }
 #pragma unroll
-            for (int n = 0; n < 16; ++n) {
-                const int d = kr * 128 + n * 8 + 2 * c4;
-                *reinterpret_cast<float2*>(obase + static_cast<size_t>(g) * kDimCkv + d) =
-                    make_float2(o[n][0] * inv0, o[n][1] * inv0);
-                *reinterpret_cast<float2*>(obase + static_cast<size_t>(g + 8) * kDimCkv + d) =
-                    make_float2(o[n][2] * inv1, o[n][3] * inv1);
-            }
-            if (kr == 0 && c4 == 0) {
-                lbase[g] = (m_run[0] + log2f(l[0])) * 0.69314718055994530942f;
-                lbase[g + 8] = (m_run[1] + log2f(l[1])) * 0.69314718055994530942f;
+                for (int n = 0; n < 16; ++n) {
+                    const int d = kr * 128 + n * 8 + 2 * c4;
+                    *reinterpret_cast<float2*>(obase + static_cast<size_t>(g) * kDimCkv + d) =
+                        make_float2(o[n][0] * inv0, o[n][1] * inv0);
+                    *reinterpret_cast<float2*>(obase + static_cast<size_t>(g + 8) * kDimCkv + d) =
+                        make_float2(o[n][2] * inv1, o[n][3] * inv1);
+                }
+                if (kr == 0 && c4 == 0) {
+                    lbase[g] = (m_run[0] + log2f(l[0])) * 0.69314718055994530942f;
+                    lbase[g + 8] = (m_run[1] + log2f(l[1])) * 0.69314718055994530942f;
+                }
             }
             if (sg.slot >= 0) {
                 // ---- split request: the last piece to arrive merges all of them in slot order
-                __threadfence();
-                named_barrier_sync(named_bar, 128);
+                // (group 0 alone, or both token groups at the unit's last segment)
+                const uint32_t mbar = wide ? merge_bar : named_bar;
+                const uint32_t nthr = wide ? 256u : 128u;
+                if (tg == 0) __threadfence();
+                named_barrier_sync(mbar, nthr);
                 const int gt = kr * 32 + lane;   // 0..127 within the group
                 const int ctr = (sg.item * prm.head_groups + group_cta) * C::kHeadGroups + hgi;
-                if (gt == 0) {
+                if (tg == 0 && gt == 0) {
                     const int old = atomicAdd(&prm.counters[ctr], 1);
                     misc->merge_flag[hgi] = (old == sg.n_slots - 1);
                 }
-                named_barrier_sync(named_bar, 128);
+                named_barrier_sync(mbar, nthr);
                 if (misc->merge_flag[hgi]) {
-                    if (gt == 0) MLA_TRACE_CTA(4);
+                    if (tg == 0 && gt == 0) MLA_TRACE_CTA(4);
                     __threadfence();
-                    merge_split_pieces<16, 128>(prm, sg.b, sg.slot_begin, sg.n_slots, head0, gt, named_bar,
-                                                misc->mrg_max[hgi], misc->mrg_inv[hgi], misc->mrg_w[hgi]);
-                    if (gt == 0) prm.counters[ctr] = 0;
-                    if (gt == 0) MLA_TRACE_CTA(5);
+                    if (wide)
+                        merge_split_pieces_wide16(prm, sg.b, sg.slot_begin, sg.n_slots, head0, tg * 128 + gt, merge_bar,
+                                                  named_bar, misc->mrg_max[hgi], misc->mrg_inv[hgi], misc->mrg_w[hgi]);
+                    else
+                        merge_split_pieces<16, 128>(prm, sg.b, sg.slot_begin, sg.n_slots, head0, gt, named_bar,
+                                                    misc->mrg_max[hgi], misc->mrg_inv[hgi], misc->mrg_w[hgi]);
+                    if (tg == 0 && gt == 0) prm.counters[ctr] = 0;
+                    if (tg == 0 && gt == 0) MLA_TRACE_CTA(5);
                 }
-                named_barrier_sync(named_bar, 128);
+                named_barrier_sync(mbar, nthr);
             }
         }
     }
