@@ -139,6 +139,15 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of the ranks' values (the slowest rank's time); x itself on one rank."""
+    if world <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t)
+
+
 def aggregate(per_rank_seconds, per_rank_units, world):
     """Whole-job throughput: units of every rank / the slowest rank's time."""
     t = max(per_rank_seconds)
@@ -383,12 +392,7 @@ def main():
     total_s = start.elapsed_time(end) / 1e3
     clocks = sampler.summary(t_wall0, t_wall1)
 
-    if world > 1:
-        t = torch.tensor([total_s], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_max = float(t)
-    else:
-        total_max = total_s
+    total_max = max_over_ranks(total_s, world, "cuda")
     value, _ = aggregate([total_max], [alg_bytes * args.steps * world], world)
     value /= 1e9
     attn_avg = total_s / args.steps
@@ -424,10 +428,7 @@ def main():
     for _ in range(e2e_steps):
         e2e_step()
     e2e_s = (time.perf_counter() - t0) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_s], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t)
+    e2e_s = max_over_ranks(e2e_s, world, "cuda")
     e2e_value = alg_bytes * world / e2e_s / 1e9
 
     # ---- secondary: compute-shaped workload (TFLOPS), device-timed the same way
