@@ -62,6 +62,11 @@ typedef enum {
     MLA_KV_FP8_E4M3 = 1  /* ckv uint8 e4m3 codes [num_pages, page_size, 512] + fp32 scale [num_pages, page_size] */
 } mla_kv_dtype_t;
 
+typedef enum {
+    MLA_OUT_F32 = 0,   /* out fp32 [rows, h_q, 512] */
+    MLA_OUT_BF16 = 1   /* out bf16 [rows, h_q, 512], each value the fp32 result rounded to nearest even */
+} mla_out_dtype_t;
+
 /* Build a balanced split-KV work list (host only, no device call).
  *
  * Work is measured in tokens.  Requests are laid out in order, cut into
@@ -87,6 +92,30 @@ typedef enum {
 mla_status_t mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_last_page_len_host, int batch,
                              int h_q, int page_size, int num_sms, mla_kv_dtype_t kv_dtype, mla_plan_t* plan_out);
 
+/* mla_decode_plan with several query tokens per request and a choice of output type.
+ *
+ * A request may decode qo_len new tokens at once (the pages' tests carry
+ * batch_size * qo_len query rows, "perf: MLA decode kernel implemented by CuTe
+ * targeted to SM80").  The new tokens are the last qo_len tokens of the
+ * request's cache.  Query token j (0-based) of request b is query row
+ * r = b * qo_len + j of q_nope / q_pe / out / lse, which then hold
+ * rows = batch * qo_len rows:
+ *   q_nope [rows, h_q, 512], q_pe [rows, h_q, 64], out [rows, h_q, 512], lse [rows, h_q].
+ * Row r attends to request b's first L_b tokens, or with causal != 0 to its
+ * first max(0, L_b - (qo_len - 1 - j)) tokens: each new token sees the cache
+ * up to and including itself.  A row with no tokens gets out = 0, lse = -inf.
+ * Each row streams its request's pages itself: the cache is read qo_len times.
+ *
+ *   qo_len     1 .. 64
+ *   causal     0 or 1 (no effect when qo_len == 1)
+ *   out_dtype  MLA_OUT_F32, or MLA_OUT_BF16: out holds bf16 values, each the fp32
+ *              result rounded to nearest even; lse stays fp32
+ * The other arguments and the return codes are those of mla_decode_plan, which
+ * equals this call with qo_len 1, causal 0 and MLA_OUT_F32. */
+mla_status_t mla_decode_plan_ex(const int32_t* kv_indptr_host, const int32_t* kv_last_page_len_host, int batch,
+                                int qo_len, int causal, int h_q, int page_size, int num_sms,
+                                mla_kv_dtype_t kv_dtype, mla_out_dtype_t out_dtype, mla_plan_t* plan_out);
+
 /* Device workspace the plan needs (bytes, a multiple of 256): the work list,
  * the split partials and a status word.  0 for a NULL plan. */
 size_t mla_decode_plan_workspace_bytes(mla_plan_t plan);
@@ -107,8 +136,8 @@ mla_status_t mla_decode_plan_commit(mla_plan_t plan, void* workspace_dev, size_t
  * them in slot order (FlashMLA PR #233, "deterministic combine"), so the
  * result does not depend on which CTA merges.
  *
- *   q_nope           device bf16 [batch, h_q, 512]
- *   q_pe             device bf16 [batch, h_q, 64]
+ *   q_nope           device bf16 [batch, h_q, 512] ([rows, h_q, 512] for a plan with qo_len > 1)
+ *   q_pe             device bf16 [batch, h_q, 64]  ([rows, h_q, 64])
  *   ckv_cache        device bf16 [num_pages, page_size, 512], or uint8 e4m3 codes of the
  *                    same shape for MLA_KV_FP8_E4M3
  *   ckv_scale        NULL for bf16; device fp32 [num_pages, page_size] for e4m3
@@ -120,9 +149,10 @@ mla_status_t mla_decode_plan_commit(mla_plan_t plan, void* workspace_dev, size_t
  *   kv_indptr        device int32 [batch + 1], same values the plan was built from
  *   kv_last_page_len device int32 [batch],     same values the plan was built from
  *   sm_scale         softmax scale applied to q.k (e.g. 1/sqrt(192))
- *   out              device fp32 [batch, h_q, 512]
- *   lse              device fp32 [batch, h_q], natural log of sum_t exp(x_t); -inf and
- *                    out = 0 for a request with no tokens
+ *   out              device fp32 [batch, h_q, 512], or bf16 when the plan was made with
+ *                    MLA_OUT_BF16 ([rows, h_q, 512] for a plan with qo_len > 1)
+ *   lse              device fp32 [batch, h_q] ([rows, h_q]), natural log of sum_t exp(x_t);
+ *                    -inf and out = 0 for a request with no tokens
  *   workspace_dev    the workspace passed to mla_decode_plan_commit
  * Every device buffer needs 16-byte alignment.  Slots past kv_last_page_len
  * and pages no request references are never used (they may hold NaN).
@@ -133,7 +163,7 @@ mla_status_t mla_decode_plan_commit(mla_plan_t plan, void* workspace_dev, size_t
 mla_status_t mla_decode_run(mla_plan_t plan, const void* q_nope, const void* q_pe, const void* ckv_cache,
                             const float* ckv_scale, const void* kpe_cache, int num_pages,
                             const int32_t* kv_indices, const int32_t* kv_indptr,
-                            const int32_t* kv_last_page_len, float sm_scale, float* out, float* lse,
+                            const int32_t* kv_last_page_len, float sm_scale, void* out, float* lse,
                             void* workspace_dev, void* cuda_stream);
 
 /* Kernel launches mla_decode_run issues for this plan (1, or 0 when no request has work). */
@@ -154,9 +184,12 @@ int mla_plan_heads_per_cta(mla_plan_t plan);
  * charges for each request start after the first: CTA slots are cut so that tiles plus
  * these costs are equal to within one tile. */
 int mla_plan_segment_cost_tiles(mla_plan_t plan);
-/* Copy the work list: for segment i, out[4i..4i+3] = (request, token_begin, token_end,
- * partial slot or -1); unit_ptr[u] .. unit_ptr[u+1] are unit u's segments.  Either
- * pointer may be NULL.  Returns the number of segments. */
+/* Query rows of out / lse: batch * qo_len. */
+int mla_plan_num_rows(mla_plan_t plan);
+/* Copy the work list: for segment i, out[4i..4i+3] = (query row, token_begin, token_end,
+ * partial slot or -1), the query row being the request with qo_len 1; unit_ptr[u] ..
+ * unit_ptr[u+1] are unit u's segments.  Either pointer may be NULL.  Returns the number
+ * of segments. */
 int mla_plan_get_segments(mla_plan_t plan, int32_t* segments, int32_t* unit_ptr);
 
 /* Decode for callers that cannot allocate device memory: cudaMalloc may be off
@@ -181,7 +214,7 @@ int mla_plan_get_segments(mla_plan_t plan, int32_t* segments, int32_t* unit_ptr)
 mla_status_t mla_decode_run_noalloc(mla_plan_t plan, const void* q_nope, const void* q_pe, const void* ckv_cache,
                                     const float* ckv_scale, const void* kpe_cache, int num_pages,
                                     const int32_t* kv_indices, const int32_t* kv_indptr,
-                                    const int32_t* kv_last_page_len, float sm_scale, float* out, float* lse,
+                                    const int32_t* kv_last_page_len, float sm_scale, void* out, float* lse,
                                     void* cuda_stream);
 /* Size of the fixed workspace array mla_decode_run_noalloc uses (bytes). */
 size_t mla_decode_noalloc_max_workspace_bytes(void);

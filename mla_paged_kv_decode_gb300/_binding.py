@@ -27,12 +27,15 @@ MLA_ERR_NOT_COMMITTED = 6
 MLA_KV_BF16 = 0
 MLA_KV_FP8_E4M3 = 1
 
+MLA_OUT_F32 = 0
+MLA_OUT_BF16 = 1
+
 EXPORTED = (
     "mla_decode_plan", "mla_decode_plan_workspace_bytes", "mla_decode_plan_commit", "mla_decode_run",
     "mla_decode_device_status", "mla_plan_num_ctas", "mla_plan_num_segments", "mla_plan_num_partials",
     "mla_plan_heads_per_cta", "mla_plan_get_segments", "mla_plan_destroy", "mla_status_string",
     "mla_plan_num_launches", "mla_decode_run_noalloc", "mla_decode_noalloc_max_workspace_bytes",
-    "mla_plan_segment_cost_tiles", "mla_plan_num_units",
+    "mla_plan_segment_cost_tiles", "mla_plan_num_units", "mla_decode_plan_ex", "mla_plan_num_rows",
 )
 
 _lib = None
@@ -63,6 +66,8 @@ def load(path: Optional[str] = None):
     lib.mla_decode_plan.restype = ctypes.c_int
     lib.mla_decode_plan.argtypes = [i32p, i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, ctypes.POINTER(vp)]
+    lib.mla_decode_plan_ex.restype = ctypes.c_int
+    lib.mla_decode_plan_ex.argtypes = [i32p, i32p] + [ctypes.c_int] * 8 + [ctypes.POINTER(vp)]
     lib.mla_decode_plan_workspace_bytes.restype = sz
     lib.mla_decode_plan_workspace_bytes.argtypes = [vp]
     lib.mla_decode_plan_commit.restype = ctypes.c_int
@@ -79,7 +84,7 @@ def load(path: Optional[str] = None):
     lib.mla_decode_device_status.restype = ctypes.c_int
     lib.mla_decode_device_status.argtypes = [vp, vp, vp]
     for name in ("mla_plan_num_ctas", "mla_plan_num_segments", "mla_plan_num_partials", "mla_plan_heads_per_cta",
-                 "mla_plan_segment_cost_tiles", "mla_plan_num_units"):
+                 "mla_plan_segment_cost_tiles", "mla_plan_num_units", "mla_plan_num_rows"):
         getattr(lib, name).restype = ctypes.c_int
         getattr(lib, name).argtypes = [vp]
     lib.mla_plan_get_segments.restype = ctypes.c_int
@@ -118,9 +123,10 @@ def _stream(stream) -> ctypes.c_void_p:
 class Plan:
     """Owns an mla_plan_t handle (destroyed with the object)."""
 
-    def __init__(self, handle, batch, h_q, page_size, kv_dtype):
+    def __init__(self, handle, batch, h_q, page_size, kv_dtype, qo_len=1, causal=False, out_dtype=MLA_OUT_F32):
         self.handle = handle
         self.batch, self.h_q, self.page_size, self.kv_dtype = batch, h_q, page_size, kv_dtype
+        self.qo_len, self.causal, self.out_dtype = qo_len, causal, out_dtype
 
     @property
     def workspace_bytes(self) -> int:
@@ -143,6 +149,25 @@ def mla_decode_plan(kv_indptr, kv_last_page_len, batch: int, h_q: int, page_size
                              int(page_size), int(num_sms), int(kv_dtype), ctypes.byref(h))
     _check(st, "mla_decode_plan")
     return Plan(h, batch, h_q, page_size, kv_dtype)
+
+
+def mla_decode_plan_ex(kv_indptr, kv_last_page_len, batch: int, qo_len: int, causal: bool, h_q: int,
+                       page_size: int, num_sms: int, kv_dtype: int = MLA_KV_BF16,
+                       out_dtype: int = MLA_OUT_F32) -> Plan:
+    lib = load()
+    ip = np.ascontiguousarray(torch.as_tensor(kv_indptr).cpu().to(torch.int32).numpy())
+    lp = np.ascontiguousarray(torch.as_tensor(kv_last_page_len).cpu().to(torch.int32).numpy())
+    h = ctypes.c_void_p()
+    st = lib.mla_decode_plan_ex(ip.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                lp.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), int(batch), int(qo_len),
+                                int(bool(causal)), int(h_q), int(page_size), int(num_sms), int(kv_dtype),
+                                int(out_dtype), ctypes.byref(h))
+    _check(st, "mla_decode_plan_ex")
+    return Plan(h, batch, h_q, page_size, kv_dtype, qo_len, bool(causal), out_dtype)
+
+
+def mla_plan_num_rows(plan: Plan) -> int:
+    return int(load().mla_plan_num_rows(plan.handle))
 
 
 def mla_decode_plan_workspace_bytes(plan: Plan) -> int:

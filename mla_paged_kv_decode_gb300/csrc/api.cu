@@ -193,7 +193,7 @@ cudaError_t launch_pair(const mla_plan_s* p, const MapCache& mc, const mla::Attn
 // mla_decode_run_noalloc; `ws` is the committed workspace (device).
 mla_status_t run_checked(mla_plan_t plan, const void* q_nope, const void* q_pe, const void* ckv_cache,
                          const float* ckv_scale, const void* kpe_cache, int num_pages, const int32_t* kv_indices,
-                         const int32_t* kv_indptr, float sm_scale, float* out, float* lse, uint8_t* ws,
+                         const int32_t* kv_indptr, float sm_scale, void* out, float* lse, uint8_t* ws,
                          cudaStream_t stream, uint64_t* trace) {
     const auto& d = plan->d;
     const bool f8 = d.kv_dtype == MLA_KV_FP8_E4M3;
@@ -203,7 +203,7 @@ mla_status_t run_checked(mla_plan_t plan, const void* q_nope, const void* q_pe, 
     if (!mc.valid || mc.ckv != ckv_cache || mc.kpe != kpe_cache || mc.qn != q_nope || mc.qp != q_pe ||
         mc.scale != ckv_scale || mc.num_pages != num_pages) {
         const uint64_t rows = static_cast<uint64_t>(num_pages) * d.page_size;
-        const uint64_t qrows = static_cast<uint64_t>(d.batch) * d.h_q;
+        const uint64_t qrows = static_cast<uint64_t>(d.rows) * d.h_q;
         const uint32_t hg = static_cast<uint32_t>(d.heads_per_cta);
         // box rows: a whole page for the tcgen05 kernel, a 32-token ring stage at most for the narrow one
         const uint32_t box = d.narrow ? std::min(d.page_size, mla::kNarrowStageTok) : d.page_size;
@@ -234,7 +234,7 @@ mla_status_t run_checked(mla_plan_t plan, const void* q_nope, const void* q_pe, 
     prm.kv_indptr = kv_indptr;
     prm.ckv = static_cast<const uint8_t*>(ckv_cache);
     prm.kpe = static_cast<const uint8_t*>(kpe_cache);
-    prm.out = out;
+    prm.out = static_cast<float*>(out);
     prm.lse = lse;
     prm.part_o = reinterpret_cast<float*>(ws + L.off_part_o);
     prm.part_lse = reinterpret_cast<float*>(ws + L.off_part_lse);
@@ -247,6 +247,7 @@ mla_status_t run_checked(mla_plan_t plan, const void* q_nope, const void* q_pe, 
     prm.page_size = d.page_size;
     prm.head_groups = d.head_groups;
     prm.num_pages = num_pages;
+    prm.out_bf16 = d.out_dtype == MLA_OUT_BF16 ? 1 : 0;
     cudaError_t e;
     if (d.e4m3) {
         e = launch_e4m3(plan, mc, prm, q_nope, q_pe, stream);
@@ -266,7 +267,7 @@ mla_status_t run_checked(mla_plan_t plan, const void* q_nope, const void* q_pe, 
 mla_status_t check_run_args(mla_plan_t plan, const void* q_nope, const void* q_pe, const void* ckv_cache,
                             const float* ckv_scale, const void* kpe_cache, int num_pages, const int32_t* kv_indices,
                             const int32_t* kv_indptr, const int32_t* kv_last_page_len, float sm_scale,
-                            const float* out, const float* lse) {
+                            const void* out, const float* lse) {
     if (!plan || !q_nope || !q_pe || !ckv_cache || !kpe_cache || !kv_indices || !kv_indptr || !kv_last_page_len ||
         !out || !lse || num_pages < 1)
         return MLA_ERR_INVALID_ARG;
@@ -287,10 +288,17 @@ extern "C" {
 
 mla_status_t mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_last_page_len_host, int batch,
                              int h_q, int page_size, int num_sms, mla_kv_dtype_t kv_dtype, mla_plan_t* plan_out) {
+    return mla_decode_plan_ex(kv_indptr_host, kv_last_page_len_host, batch, 1, 0, h_q, page_size, num_sms, kv_dtype,
+                              MLA_OUT_F32, plan_out);
+}
+
+mla_status_t mla_decode_plan_ex(const int32_t* kv_indptr_host, const int32_t* kv_last_page_len_host, int batch,
+                                int qo_len, int causal, int h_q, int page_size, int num_sms,
+                                mla_kv_dtype_t kv_dtype, mla_out_dtype_t out_dtype, mla_plan_t* plan_out) {
     if (!plan_out) return MLA_ERR_INVALID_ARG;
     mla::PlanData d;
-    const int rc = mla::build_plan(kv_indptr_host, kv_last_page_len_host, batch, h_q, page_size, num_sms,
-                                   static_cast<int>(kv_dtype), &d);
+    const int rc = mla::build_plan(kv_indptr_host, kv_last_page_len_host, batch, qo_len, causal != 0, h_q, page_size,
+                                   num_sms, static_cast<int>(kv_dtype), static_cast<int>(out_dtype), &d);
     if (rc == 1) return MLA_ERR_INVALID_ARG;
     if (rc == 2) return MLA_ERR_UNSUPPORTED;
     auto* p = new (std::nothrow) mla_plan_s;
@@ -326,7 +334,7 @@ mla_status_t mla_decode_plan_commit(mla_plan_t plan, void* workspace_dev, size_t
 mla_status_t mla_decode_run(mla_plan_t plan, const void* q_nope, const void* q_pe, const void* ckv_cache,
                             const float* ckv_scale, const void* kpe_cache, int num_pages,
                             const int32_t* kv_indices, const int32_t* kv_indptr,
-                            const int32_t* kv_last_page_len, float sm_scale, float* out, float* lse,
+                            const int32_t* kv_last_page_len, float sm_scale, void* out, float* lse,
                             void* workspace_dev, void* cuda_stream) {
     mla_status_t st = check_run_args(plan, q_nope, q_pe, ckv_cache, ckv_scale, kpe_cache, num_pages, kv_indices,
                                      kv_indptr, kv_last_page_len, sm_scale, out, lse);
@@ -373,6 +381,7 @@ int mla_plan_num_segments(mla_plan_t plan) { return plan ? static_cast<int>(plan
 int mla_plan_num_partials(mla_plan_t plan) { return plan ? plan->d.num_partials : 0; }
 int mla_plan_heads_per_cta(mla_plan_t plan) { return plan ? plan->d.heads_per_cta : 0; }
 int mla_plan_segment_cost_tiles(mla_plan_t plan) { return plan ? plan->d.segment_cost : 0; }
+int mla_plan_num_rows(mla_plan_t plan) { return plan ? plan->d.rows : 0; }
 
 int mla_plan_get_segments(mla_plan_t plan, int32_t* segments, int32_t* unit_ptr) {
     if (!plan) return 0;
@@ -447,7 +456,7 @@ extern "C" size_t mla_decode_noalloc_max_workspace_bytes(void) { return kNoAlloc
 extern "C" mla_status_t mla_decode_run_noalloc(mla_plan_t plan, const void* q_nope, const void* q_pe,
                                                const void* ckv_cache, const float* ckv_scale, const void* kpe_cache,
                                                int num_pages, const int32_t* kv_indices, const int32_t* kv_indptr,
-                                               const int32_t* kv_last_page_len, float sm_scale, float* out,
+                                               const int32_t* kv_last_page_len, float sm_scale, void* out,
                                                float* lse, void* cuda_stream) {
     mla_status_t st = check_run_args(plan, q_nope, q_pe, ckv_cache, ckv_scale, kpe_cache, num_pages, kv_indices,
                                      kv_indptr, kv_last_page_len, sm_scale, out, lse);

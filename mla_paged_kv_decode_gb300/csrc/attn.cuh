@@ -35,8 +35,8 @@ struct AttnParams {
     const int32_t* kv_indptr;
     const uint8_t* ckv;           // cache base addresses (L2 prefetch of whole pages)
     const uint8_t* kpe;
-    float* out;                   // [B, h_q, 512]
-    float* lse;                   // [B, h_q]
+    float* out;                   // [rows, h_q, 512]: fp32, or bf16 at the same address when out_bf16
+    float* lse;                   // [rows, h_q] fp32
     float* part_o;                // [num_partials, h_q, 512]
     float* part_lse;              // [num_partials, h_q]
     const float* ckv_scale;       // e4m3 cache: fp32 scale per token [num_pages * page_size], else null
@@ -48,7 +48,43 @@ struct AttnParams {
     int page_size;
     int head_groups;
     int num_pages;                // pages in the cache buffers
+    int out_bf16;                 // the final output is bf16 (partials stay fp32)
 };
+
+// A destination of fp32 results: a buffer base and its element type.  The final output may
+// be bf16 (rounded to nearest even); partials are always fp32.  Element offsets are counted
+// from the base in elements of the buffer's own type.
+struct OutDst {
+    float* base;
+    bool bf16;
+};
+
+__device__ __forceinline__ OutDst final_out(const AttnParams& prm) { return OutDst{prm.out, prm.out_bf16 != 0}; }
+__device__ __forceinline__ OutDst fp32_dst(float* base) { return OutDst{base, false}; }
+
+__device__ __forceinline__ void st_out(OutDst d, size_t i, float v) {
+    if (d.bf16)
+        reinterpret_cast<__nv_bfloat16*>(d.base)[i] = __float2bfloat16_rn(v);
+    else
+        d.base[i] = v;
+}
+
+__device__ __forceinline__ void st_out2(OutDst d, size_t i, float a, float b) {   // i even
+    if (d.bf16)
+        *reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(d.base) + i) = __floats2bfloat162_rn(a, b);
+    else
+        *reinterpret_cast<float2*>(d.base + i) = make_float2(a, b);
+}
+
+__device__ __forceinline__ void st_out4(OutDst d, size_t i, float4 v) {   // i a multiple of 4
+    if (d.bf16) {
+        __nv_bfloat162* p = reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(d.base) + i);
+        p[0] = __floats2bfloat162_rn(v.x, v.y);
+        p[1] = __floats2bfloat162_rn(v.z, v.w);
+    } else {
+        *reinterpret_cast<float4*>(d.base + i) = v;
+    }
+}
 
 // Bounded wait on an mbarrier phase.  Returns false if the kernel is aborting
 // (abort_flag set by another warp) or after kWaitLimitNs without completion, in which
@@ -166,7 +202,8 @@ __device__ __forceinline__ void merge_split_pieces_chunked(const AttnParams& prm
     }
     named_barrier_sync(bar, NTHR);
     // ---- outputs: thread tid owns dims [4 tid, 4 tid + 4) of every head
-    float4* out4 = reinterpret_cast<float4*>(prm.out + (static_cast<size_t>(b) * hq + head0) * kDimCkv) + tid;
+    const OutDst od = final_out(prm);
+    const size_t o0 = (static_cast<size_t>(b) * hq + head0) * kDimCkv + 4 * tid;
 #pragma unroll 1
     for (int hb = 0; hb < NH; hb += 16) {
         float4 acc[16];
@@ -203,7 +240,7 @@ __device__ __forceinline__ void merge_split_pieces_chunked(const AttnParams& prm
             named_barrier_sync(bar, NTHR);   // s_w is rewritten next
         }
 #pragma unroll
-        for (int h = 0; h < 16; ++h) out4[(hb + h) * (kDimCkv / 4)] = acc[h];
+        for (int h = 0; h < 16; ++h) st_out4(od, o0 + static_cast<size_t>(hb + h) * kDimCkv, acc[h]);
     }
 }
 
@@ -269,7 +306,8 @@ __device__ __forceinline__ void merge_split_pieces(const AttnParams& prm, int b,
         }
     }
     named_barrier_sync(bar, NTHR);
-    float4* out4 = reinterpret_cast<float4*>(prm.out + (static_cast<size_t>(b) * hq + head0) * kDimCkv) + tid;
+    const OutDst od = final_out(prm);
+    const size_t o0 = (static_cast<size_t>(b) * hq + head0) * kDimCkv + 4 * tid;
 #pragma unroll 1
     for (int hb = 0; hb < NH; hb += kHB) {
         float4 acc[kHB];
@@ -292,7 +330,7 @@ __device__ __forceinline__ void merge_split_pieces(const AttnParams& prm, int b,
             }
         }
 #pragma unroll
-        for (int h = 0; h < kHB; ++h) out4[(hb + h) * (kDimCkv / 4)] = acc[h];
+        for (int h = 0; h < kHB; ++h) st_out4(od, o0 + static_cast<size_t>(hb + h) * kDimCkv, acc[h]);
     }
 }
 
@@ -362,9 +400,10 @@ __device__ __forceinline__ void merge_split_pieces_wide16(const AttnParams& prm,
             }
         }
     }
-    float4* out4 = reinterpret_cast<float4*>(prm.out + (static_cast<size_t>(b) * hq + head0) * kDimCkv) + t;
+    const OutDst od = final_out(prm);
+    const size_t o0 = (static_cast<size_t>(b) * hq + head0) * kDimCkv + 4 * t;
 #pragma unroll
-    for (int h = 0; h < kHB; ++h) out4[(hb + h) * (kDimCkv / 4)] = acc[h];
+    for (int h = 0; h < kHB; ++h) st_out4(od, o0 + static_cast<size_t>(hb + h) * kDimCkv, acc[h]);
 }
 
 // Walks the non-empty segments of one CTA slot tile by tile.

@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(E4m3Cfg::kThreads, 1)
         const int32_t* pages = nullptr;
         while (more && ok) {
             if (new_seg) {
-                pages = prm.kv_indices + prm.kv_indptr[cur.sg.b];
+                pages = prm.kv_indices + prm.kv_indptr[cur.sg.kv];
                 win_base = -(1 << 30);
             }
             const int ntok = cur.ntok();
@@ -412,17 +412,20 @@ __global__ void __launch_bounds__(E4m3Cfg::kThreads, 1)
         bool ok = true;
         for (int si = seg_begin; si < seg_end && ok; ++si) {
             const Segment sg = prm.segments[si];
-            float* obase;
+            OutDst od;
+            size_t o0;
             float* lbase;
             if (sg.slot < 0) {
-                obase = prm.out + (static_cast<size_t>(sg.b) * prm.h_q + head0) * kDimCkv;
+                od = final_out(prm);
+                o0 = (static_cast<size_t>(sg.b) * prm.h_q + head0) * kDimCkv;
                 lbase = prm.lse + static_cast<size_t>(sg.b) * prm.h_q + head0;
             } else {
-                obase = prm.part_o + (static_cast<size_t>(sg.slot) * prm.h_q + head0) * kDimCkv;
+                od = fp32_dst(prm.part_o);
+                o0 = (static_cast<size_t>(sg.slot) * prm.h_q + head0) * kDimCkv;
                 lbase = prm.part_lse + static_cast<size_t>(sg.slot) * prm.h_q + head0;
             }
             if (sg.t_end <= sg.t_begin) {   // a request with no tokens
-                for (int i = tid; i < 16 * kDimCkv; i += 256) obase[i] = 0.f;
+                for (int i = tid; i < 16 * kDimCkv; i += 256) st_out(od, o0 + i, 0.f);
                 if (tid < 16) lbase[tid] = -INFINITY;
                 continue;
             }
@@ -657,8 +660,8 @@ __global__ void __launch_bounds__(E4m3Cfg::kThreads, 1)
                 tmem_wait_ld();
 #pragma unroll
                 for (int h = 0; h < 8; ++h)
-                    obase[static_cast<size_t>(hb + h) * kDimCkv + 128 * c + t] =
-                        (__uint_as_float(rh[h]) + __uint_as_float(rl[h])) * f[h];
+                    st_out(od, o0 + static_cast<size_t>(hb + h) * kDimCkv + 128 * c + t,
+                           (__uint_as_float(rh[h]) + __uint_as_float(rl[h])) * f[h]);
             }
             tc_fence_before();
             {

@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
         const int32_t* pages = nullptr;
         while (more && ok) {
             if (new_seg) {
-                pages = prm.kv_indices + prm.kv_indptr[cur.sg.b];
+                pages = prm.kv_indices + prm.kv_indptr[cur.sg.kv];
                 win_base = -(1 << 30);
             }
             const int ntok = cur.ntok();
@@ -284,8 +284,8 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
             const Segment sg = prm.segments[si];
             if (sg.t_end <= sg.t_begin) {
                 if (tg == 0) {
-                    float* o = prm.out + (static_cast<size_t>(sg.b) * prm.h_q + head0) * kDimCkv;
-                    for (int i = kr * 32 + lane; i < 16 * kDimCkv; i += 128) o[i] = 0.f;
+                    const size_t o0 = (static_cast<size_t>(sg.b) * prm.h_q + head0) * kDimCkv;
+                    for (int i = kr * 32 + lane; i < 16 * kDimCkv; i += 128) st_out(final_out(prm), o0 + i, 0.f);
                     if (kr == 0 && lane < 16) prm.lse[static_cast<size_t>(sg.b) * prm.h_q + head0 + lane] = -INFINITY;
                 }
                 continue;
@@ -537,22 +537,23 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
             if (tg == 0) {
                 // ---- epilogue (token group 0): normalise and store this warp's 128 dims
                 const float inv0 = 1.f / l[0], inv1 = 1.f / l[1];
-                float* obase;
+                OutDst od;
+                size_t o0;
                 float* lbase;
                 if (sg.slot < 0) {
-                    obase = prm.out + (static_cast<size_t>(sg.b) * prm.h_q + head0) * kDimCkv;
+                    od = final_out(prm);
+                    o0 = (static_cast<size_t>(sg.b) * prm.h_q + head0) * kDimCkv;
                     lbase = prm.lse + static_cast<size_t>(sg.b) * prm.h_q + head0;
                 } else {
-                    obase = prm.part_o + (static_cast<size_t>(sg.slot) * prm.h_q + head0) * kDimCkv;
+                    od = fp32_dst(prm.part_o);
+                    o0 = (static_cast<size_t>(sg.slot) * prm.h_q + head0) * kDimCkv;
                     lbase = prm.part_lse + static_cast<size_t>(sg.slot) * prm.h_q + head0;
                 }
 #pragma unroll
                 for (int n = 0; n < 16; ++n) {
                     const int d = kr * 128 + n * 8 + 2 * c4;
-                    *reinterpret_cast<float2*>(obase + static_cast<size_t>(g) * kDimCkv + d) =
-                        make_float2(o[n][0] * inv0, o[n][1] * inv0);
-                    *reinterpret_cast<float2*>(obase + static_cast<size_t>(g + 8) * kDimCkv + d) =
-                        make_float2(o[n][2] * inv1, o[n][3] * inv1);
+                    st_out2(od, o0 + static_cast<size_t>(g) * kDimCkv + d, o[n][0] * inv0, o[n][1] * inv0);
+                    st_out2(od, o0 + static_cast<size_t>(g + 8) * kDimCkv + d, o[n][2] * inv1, o[n][3] * inv1);
                 }
                 if (kr == 0 && c4 == 0) {
                     lbase[g] = (m_run[0] + log2f(l[0])) * 0.69314718055994530942f;

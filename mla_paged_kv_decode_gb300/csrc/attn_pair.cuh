@@ -230,7 +230,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                         tma_load_2d(smem + C::kOffQpe, &tm_qpe, &misc->q_full, 0, cur.sg.b * hq);
                     }
                     ++segc;
-                    pages = prm.kv_indices + prm.kv_indptr[cur.sg.b];
+                    pages = prm.kv_indices + prm.kv_indptr[cur.sg.kv];
                     win_base = -(1 << 30);
                 }
                 const int ntok = cur.ntok();
@@ -473,7 +473,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
             const int32_t* pages = nullptr;
             while (more && ok) {
                 if (new_seg) {
-                    pages = prm.kv_indices + prm.kv_indptr[cur.sg.b];
+                    pages = prm.kv_indices + prm.kv_indptr[cur.sg.kv];
                     win_base = -(1 << 30);
                 }
                 const int ntok = cur.ntok();
@@ -593,8 +593,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
             for (int si = seg_begin; si < seg_end; ++si) {
                 const Segment sg = prm.segments[si];
                 if (sg.t_end > sg.t_begin) continue;
-                float4* o = reinterpret_cast<float4*>(prm.out + static_cast<size_t>(sg.b) * hq * kDimCkv);
-                for (int i = h; i < hq * kDimCkv / 4; i += 128) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                const size_t o0 = static_cast<size_t>(sg.b) * hq * kDimCkv;
+                for (int i = h; i < hq * kDimCkv / 4; i += 128)
+                    st_out4(final_out(prm), o0 + 4 * static_cast<size_t>(i), make_float4(0.f, 0.f, 0.f, 0.f));
                 if (h < hq) prm.lse[static_cast<size_t>(sg.b) * hq + h] = -INFINITY;
             }
             uint32_t tcount = 0, vcount = 0, zcount = 0;
@@ -677,16 +678,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                     tc_fence_after();
                     const float inv = 1.f / fin_l;
                     const float lse_h = (fin_m + log2f(fin_l)) * 0.69314718055994530942f;
-                    float* obase;
+                    OutDst od;
+                    size_t orow;
                     float* lbase;
                     if (sg.slot < 0) {
-                        obase = prm.out + static_cast<size_t>(sg.b) * hq * kDimCkv;
+                        od = final_out(prm);
+                        orow = (static_cast<size_t>(sg.b) * hq + h) * kDimCkv;
                         lbase = prm.lse + static_cast<size_t>(sg.b) * hq;
                     } else {
-                        obase = prm.part_o + static_cast<size_t>(sg.slot) * hq * kDimCkv;
+                        od = fp32_dst(prm.part_o);
+                        orow = (static_cast<size_t>(sg.slot) * hq + h) * kDimCkv;
                         lbase = prm.part_lse + static_cast<size_t>(sg.slot) * hq;
                     }
-                    float4* orow = reinterpret_cast<float4*>(obase + static_cast<size_t>(h) * kDimCkv);
 #pragma unroll 1
                     for (int c = 0; c < 512; c += 32) {   // the TMEM loads are warp-collective: every lane
                         uint32_t r[32];
@@ -695,9 +698,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                         if (h < hq) {
 #pragma unroll
                             for (int i = 0; i < 8; ++i)
-                                orow[c / 4 + i] =
-                                    make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
-                                                __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
+                                st_out4(od, orow + c + 4 * i,
+                                        make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
+                                                    __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv));
                         }
                     }
                     if (h < hq) lbase[h] = lse_h;

@@ -12,6 +12,12 @@
 // partial write).  A request whose tiles land in more than one slot becomes
 // several split pieces, each writing a partial (out, lse); the CTA finishing the
 // last piece merges them in slot order.
+//
+// With qo_len query tokens per request (several new tokens decoded at once), every
+// (request, query token) pair is a query row of its own, laid out in order on the same
+// axis: row b * qo_len + j reads request b's pages, over its first L_b tokens, or, causal
+// within the new tokens, over its first L_b - (qo_len - 1 - j) (the new tokens being the
+// last qo_len of the cache).  Each row streams its pages itself.
 #include "plan.h"
 
 #include <algorithm>
@@ -35,10 +41,13 @@ int heads_per_cta_for(int h_q, int kv_dtype) {
     }
 }
 
-int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int batch, int h_q, int page_size,
-               int num_sms, int kv_dtype, PlanData* out) {
+int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int batch, int qo_len, bool causal,
+               int h_q, int page_size, int num_sms, int kv_dtype, int out_dtype, PlanData* out) {
     if (!kv_indptr || !kv_last_page_len || !out || batch < 1 || num_sms < 1) return 1;
     if (kv_dtype != 0 && kv_dtype != 1) return 1;
+    if (out_dtype != 0 && out_dtype != 1) return 1;
+    if (qo_len < 1 || qo_len > kMaxQoLen) return 1;
+    if (static_cast<int64_t>(batch) * qo_len * 128 >= (int64_t(1) << 31)) return 1;
     if (page_size != 16 && page_size != 32 && page_size != 64) return 2;
     const int hg = heads_per_cta_for(h_q, kv_dtype);
     if (hg == 0) return 2;
@@ -47,25 +56,33 @@ int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int ba
     const bool e4m3 = kv_dtype == 1;
     const bool narrow = h_q <= 32 && !e4m3;
     const int tile_tok = narrow ? kNarrowTileTokens : kTileTokens;
-    std::vector<int64_t> len(batch), tiles(batch);
+    const int rows = batch * qo_len;
+    std::vector<int64_t> len(rows), tiles(rows);
     int64_t total_tiles = 0;
     for (int b = 0; b < batch; ++b) {
         int64_t n = static_cast<int64_t>(kv_indptr[b + 1]) - kv_indptr[b];
         if (n < 0) return 1;
+        int64_t L = 0;
         if (n > 0) {
             int last = kv_last_page_len[b];
             if (last < 1 || last > page_size) return 1;
-            len[b] = (n - 1) * page_size + last;
-            if (len[b] > (int64_t(1) << 30)) return 1;
-        } else {
-            len[b] = 0;
+            L = (n - 1) * page_size + last;
+            if (L > (int64_t(1) << 30)) return 1;
         }
-        tiles[b] = (len[b] + tile_tok - 1) / tile_tok;
-        total_tiles += tiles[b];
+        for (int j = 0; j < qo_len; ++j) {
+            const int r = b * qo_len + j;
+            len[r] = causal ? std::max<int64_t>(0, L - (qo_len - 1 - j)) : L;
+            tiles[r] = (len[r] + tile_tok - 1) / tile_tok;
+            total_tiles += tiles[r];
+        }
     }
 
     PlanData p;
     p.batch = batch;
+    p.qo_len = qo_len;
+    p.causal = causal;
+    p.out_dtype = out_dtype;
+    p.rows = rows;
     p.h_q = h_q;
     p.page_size = page_size;
     p.num_sms = num_sms;
@@ -82,11 +99,11 @@ int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int ba
     p.num_units = static_cast<int>(units);
     p.segment_cost = narrow ? kNarrowSegmentCost : kSegmentCost;
 
-    // cost axis: request b occupies [start_b, start_b + c_b + tiles_b), its first c_b units
-    // being the request-start cost (0 for the first non-empty request)
+    // cost axis: row b occupies [start_b, start_b + c_b + tiles_b), its first c_b units
+    // being the request-start cost (0 for the first non-empty row)
     int64_t total_cost = 0;
     bool first = true;
-    for (int b = 0; b < batch; ++b) {
+    for (int b = 0; b < rows; ++b) {
         if (tiles[b] == 0) continue;
         total_cost += (first ? 0 : p.segment_cost) + tiles[b];
         first = false;
@@ -95,11 +112,11 @@ int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int ba
     auto bound = [&](int64_t u) { return u * total_cost / units; };
 
     std::vector<std::vector<Segment>> per_unit(units);
-    std::vector<int> pieces(batch, 0);
+    std::vector<int> pieces(rows, 0);
     int64_t cost_base = 0;
     int64_t u = 0;
     first = true;
-    for (int b = 0; b < batch; ++b) {
+    for (int b = 0; b < rows; ++b) {
         if (tiles[b] == 0) continue;
         const int64_t r0 = cost_base + (first ? 0 : p.segment_cost);   // cost position of tile 0
         const int64_t r1 = r0 + tiles[b];
@@ -109,6 +126,7 @@ int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int ba
             const int64_t end = std::min<int64_t>(r1, bound(u + 1));
             Segment s{};
             s.b = b;
+            s.kv = b / qo_len;
             s.t_begin = static_cast<int32_t>((t0 - r0) * tile_tok);
             s.t_end = static_cast<int32_t>(std::min<int64_t>((end - r0) * tile_tok, len[b]));
             s.slot = -1;
@@ -121,9 +139,9 @@ int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int ba
     }
 
     // partial slots: a split request's pieces get consecutive slots in token order
-    std::vector<int> slot_begin(batch, -1);
+    std::vector<int> slot_begin(rows, -1);
     int next_slot = 0;
-    for (int b = 0; b < batch; ++b) {
+    for (int b = 0; b < rows; ++b) {
         if (pieces[b] > 1) {
             slot_begin[b] = next_slot;
             next_slot += pieces[b];
@@ -131,17 +149,17 @@ int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int ba
     }
     // split requests get an arrival counter each; empty requests become zero-length
     // segments spread round-robin over the units (their CTA writes out = 0, lse = -inf)
-    std::vector<int> item_of(batch, -1);
+    std::vector<int> item_of(rows, -1);
     int next_item = 0;
-    for (int b = 0; b < batch; ++b)
+    for (int b = 0; b < rows; ++b)
         if (pieces[b] > 1) item_of[b] = next_item++;
     int rr = 0;
-    for (int b = 0; b < batch; ++b)
+    for (int b = 0; b < rows; ++b)
         if (pieces[b] == 0) {
-            per_unit[rr % units].push_back(Segment{b, 0, 0, -1, -1, 0, 0, 0});
+            per_unit[rr % units].push_back(Segment{b, 0, 0, -1, -1, 0, 0, b / qo_len});
             ++rr;
         }
-    std::vector<int> used(batch, 0);
+    std::vector<int> used(rows, 0);
     p.unit_ptr.push_back(0);
     for (int64_t v = 0; v < units; ++v) {
         for (Segment s : per_unit[v]) {

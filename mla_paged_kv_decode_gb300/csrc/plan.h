@@ -18,15 +18,16 @@ constexpr int kSegmentCost = 1;
 constexpr int kDimCkv = 512;
 constexpr int kDimKpe = 64;
 
-// One (request, token range) piece of work.  slot < 0: the piece is the whole
-// request and the kernel writes out/lse directly (t_begin == t_end == 0 for a
-// request with no tokens: out = 0, lse = -inf); otherwise it writes the
-// partial (out, lse) to partial slot `slot`, and the CTA that finishes the
-// request's last piece merges slots [slot_begin, slot_begin + n_slots) using
-// the arrival counter `item`.
+// One (query row, token range) piece of work.  `b` is the query row (q, out and lse are
+// indexed by it: row b * qo_len + j is query token j of request b) and `kv` the request
+// whose pages are read; with one query token per request they are equal.  slot < 0: the
+// piece is the whole row and the kernel writes out/lse directly (t_begin == t_end == 0 for
+// a row with no tokens: out = 0, lse = -inf); otherwise it writes the partial (out, lse)
+// to partial slot `slot`, and the CTA that finishes the row's last piece merges slots
+// [slot_begin, slot_begin + n_slots) using the arrival counter `item`.
 struct Segment {
     int32_t b, t_begin, t_end, slot;
-    int32_t item, slot_begin, n_slots, pad;
+    int32_t item, slot_begin, n_slots, kv;
 };
 
 struct PlanLayout {
@@ -42,6 +43,10 @@ struct PlanLayout {
 
 struct PlanData {
     int batch = 0, h_q = 0, page_size = 0, num_sms = 0, kv_dtype = 0;
+    int qo_len = 1;                   // query tokens per request
+    bool causal = false;              // query token j of qo_len sees the first L - (qo_len - 1 - j) tokens
+    int out_dtype = 0;                // 0: fp32 out, 1: bf16 out
+    int rows = 0;                     // query rows: batch * qo_len
     int heads_per_cta = 0, head_groups = 0, num_units = 0;
     int tile_tokens = 0;              // plan granularity = the kernel's tile
     bool narrow = false;              // bf16 cache, h_q <= 32: warp-MMA kernel
@@ -55,9 +60,11 @@ struct PlanData {
     PlanLayout layout;
 };
 
+constexpr int kMaxQoLen = 64;
+
 // Returns 0 on success, 1 invalid argument, 2 unsupported.
-int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int batch, int h_q, int page_size,
-               int num_sms, int kv_dtype, PlanData* out);
+int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int batch, int qo_len, bool causal,
+               int h_q, int page_size, int num_sms, int kv_dtype, int out_dtype, PlanData* out);
 
 // Heads handled by one CTA for a given h_q and cache type (0 if unsupported): bf16 cache, all
 // of them (the narrow-head kernel for h_q <= 32, the two-CTA kernel for 64/128); e4m3 cache,

@@ -137,6 +137,38 @@ def mla_decode_range(b, t_begin, t_end, q_nope, q_pe, ckv, kpe, kv_indices, kv_i
     return torch.from_numpy(out), torch.from_numpy(lse)
 
 
+def mla_decode_rows(q_nope, q_pe, ckv, kpe, kv_indices, kv_indptr, kv_last_page_len, sm_scale, qo_len: int,
+                    causal: bool, ckv_scale=None, lib=None):
+    """Several query tokens per request.  q_nope [B * qo_len, H, 512], q_pe [B * qo_len, H, 64];
+    row r = b * qo_len + j is query token j of request b, the new tokens being the last qo_len
+    of its L_b cached tokens.  The row attends to the first L_b tokens, or, causal, to the first
+    max(0, L_b - (qo_len - 1 - j)): each new token sees the cache up to itself.  Returns
+    (out [B * qo_len, H, 512], lse [B * qo_len, H]) in fp64; a row with no tokens gets 0, -inf.
+    Each row is the definition over its token prefix (``mla_decode_range`` of request b's pages)."""
+    lib = lib or load()
+    R, H, _ = q_nope.shape
+    P = ckv.shape[1]
+    B = R // qo_len
+    assert B * qo_len == R
+    indptr = [int(x) for x in kv_indptr]
+    out = torch.zeros(R, H, 512, dtype=torch.float64)
+    lse = torch.full((R, H), float("-inf"), dtype=torch.float64)
+    for b in range(B):
+        n = indptr[b + 1] - indptr[b]
+        L = (n - 1) * P + int(kv_last_page_len[b]) if n > 0 else 0
+        pages = kv_indices[indptr[b]:indptr[b + 1]]
+        one = torch.tensor([0, n], dtype=torch.int32)
+        for j in range(qo_len):
+            r = b * qo_len + j
+            Lr = max(0, L - (qo_len - 1 - j)) if causal else L
+            if Lr == 0:
+                continue
+            o, l = mla_decode_range(0, 0, Lr, q_nope[r:r + 1], q_pe[r:r + 1], ckv, kpe, pages, one, sm_scale,
+                                    ckv_scale=ckv_scale, lib=lib)
+            out[r], lse[r] = o, l
+    return out, lse
+
+
 def merge(o_parts, lse_parts, lib=None):
     """Merge k partials [k,H,D] / [k,H] (fixed order) -> (out [H,D], lse [H])."""
     lib = lib or load()

@@ -42,3 +42,38 @@ def brute_force(q_nope, q_pe, ckv, kpe, kv_indices, kv_indptr, kv_last_page_len,
         out[b] = torch.softmax(S, dim=1) @ V
         lse[b] = torch.logsumexp(S, dim=1)
     return out, lse
+
+
+def brute_force_rows(q_nope, q_pe, ckv, kpe, kv_indices, kv_indptr, kv_last_page_len, sm_scale, qo_len,
+                     causal, ckv_scale=None):
+    """Several query tokens per request (row b * qo_len + j is new token j of request b, the new
+    tokens being the last qo_len of the cache), written as a mask: the scores of the whole
+    request are formed and those of tokens after the row's own position are set to -inf
+    before ``torch.softmax``."""
+    R, H, Dc = q_nope.shape
+    B = R // qo_len
+    P = ckv.shape[1]
+    ckv64 = _dequant_e4m3(ckv, ckv_scale) if ckv.dtype == torch.uint8 else ckv.to(torch.float64)
+    kpe64 = kpe.to(torch.float64)
+    out = torch.zeros(R, H, Dc, dtype=torch.float64)
+    lse = torch.full((R, H), float("-inf"), dtype=torch.float64)
+    indptr = [int(x) for x in kv_indptr]
+    for b in range(B):
+        pages = [int(x) for x in kv_indices[indptr[b]:indptr[b + 1]]]
+        if not pages:
+            continue
+        L = (len(pages) - 1) * P + int(kv_last_page_len[b])
+        V = torch.stack([ckv64[pages[t // P], t % P] for t in range(L)])
+        K = torch.cat([V, torch.stack([kpe64[pages[t // P], t % P] for t in range(L)])], dim=1)
+        pos = torch.arange(L)
+        for j in range(qo_len):
+            r = b * qo_len + j
+            Q = torch.cat([q_nope[r].to(torch.float64), q_pe[r].to(torch.float64)], dim=1)
+            S = (Q @ K.T) * sm_scale
+            if causal:
+                S = S.masked_fill(pos > L - qo_len + j, float("-inf"))
+            if not torch.isfinite(S).any():
+                continue
+            out[r] = torch.softmax(S, dim=1) @ V
+            lse[r] = torch.logsumexp(S, dim=1)
+    return out, lse

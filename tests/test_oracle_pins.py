@@ -16,8 +16,8 @@ import pytest
 import torch
 
 import oracle
-from oracle.brute import brute_force
-from workloads import WORKLOADS, make_inputs, quantize_e4m3_per_token
+from oracle.brute import brute_force, brute_force_rows
+from workloads import WORKLOADS, make_inputs, quantize_e4m3_per_token, query_rows
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 CONSTS = {"ln2": math.log(2.0), "ln3": math.log(3.0), "ln4": math.log(4.0), "ln1.5": math.log(1.5)}
@@ -321,6 +321,65 @@ def test_fp8_oracle_equals_bf16_oracle_on_exact_codes(lib=None):
     ob, lb = oracle.mla_decode(inp.q_nope, inp.q_pe, ckv_bf, inp.kpe, inp.kv_indices, inp.kv_indptr,
                                inp.kv_last_page_len, inp.sm_scale, lib=lib)
     assert torch.equal(o8, ob) and torch.equal(l8, lb)
+
+
+# ---------------------------------------------------------------- several query tokens per request
+
+def _rows_args(inp, qn, qp):
+    return (qn, qp, inp.ckv, inp.kpe, inp.kv_indices, inp.kv_indptr, inp.kv_last_page_len, inp.sm_scale)
+
+
+@pytest.mark.parametrize("qo_len,causal", [(1, True), (3, True), (3, False), (4, True)])
+def test_rows_match_masked_brute_force(qo_len, causal):
+    """Row b * qo_len + j over its causal prefix (a range of the definition) equals the whole
+    request's scores with the later tokens masked to -inf before a library softmax.  Lengths
+    0, 1 and 2 leave some causal rows with no token at all."""
+    inp = _small(seed=31, kv_lens=(0, 1, 2, 5, 33, 70), H=3, P=16)
+    qn, qp = query_rows(inp, qo_len, seed=32)
+    out, lse = oracle.mla_decode_rows(*_rows_args(inp, qn, qp), qo_len, causal)
+    bo, bl = brute_force_rows(*_rows_args(inp, qn, qp), qo_len, causal)
+    assert torch.equal(torch.isinf(lse), torch.isinf(bl))
+    fin = torch.isfinite(bl)
+    assert (out - bo).abs().max().item() <= 1e-12
+    assert (lse[fin] - bl[fin]).abs().max().item() <= 1e-12
+    # the rows left with no token: out 0, lse -inf
+    if causal and qo_len > 1:
+        assert torch.isinf(lse[1 * qo_len]).all() and (out[1 * qo_len] == 0).all()   # L = 1, j = 0
+
+
+def test_rows_with_one_token_per_request_equal_decode():
+    inp = _small(seed=33)
+    out, lse = oracle.mla_decode_rows(*_rows_args(inp, inp.q_nope, inp.q_pe), 1, True)
+    o1, l1 = oracle.mla_decode(*_tiny_args(inp))
+    assert (out - o1).abs().max().item() <= 1e-13
+    assert (lse - l1).abs().max().item() <= 1e-13
+
+
+def test_causal_rows_first_and_last():
+    """With L = qo_len, new token 0 sees only token 0 (out = its ckv row, exactly); the last new
+    token sees the whole request, as a one-token decode with that query does."""
+    qo_len = 4
+    inp = _small(seed=34, kv_lens=(4, 50), H=2, P=16)
+    qn, qp = query_rows(inp, qo_len, seed=35)
+    out, lse = oracle.mla_decode_rows(*_rows_args(inp, qn, qp), qo_len, True)
+    pg = int(inp.kv_indices[inp.kv_indptr[0]])
+    assert torch.equal(out[0], inp.ckv[pg, 0].to(torch.float64).expand_as(out[0]))
+    last = torch.tensor([b * qo_len + qo_len - 1 for b in range(inp.batch)])
+    o1, l1 = oracle.mla_decode(qn[last], qp[last], inp.ckv, inp.kpe, inp.kv_indices, inp.kv_indptr,
+                               inp.kv_last_page_len, inp.sm_scale)
+    assert (out[last] - o1).abs().max().item() <= 1e-13
+    assert (lse[last] - l1).abs().max().item() <= 1e-13
+
+
+def test_non_causal_rows_with_equal_queries_are_equal():
+    qo_len = 3
+    inp = _small(seed=36, kv_lens=(9, 40), H=2, P=16)
+    qn = inp.q_nope.repeat_interleave(qo_len, dim=0)
+    qp = inp.q_pe.repeat_interleave(qo_len, dim=0)
+    out, lse = oracle.mla_decode_rows(*_rows_args(inp, qn, qp), qo_len, False)
+    o1, _ = oracle.mla_decode(*_tiny_args(inp))
+    for j in range(qo_len):
+        assert (out[j::qo_len] - o1).abs().max().item() <= 1e-13
 
 
 # ---------------------------------------------------------------- the pins catch planted mistakes

@@ -165,3 +165,50 @@ def test_request_starts_cost_tiles():
     assert inside and crossing
     # a unit ending inside the next request's start cost also has fewer tiles, so compare means
     assert sum(inside) / len(inside) - sum(crossing) / len(crossing) >= c / 2
+
+
+@pytest.mark.parametrize("qo_len,causal,h_q,kv_dtype", [(2, True, 16, mla.MLA_KV_BF16), (3, True, 128, mla.MLA_KV_BF16),
+                                                         (3, False, 64, mla.MLA_KV_BF16), (4, True, 16, mla.MLA_KV_FP8_E4M3)])
+def test_query_rows_plan(qo_len, causal, h_q, kv_dtype):
+    """Several query tokens per request: row b * qo_len + j covers exactly the first
+    max(0, L_b - (qo_len - 1 - j)) tokens (causal) or all L_b, once, and nothing else."""
+    rng = random.Random(7 + qo_len)
+    P = 16
+    lens = [rng.choice([0, 1, 2, rng.randint(3, 300), rng.randint(300, 5000)]) for _ in range(37)]
+    indptr, last = _lens_to_arrays(lens, P)
+    plan = mla.mla_decode_plan_ex(torch.from_numpy(indptr), torch.from_numpy(last), len(lens), qo_len, causal, h_q,
+                                  P, 152, kv_dtype, mla.MLA_OUT_BF16)
+    assert mla.mla_plan_num_rows(plan) == len(lens) * qo_len
+    segs, uptr = mla.mla_plan_get_segments(plan)
+    covered = {}
+    for r, t0, t1, _ in segs:
+        covered.setdefault(int(r), []).append((int(t0), int(t1)))
+    for b, L in enumerate(lens):
+        for j in range(qo_len):
+            r = b * qo_len + j
+            Lr = max(0, L - (qo_len - 1 - j)) if causal else L
+            pieces = sorted(covered.get(r, []))
+            assert pieces, f"row {r} missing"
+            if Lr == 0:
+                assert pieces == [(0, 0)]
+                continue
+            assert pieces[0][0] == 0 and pieces[-1][1] == Lr
+            for (a0, a1), (b0, b1) in zip(pieces, pieces[1:]):
+                assert a1 == b0
+    assert set(covered) == set(range(len(lens) * qo_len))
+
+
+def test_query_rows_argument_checks():
+    indptr, last = _lens_to_arrays([5, 9], 16)
+    ip, lp = torch.from_numpy(indptr), torch.from_numpy(last)
+    for qo_len in (0, 65):
+        with pytest.raises(mla.MLAError):
+            mla.mla_decode_plan_ex(ip, lp, 2, qo_len, True, 16, 16, 152)
+    with pytest.raises(mla.MLAError):
+        mla.mla_decode_plan_ex(ip, lp, 2, 2, True, 16, 16, 152, out_dtype=2)
+    # qo_len 1 with fp32 output is mla_decode_plan itself
+    a = mla.mla_decode_plan(ip, lp, 2, 16, 16, 152)
+    b = mla.mla_decode_plan_ex(ip, lp, 2, 1, True, 16, 16, 152)
+    sa, ua = mla.mla_plan_get_segments(a)
+    sb, ub = mla.mla_plan_get_segments(b)
+    assert np.array_equal(sa, sb) and np.array_equal(ua, ub)

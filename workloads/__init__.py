@@ -201,6 +201,17 @@ def make_inputs(w: Workload, *, kv_lens=None, batch=None, h_q=None, page_size=No
                   torch.tensor(kv_lens, dtype=torch.int64), ckv_scale, ckv_bf16)
 
 
+def query_rows(inp: Inputs, qo_len: int, seed: int):
+    """Queries for qo_len new tokens per request, from their own seeded generator:
+    (q_nope [B * qo_len, H, 512], q_pe [B * qo_len, H, 64]) bf16, row b * qo_len + j being
+    token j of request b."""
+    gen = torch.Generator().manual_seed(seed)
+    R = inp.batch * qo_len
+    q_nope = torch.randn(R, inp.h_q, D_CKV, generator=gen).to(torch.bfloat16)
+    q_pe = torch.randn(R, inp.h_q, D_KPE, generator=gen).to(torch.bfloat16)
+    return q_nope, q_pe
+
+
 def algorithmic_bytes(inp: Inputs) -> int:
     """Bytes the method must move once: the KV tokens, q, out, lse and the page indices."""
     H = inp.h_q
