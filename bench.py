@@ -51,9 +51,13 @@ def peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the sources the attention kernels are built from (the prologue kernel, a
+    separate translation unit, is not one of them)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_paged_kv_decode_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
+        if f == "prologue.cu":
+            continue
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]

@@ -219,6 +219,47 @@ mla_status_t mla_decode_run_noalloc(mla_plan_t plan, const void* q_nope, const v
 /* Size of the fixed workspace array mla_decode_run_noalloc uses (bytes). */
 size_t mla_decode_noalloc_max_workspace_bytes(void);
 
+/* The decode prologue: one launch that prepares the new tokens before the decode
+ * (FlashMLA PR #233: "one prologue kernel (RoPE, concat, cache write,
+ * quantize-on-write)").  The new tokens are the last qo_len tokens of each request,
+ * so kv_indptr / kv_last_page_len already count them (the same arrays the plan is
+ * built from); row r = b * qo_len + j is token j of request b, at position
+ * t = L_b - qo_len + j in page kv_indices[kv_indptr[b] + t / page_size], slot
+ * t % page_size.  For each row:
+ *   q_pe_out[r, h, :]      = rope(q_pe_in[r, h, :], t) for every head h
+ *   kpe_cache[page, slot]  = rope(kpe_new[r, :], t)
+ *   ckv_cache[page, slot]  = ckv_new[r, :]               (MLA_KV_BF16)
+ *   or, MLA_KV_FP8_E4M3 (quantise on write, every step in fp32):
+ *     s = max_i |ckv_new[r, i]| / 448, ckv_scale[page, slot] = s,
+ *     ckv_cache[page, slot, i] = e4m3(clamp(ckv_new[r, i] / s, -448, 448)), rounded to
+ *     nearest even (s = 0 and codes 0 when the token is all zeros).
+ * q_nope needs no work: the decode reads [q_nope | q_pe] as two buffers.
+ * rope(x, t) rotates 32 pairs of the 64 rope dims ("partial apply RoPE (only on first
+ * 64-dimension)", "Benchmarking MLA", FlashInfer issue #700): pair i, (x, y) ->
+ * (x c - y s, x s + y c) with c = rope_cos_sin[t * 64 + i], s = rope_cos_sin[t * 64 + 32 + i],
+ * computed in fp32 and rounded to bf16.  Pair i is dims (2i, 2i + 1) when
+ * rope_interleaved != 0, else (i, i + 32).
+ *
+ *   batch, qo_len      requests (>= 1) and new tokens per request (1 .. 64)
+ *   h_q, page_size     1 .. 128 heads; 16, 32 or 64
+ *   kv_dtype           the cache type (ckv_scale NULL for bf16, required for e4m3)
+ *   q_pe_in, q_pe_out  device bf16 [batch * qo_len, h_q, 64]; may be the same buffer
+ *   ckv_new, kpe_new   device bf16 [batch * qo_len, 512] (8-byte aligned), [batch * qo_len, 64]
+ *   rope_cos_sin       device fp32 [max_pos, 64]
+ *   kv_indices, kv_indptr, kv_last_page_len   device int32, as for mla_decode_run
+ *   ckv_cache, ckv_scale, kpe_cache           device caches, written in place
+ *   num_pages          pages in the cache buffers
+ * A row whose position is negative (a request shorter than qo_len) or >= max_pos is left
+ * untouched; a page index outside [0, num_pages) is not written.  One kernel launch on
+ * cuda_stream, no allocation, no synchronisation.  Returns MLA_OK, MLA_ERR_INVALID_ARG,
+ * MLA_ERR_UNSUPPORTED or MLA_ERR_CUDA. */
+mla_status_t mla_decode_prologue(int batch, int qo_len, int h_q, int page_size, mla_kv_dtype_t kv_dtype,
+                                 int rope_interleaved, const void* q_pe_in, void* q_pe_out, const void* ckv_new,
+                                 const void* kpe_new, const float* rope_cos_sin, int max_pos,
+                                 const int32_t* kv_indices, const int32_t* kv_indptr,
+                                 const int32_t* kv_last_page_len, void* ckv_cache, float* ckv_scale,
+                                 void* kpe_cache, int num_pages, void* cuda_stream);
+
 void mla_plan_destroy(mla_plan_t plan);
 
 /* Static string for a status code. */

@@ -19,7 +19,7 @@ from ._binding import (  # noqa: F401
     mla_plan_num_ctas, mla_plan_num_partials, mla_plan_num_segments, mla_status_string,
     mla_plan_num_launches, mla_decode_run_noalloc, mla_decode_noalloc_max_workspace_bytes,
     mla_plan_segment_cost_tiles, mla_plan_num_units, MLA_OUT_F32, MLA_OUT_BF16, mla_decode_plan_ex,
-    mla_plan_num_rows,
+    mla_plan_num_rows, mla_decode_prologue,
 )
 
 

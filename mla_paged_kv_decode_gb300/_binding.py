@@ -36,6 +36,7 @@ EXPORTED = (
     "mla_plan_heads_per_cta", "mla_plan_get_segments", "mla_plan_destroy", "mla_status_string",
     "mla_plan_num_launches", "mla_decode_run_noalloc", "mla_decode_noalloc_max_workspace_bytes",
     "mla_plan_segment_cost_tiles", "mla_plan_num_units", "mla_decode_plan_ex", "mla_plan_num_rows",
+    "mla_decode_prologue",
 )
 
 _lib = None
@@ -68,6 +69,8 @@ def load(path: Optional[str] = None):
                                     ctypes.c_int, ctypes.POINTER(vp)]
     lib.mla_decode_plan_ex.restype = ctypes.c_int
     lib.mla_decode_plan_ex.argtypes = [i32p, i32p] + [ctypes.c_int] * 8 + [ctypes.POINTER(vp)]
+    lib.mla_decode_prologue.restype = ctypes.c_int
+    lib.mla_decode_prologue.argtypes = [ctypes.c_int] * 6 + [vp] * 5 + [ctypes.c_int] + [vp] * 6 + [ctypes.c_int, vp]
     lib.mla_decode_plan_workspace_bytes.restype = sz
     lib.mla_decode_plan_workspace_bytes.argtypes = [vp]
     lib.mla_decode_plan_commit.restype = ctypes.c_int
@@ -164,6 +167,17 @@ def mla_decode_plan_ex(kv_indptr, kv_last_page_len, batch: int, qo_len: int, cau
                                 int(out_dtype), ctypes.byref(h))
     _check(st, "mla_decode_plan_ex")
     return Plan(h, batch, h_q, page_size, kv_dtype, qo_len, bool(causal), out_dtype)
+
+
+def mla_decode_prologue(batch: int, qo_len: int, h_q: int, page_size: int, kv_dtype: int, rope_interleaved: bool,
+                        q_pe_in, q_pe_out, ckv_new, kpe_new, rope_cos_sin, kv_indices, kv_indptr, kv_last_page_len,
+                        ckv_cache, ckv_scale, kpe_cache, stream=None):
+    _check(load().mla_decode_prologue(int(batch), int(qo_len), int(h_q), int(page_size), int(kv_dtype),
+                                      int(bool(rope_interleaved)), _ptr(q_pe_in), _ptr(q_pe_out), _ptr(ckv_new),
+                                      _ptr(kpe_new), _ptr(rope_cos_sin), int(rope_cos_sin.shape[0]), _ptr(kv_indices),
+                                      _ptr(kv_indptr), _ptr(kv_last_page_len), _ptr(ckv_cache), _ptr(ckv_scale),
+                                      _ptr(kpe_cache), int(ckv_cache.shape[0]), _stream(stream)),
+           "mla_decode_prologue")
 
 
 def mla_plan_num_rows(plan: Plan) -> int:

@@ -14,7 +14,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB_PATH = os.path.join(HERE, "libmla_decode.so")
-SOURCES = ["api.cu", "plan.cpp"]
+SOURCES = ["api.cu", "plan.cpp", "prologue.cu"]
 GENCODE = "-gencode=arch=compute_103a,code=sm_103a"
 
 

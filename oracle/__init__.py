@@ -169,6 +169,65 @@ def mla_decode_rows(q_nope, q_pe, ckv, kpe, kv_indices, kv_indptr, kv_last_page_
     return out, lse
 
 
+def rope_f64(x, cos, sin, interleaved: bool):
+    """Rotate the 32 pairs of the last (64) dim of x in fp64: pair i is dims (2i, 2i + 1)
+    when interleaved, else (i, i + 32); (a, b) -> (a cos_i - b sin_i, a sin_i + b cos_i)."""
+    x = torch.as_tensor(x).to(torch.float64)
+    c = torch.as_tensor(cos).to(torch.float64)
+    s = torch.as_tensor(sin).to(torch.float64)
+    ia = torch.arange(32) * 2 if interleaved else torch.arange(32)
+    ib = ia + 1 if interleaved else ia + 32
+    a, b = x[..., ia], x[..., ib]
+    out = x.clone()
+    out[..., ia] = a * c - b * s
+    out[..., ib] = a * s + b * c
+    return out
+
+
+def decode_prologue(q_pe, ckv_new, kpe_new, rope_cos_sin, kv_indices, kv_indptr, kv_last_page_len, qo_len: int,
+                    interleaved: bool, ckv_cache, kpe_cache, ckv_scale=None, lib=None):
+    """The decode prologue on CPU tensors; returns new (q_pe_out, ckv_cache, kpe_cache, ckv_scale)
+    and leaves the inputs untouched.  Row r = b * qo_len + j is new token j of request b, at
+    position t = L_b - qo_len + j (the new tokens are the last qo_len of the cache), page
+    kv_indices[kv_indptr[b] + t // P], slot t % P; a row with t < 0 or t >= max_pos is skipped.
+    q_pe and kpe are rotated (``rope_f64``, then rounded to bf16); ckv is copied, or for the
+    8-bit cache quantised with s = absmax / 448 and codes e4m3(x / s), both in fp32 (the
+    precision the quantised code is decided in), ``e4m3_encode`` rounding to nearest even."""
+    lib = lib or load()
+    P = ckv_cache.shape[1]
+    num_pages = ckv_cache.shape[0]
+    max_pos = rope_cos_sin.shape[0]
+    q_out, ckv, kpe = q_pe.clone(), ckv_cache.clone(), kpe_cache.clone()
+    sc = ckv_scale.clone() if ckv_scale is not None else None
+    indptr = [int(x) for x in kv_indptr]
+    for r in range(q_pe.shape[0]):
+        b, j = divmod(r, qo_len)
+        n = indptr[b + 1] - indptr[b]
+        L = (n - 1) * P + int(kv_last_page_len[b]) if n > 0 else 0
+        t = L - qo_len + j
+        if t < 0 or t >= max_pos:
+            continue
+        c, s = rope_cos_sin[t, :32], rope_cos_sin[t, 32:]
+        q_out[r] = rope_f64(q_pe[r], c, s, interleaved).to(torch.bfloat16)
+        page = int(kv_indices[indptr[b] + t // P])
+        if not 0 <= page < num_pages:
+            continue
+        slot = t % P
+        kpe[page, slot] = rope_f64(kpe_new[r], c, s, interleaved).to(torch.bfloat16)
+        if ckv.dtype == torch.uint8:
+            x = ckv_new[r].to(torch.float32).numpy()
+            scale = np.float32(np.abs(x).max()) / np.float32(448.0)
+            if scale > 0:
+                y = np.clip(x / scale, np.float32(-448.0), np.float32(448.0)).astype(np.float32)
+                ckv[page, slot] = torch.from_numpy(e4m3_encode(y, lib=lib))
+            else:
+                ckv[page, slot] = 0
+            sc[page, slot] = float(scale)
+        else:
+            ckv[page, slot] = ckv_new[r]
+    return q_out, ckv, kpe, sc
+
+
 def merge(o_parts, lse_parts, lib=None):
     """Merge k partials [k,H,D] / [k,H] (fixed order) -> (out [H,D], lse [H])."""
     lib = lib or load()

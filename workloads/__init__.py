@@ -212,6 +212,27 @@ def query_rows(inp: Inputs, qo_len: int, seed: int):
     return q_nope, q_pe
 
 
+def rope_table(max_pos: int, base: float = 10000.0) -> torch.Tensor:
+    """fp32 [max_pos, 64]: cos(t * base^(-i / 32)) for pairs i = 0..31, then their sin (the
+    usual rotary frequencies over the 64 rope dims)."""
+    t = torch.arange(max_pos, dtype=torch.float64).unsqueeze(1)
+    inv = base ** (-torch.arange(32, dtype=torch.float64) / 32.0)
+    ang = t * inv
+    return torch.cat([torch.cos(ang), torch.sin(ang)], dim=1).to(torch.float32)
+
+
+def new_tokens(inp: Inputs, qo_len: int, seed: int):
+    """The new tokens' inputs to the prologue, from their own seeded generator: pre-rotation
+    q_pe [B * qo_len, H, 64], latent ckv [B * qo_len, 512] and pre-rotation kpe [B * qo_len, 64],
+    all bf16."""
+    gen = torch.Generator().manual_seed(seed)
+    R = inp.batch * qo_len
+    q_pe = torch.randn(R, inp.h_q, D_KPE, generator=gen).to(torch.bfloat16)
+    ckv = torch.randn(R, D_CKV, generator=gen).to(torch.bfloat16)
+    kpe = torch.randn(R, D_KPE, generator=gen).to(torch.bfloat16)
+    return q_pe, ckv, kpe
+
+
 def algorithmic_bytes(inp: Inputs) -> int:
     """Bytes the method must move once: the KV tokens, q, out, lse and the page indices."""
     H = inp.h_q
