@@ -117,3 +117,27 @@ def test_fp8_plan_and_run_checks(lib):
     rc = lib.mla_decode_run(plan16.handle, fake, fake, fake, fake, fake, 4, fake, fake, fake, ctypes.c_float(0.1),
                             fake, fake, vp(1 << 21), None)
     assert rc == mla.MLA_ERR_INVALID_ARG
+
+
+def test_prologue_rejects_bad_arguments_without_touching_a_gpu(lib):
+    """Every case fails a host check before any CUDA call (the pointers are never dereferenced)."""
+    vp = ctypes.c_void_p
+    f = vp(1 << 20)
+
+    def rc(batch=1, qo_len=1, h_q=16, P=16, dtype=mla.MLA_KV_BF16, scale=None, max_pos=8, num_pages=4, ckv_new=f,
+           q_in=f):
+        return lib.mla_decode_prologue(batch, qo_len, h_q, P, dtype, 1, q_in, f, ckv_new, f, f, max_pos, f, f, f, f,
+                                       scale, f, num_pages, None)
+
+    assert rc(batch=0) == mla.MLA_ERR_INVALID_ARG
+    assert rc(qo_len=0) == mla.MLA_ERR_INVALID_ARG
+    assert rc(qo_len=65) == mla.MLA_ERR_INVALID_ARG
+    assert rc(h_q=0) == mla.MLA_ERR_INVALID_ARG
+    assert rc(max_pos=0) == mla.MLA_ERR_INVALID_ARG
+    assert rc(num_pages=0) == mla.MLA_ERR_INVALID_ARG
+    assert rc(P=24) == mla.MLA_ERR_UNSUPPORTED
+    assert rc(dtype=7) == mla.MLA_ERR_INVALID_ARG
+    assert rc(dtype=mla.MLA_KV_FP8_E4M3) == mla.MLA_ERR_INVALID_ARG              # 8-bit cache without scales
+    assert rc(dtype=mla.MLA_KV_BF16, scale=f) == mla.MLA_ERR_INVALID_ARG         # bf16 cache with scales
+    assert rc(ckv_new=vp((1 << 20) + 4)) == mla.MLA_ERR_INVALID_ARG               # latent rows need 8-byte alignment
+    assert rc(q_in=None) == mla.MLA_ERR_INVALID_ARG
