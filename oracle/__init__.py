@@ -90,10 +90,11 @@ def _ip(a: np.ndarray):
 
 
 def _cache_arrays(ckv, ckv_scale):
-    if ckv.dtype == torch.uint8:
+    """(codes or bf16 bits, cache kind: 0 bf16, 1 e4m3 codes (uint8), 2 int8 codes, scales)."""
+    if ckv.dtype in (torch.uint8, torch.int8):
         assert ckv_scale is not None, "8-bit cache needs its per-token scales"
-        return np.ascontiguousarray(ckv.contiguous().numpy()), 1, \
-            np.ascontiguousarray(ckv_scale.contiguous().to(torch.float32).numpy())
+        return np.ascontiguousarray(ckv.contiguous().view(torch.uint8).numpy()), \
+            (1 if ckv.dtype == torch.uint8 else 2), np.ascontiguousarray(ckv_scale.contiguous().to(torch.float32).numpy())
     return _u16(ckv), 0, None
 
 

@@ -16,11 +16,20 @@ def _dequant_e4m3(codes: torch.Tensor, scale: torch.Tensor) -> torch.Tensor:
     return codes.view(torch.float8_e4m3fn).to(torch.float64) * scale.to(torch.float64).unsqueeze(-1)
 
 
+def _dequant(ckv: torch.Tensor, scale) -> torch.Tensor:
+    """The cache in fp64: bf16 as is; uint8 as e4m3 codes, int8 as integers, times the token's scale."""
+    if ckv.dtype == torch.uint8:
+        return _dequant_e4m3(ckv, scale)
+    if ckv.dtype == torch.int8:
+        return ckv.to(torch.float64) * scale.to(torch.float64).unsqueeze(-1)
+    return ckv.to(torch.float64)
+
+
 def brute_force(q_nope, q_pe, ckv, kpe, kv_indices, kv_indptr, kv_last_page_len, sm_scale,
                 ckv_scale=None):
     B, H, Dc = q_nope.shape
     P = ckv.shape[1]
-    ckv64 = _dequant_e4m3(ckv, ckv_scale) if ckv.dtype == torch.uint8 else ckv.to(torch.float64)
+    ckv64 = _dequant(ckv, ckv_scale)
     kpe64 = kpe.to(torch.float64)
     out = torch.zeros(B, H, Dc, dtype=torch.float64)
     lse = torch.full((B, H), float("-inf"), dtype=torch.float64)
@@ -53,7 +62,7 @@ def brute_force_rows(q_nope, q_pe, ckv, kpe, kv_indices, kv_indptr, kv_last_page
     R, H, Dc = q_nope.shape
     B = R // qo_len
     P = ckv.shape[1]
-    ckv64 = _dequant_e4m3(ckv, ckv_scale) if ckv.dtype == torch.uint8 else ckv.to(torch.float64)
+    ckv64 = _dequant(ckv, ckv_scale)
     kpe64 = kpe.to(torch.float64)
     out = torch.zeros(R, H, Dc, dtype=torch.float64)
     lse = torch.full((R, H), float("-inf"), dtype=torch.float64)

@@ -33,7 +33,9 @@
  *   8-bit cache (FlashMLA PR #233, "FP8 e4m3 ... with one scale per token
  *   (644 instead of 1152 bytes per token), dequantized inside the kernel"):
  *   ckv_t[i] = scale_t * e4m3(code_t[i]) in exact fp64, used for both the key
- *   and the value; kpe stays bf16.  E4M3 follows the OCP 8-bit floating
+ *   and the value; kpe stays bf16.  The same page's INT8 variant ("FP8 e4m3 or
+ *   INT8 with one scale per token") reads ckv_t[i] = scale_t * code_t[i] with the
+ *   code a two's-complement signed byte.  E4M3 follows the OCP 8-bit floating
  *   point definition: 1 sign, 4 exponent (bias 7), 3 mantissa bits,
  *   subnormals at exponent field 0, no infinities, S.1111.111 is NaN,
  *   largest finite magnitude 448.
@@ -108,10 +110,18 @@ typedef struct {
 
 static void load_token(const cache_view* c, int page, int slot, double* ckv_row, double* kpe_row) {
     size_t tok = (size_t)page * (size_t)c->page_size + (size_t)slot;
-    if (c->ckv_is_fp8) {
+    if (c->ckv_is_fp8 == 1) {
         const uint8_t* codes = (const uint8_t*)c->ckv + tok * ORACLE_D_CKV;
         double s = (double)c->ckv_scale[tok];
         for (int i = 0; i < ORACLE_D_CKV; ++i) ckv_row[i] = s * oracle_e4m3_decode(codes[i]);
+    } else if (c->ckv_is_fp8 == 2) {
+#if ORACLE_PLANT == 4
+        const uint8_t* codes = (const uint8_t*)c->ckv + tok * ORACLE_D_CKV;   /* planted: codes read unsigned */
+#else
+        const int8_t* codes = (const int8_t*)c->ckv + tok * ORACLE_D_CKV;
+#endif
+        double s = (double)c->ckv_scale[tok];
+        for (int i = 0; i < ORACLE_D_CKV; ++i) ckv_row[i] = s * (double)codes[i];
     } else {
         const uint16_t* row = (const uint16_t*)c->ckv + tok * ORACLE_D_CKV;
         for (int i = 0; i < ORACLE_D_CKV; ++i) ckv_row[i] = bf16_bits_to_double(row[i]);
@@ -217,7 +227,7 @@ static int request_len(int b, int P, const int32_t* kv_indptr, const int32_t* kv
 }
 
 /* Full decode.  q_nope [B,H,512] bf16 bits, q_pe [B,H,64] bf16 bits,
- * ckv [num_pages,P,512] (bf16 bits, or e4m3 codes when ckv_is_fp8),
+ * ckv [num_pages,P,512] (bf16 bits; e4m3 codes when ckv_is_fp8 == 1, int8 codes when 2),
  * ckv_scale [num_pages,P] fp32 (8-bit cache only, else NULL),
  * kpe [num_pages,P,64] bf16 bits.  out [B,H,512], lse [B,H] in fp64.
  * threads <= 0 uses the OpenMP default.  Returns 0 on success. */

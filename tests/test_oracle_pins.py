@@ -17,7 +17,7 @@ import torch
 
 import oracle
 from oracle.brute import brute_force, brute_force_rows
-from workloads import WORKLOADS, make_inputs, quantize_e4m3_per_token, query_rows
+from workloads import WORKLOADS, make_inputs, quantize_e4m3_per_token, quantize_int8_per_token, query_rows
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 CONSTS = {"ln2": math.log(2.0), "ln3": math.log(3.0), "ln4": math.log(4.0), "ln1.5": math.log(1.5)}
@@ -323,6 +323,61 @@ def test_fp8_oracle_equals_bf16_oracle_on_exact_codes(lib=None):
     assert torch.equal(o8, ob) and torch.equal(l8, lb)
 
 
+# ---------------------------------------------------------------- the INT8 cache (oracle side)
+
+def test_matches_brute_force_int8(lib=None):
+    inp = make_inputs(WORKLOADS["fp8"], kv_lens=[5, 70, 128], batch=3, h_q=4, page_size=64, seed=22, int8=True)
+    assert inp.ckv.dtype == torch.int8
+    out, lse = oracle.mla_decode(*_tiny_args(inp), ckv_scale=inp.ckv_scale, lib=lib)
+    bo, bl = brute_force(*_tiny_args(inp), ckv_scale=inp.ckv_scale)
+    assert torch.isfinite(out).all()
+    assert (out - bo).abs().max().item() <= 1e-12
+    assert (lse - bl).abs().max().item() <= 1e-12
+
+
+def test_int8_oracle_equals_bf16_oracle_on_exact_codes(lib=None):
+    """Power-of-two scales times integer codes in [-127, 127] are exact in bf16: the INT8 oracle
+    and the bf16 oracle then see identical numbers (signed codes: a byte read unsigned fails)."""
+    inp = _small(seed=15, kv_lens=(20, 45), H=2, P=16)
+    g = torch.Generator().manual_seed(6)
+    codes = torch.randint(-127, 128, inp.ckv.shape, generator=g, dtype=torch.int32).to(torch.int8)
+    scale = torch.pow(2.0, torch.randint(-8, 2, inp.ckv.shape[:2], generator=g).float())
+    ckv_bf = (codes.float() * scale[..., None]).bfloat16()
+    assert torch.equal(ckv_bf.double(), codes.double() * scale[..., None].double())
+    o8, l8 = oracle.mla_decode(inp.q_nope, inp.q_pe, codes, inp.kpe, inp.kv_indices, inp.kv_indptr,
+                               inp.kv_last_page_len, inp.sm_scale, ckv_scale=scale, lib=lib)
+    ob, lb = oracle.mla_decode(inp.q_nope, inp.q_pe, ckv_bf, inp.kpe, inp.kv_indices, inp.kv_indptr,
+                               inp.kv_last_page_len, inp.sm_scale, lib=lib)
+    assert torch.equal(o8, ob) and torch.equal(l8, lb)
+
+
+def test_int8_quantiser_bounds():
+    """Codes within [-127, 127], the token's largest magnitude on +-127, every value within half a
+    step of scale * code; an all-zero token gets scale 0 and zero codes."""
+    g = torch.Generator().manual_seed(7)
+    x = torch.randn(6, 16, 512, generator=g).to(torch.bfloat16)
+    x[2, 3] = 0
+    codes, scale = quantize_int8_per_token(x)
+    assert codes.dtype == torch.int8 and codes.abs().max() <= 127
+    xf = x.float()
+    err = (xf - codes.float() * scale[..., None]).abs()
+    assert (err <= scale[..., None] * 0.5 + xf.abs() * 2.0 ** -21).all()   # x / scale and the check round in fp32
+    nz = scale > 0
+    assert (codes.abs().amax(dim=-1)[nz] == 127).all()
+    assert scale[2, 3] == 0 and (codes[2, 3] == 0).all()
+
+
+def test_int8_cache_is_close_to_the_bf16_cache(lib=None):
+    """The INT8 cache approximates the bf16 one it was quantised from (FlashMLA PR #233 reports a
+    worst cosine distance of 2.6e-4 for INT8 on synthetic caches)."""
+    inp = make_inputs(WORKLOADS["fp8"], kv_lens=[300, 1000, 77], batch=3, h_q=4, page_size=64, seed=23, int8=True)
+    o8, _ = oracle.decode_inputs(inp)
+    o16, _ = oracle.decode_inputs(inp, use_bf16_cache=True)
+    a, b = o8.flatten(), o16.flatten()
+    cd = 1 - float(a @ b / (a.norm() * b.norm()))
+    assert cd <= 1e-3, cd
+
+
 # ---------------------------------------------------------------- several query tokens per request
 
 def _rows_args(inp, qn, qp):
@@ -384,17 +439,18 @@ def test_non_causal_rows_with_equal_queries_are_equal():
 
 # ---------------------------------------------------------------- the pins catch planted mistakes
 
-@pytest.mark.parametrize("plant", [1, 2, 3])
+@pytest.mark.parametrize("plant", [1, 2, 3, 4])
 def test_planted_mistakes_are_caught(plant, tmp_path):
-    """Copies of the oracle with a dropped kpe term (1), min for max (2), reversed slots (3):
-    each must fail at least one pin above."""
+    """Copies of the oracle with a dropped kpe term (1), min for max (2), reversed slots (3),
+    INT8 codes read unsigned (4): each must fail at least one pin above."""
     lib = oracle.load(oracle.build(str(tmp_path / f"liboracle_plant{plant}.so"), plant=plant))
     pins = [lambda: test_golden_closed_form("two_token_ln3.json", lib=lib),
             lambda: test_golden_closed_form("gather_kpe_sign.json", lib=lib),
             lambda: test_matches_brute_force("tiny", lib=lib),
             lambda: test_zero_scale_gives_mean_and_log_length(lib=lib),
             lambda: test_score_shift_moves_only_lse(lib=lib),
-            lambda: test_dominant_score_selects_one_row(lib=lib)]
+            lambda: test_dominant_score_selects_one_row(lib=lib),
+            lambda: test_int8_oracle_equals_bf16_oracle_on_exact_codes(lib=lib)]
     failed = 0
     for pin in pins:
         try:

@@ -138,8 +138,20 @@ def quantize_e4m3_per_token(ckv_bf16: torch.Tensor):
     return codes, scale
 
 
+def quantize_int8_per_token(ckv_bf16: torch.Tensor):
+    """bf16 [N, P, 512] -> (int8 codes [N, P, 512], fp32 scale [N, P]): symmetric, one scale per
+    token, scale = absmax / 127, code = round-half-even(x / scale) in fp32 (|code| <= 127)."""
+    x = ckv_bf16.float()
+    absmax = x.abs().amax(dim=-1)
+    scale = absmax / 127.0
+    safe = torch.where(scale > 0, scale, torch.ones_like(scale))
+    q = torch.round(x / safe.unsqueeze(-1)).clamp(-127, 127)
+    q = torch.where((scale > 0).unsqueeze(-1), q, torch.zeros_like(q))
+    return q.to(torch.int8), scale
+
+
 def make_inputs(w: Workload, *, kv_lens=None, batch=None, h_q=None, page_size=None,
-                pool_pages=None, seed=None, nan_fill=True, fp8=None) -> Inputs:
+                pool_pages=None, seed=None, nan_fill=True, fp8=None, int8=False) -> Inputs:
     """Draw one seeded batch.  Keyword overrides build smaller variants of a workload."""
     B = batch if batch is not None else w.batch
     H = h_q if h_q is not None else w.h_q
@@ -188,7 +200,15 @@ def make_inputs(w: Workload, *, kv_lens=None, batch=None, h_q=None, page_size=No
 
     ckv_scale = None
     ckv_bf16 = None
-    if fp8:
+    if int8:
+        # INT8 cache: unused slots get the code -128 (never produced) and a NaN scale
+        ckv_bf16 = ckv
+        codes, ckv_scale = quantize_int8_per_token(torch.nan_to_num(ckv, nan=0.0))
+        if valid is not None:
+            codes[~valid] = -128
+            ckv_scale[~valid] = float("nan")
+        ckv = codes
+    elif fp8:
         ckv_bf16 = ckv
         fin = torch.nan_to_num(ckv, nan=0.0)
         codes, ckv_scale = quantize_e4m3_per_token(fin)
