@@ -180,6 +180,21 @@ def subset_bytes(inp, requests):
     return L * per_tok + len(requests) * (H * 576 * 2 + H * 512 * 4 + H * 4 + 8) + 4 * n
 
 
+def cpu_baseline(inp, workload: str, sample_requests: int) -> dict:
+    """The oracle on a bounded sample of the workload: on every host core, and on one core for
+    an eighth of the sample."""
+    cores = cpu_cores()
+    sample = list(range(min(sample_requests, inp.batch)))
+    time_oracle(inp, sample[:1], cores)
+    sec = time_oracle(inp, sample, cores)
+    one = sample[: max(1, len(sample) // 8)]
+    sec1 = time_oracle(inp, one, 1)
+    return {"value": subset_bytes(inp, sample) / sec / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{len(sample)} of {inp.batch} requests of {workload}, one pass, fp64",
+            "single_thread": {"value": subset_bytes(inp, one) / sec1 / 1e9, "unit": "GB/s", "cores": 1,
+                              "sample": f"{len(one)} of {inp.batch} requests of {workload}, one pass, fp64"}}
+
+
 def run_reference(args):
     """The oracle, as it stands, on the host cores: a bounded sample of the workload per step."""
     rank, world, _ = dist_env()
@@ -486,12 +501,7 @@ def main():
     # ---- cpu baseline: the oracle on a bounded sample, host cores, rank 0 at N=1
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cores = cpu_cores()
-        sample = list(range(min(args.sample_requests, inp.batch)))
-        time_oracle(inp, sample[:1], cores)
-        sec = time_oracle(inp, sample, cores)
-        cpu = {"value": subset_bytes(inp, sample) / sec / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
-               "sample": f"{len(sample)} of {inp.batch} requests of {args.workload}, one pass, fp64"}
+        cpu = cpu_baseline(inp, args.workload, args.sample_requests)
 
     if rank == 0:
         line = {

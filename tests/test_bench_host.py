@@ -57,3 +57,12 @@ def test_source_hash_covers_the_attention_sources_only():
     csrc = os.path.join(ROOT, "mla_paged_kv_decode_gb300", "csrc")
     assert "prologue.cu" in os.listdir(csrc)      # present, and left out of the hash
     assert h == bench.kernel_source_hash()        # deterministic
+
+
+def test_cpu_baseline_line():
+    from workloads import WORKLOADS, make_inputs
+    inp = make_inputs(WORKLOADS["tiny"])
+    c = bench.cpu_baseline(inp, "tiny", 4)
+    assert c["kind"] == "oracle" and c["unit"] == "GB/s" and c["cores"] >= 1 and c["value"] > 0
+    assert c["single_thread"]["cores"] == 1 and c["single_thread"]["value"] > 0
+    assert c["sample"].startswith("4 of 4 requests of tiny")
