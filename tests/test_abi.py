@@ -141,3 +141,13 @@ def test_prologue_rejects_bad_arguments_without_touching_a_gpu(lib):
     assert rc(dtype=mla.MLA_KV_BF16, scale=f) == mla.MLA_ERR_INVALID_ARG         # bf16 cache with scales
     assert rc(ckv_new=vp((1 << 20) + 4)) == mla.MLA_ERR_INVALID_ARG               # latent rows need 8-byte alignment
     assert rc(q_in=None) == mla.MLA_ERR_INVALID_ARG
+
+
+def test_header_is_plain_c(tmp_path):
+    """include/mla_decode.h compiles as C99 (no C++ in the ABI) and as C++."""
+    src = tmp_path / "use.c"
+    src.write_text('#include "mla_decode.h"\nint main(void) { mla_plan_t p = 0; (void)p; return (int)MLA_OK; }\n')
+    inc = os.path.join(ROOT, "include")
+    for lang, std in (("c", "-std=c99"), ("c++", "-std=c++17")):
+        r = os.system(f"gcc -x {lang} {std} -Wall -Werror -pedantic -fsyntax-only -I{inc} {src} 2>/dev/null")
+        assert r == 0, f"the header does not compile as {lang}"

@@ -66,3 +66,18 @@ def test_cpu_baseline_line():
     assert c["kind"] == "oracle" and c["unit"] == "GB/s" and c["cores"] >= 1 and c["value"] > 0
     assert c["single_thread"]["cores"] == 1 and c["single_thread"]["value"] > 0
     assert c["sample"].startswith("4 of 4 requests of tiny")
+
+
+def test_reference_arm_line(capsys):
+    """`bench.py --impl reference`: one JSON line with the oracle's own metric, unit, e2e and
+    cpu_baseline keys, no host-device bytes."""
+    import json
+    import types
+    args = types.SimpleNamespace(workload="tiny", sample_requests=4, steps=2, warmup=1, gpus=1)
+    bench.run_reference(args)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
+    assert line["metric"] == bench.METRIC and line["higher_is_better"] is True
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["steps"] == 2 and line["warmup"] == 1 and line["config"]["workload"] == "tiny"
