@@ -196,7 +196,7 @@ int mla_plan_get_segments(mla_plan_t plan, int32_t* segments, int32_t* unit_ptr)
  * limits (an allocator that must not be re-entered, a memory pool fixed at start-up,
  * or a framework that owns every device allocation).  This call takes no workspace;
  * it allocates nothing and calls no cudaMalloc, cudaFree or other allocating routine.
- * The paper has no counterpart to this call: it is an alternative to mla_decode_plan_commit +
+ * The pages describe no counterpart to this call: it is an alternative to mla_decode_plan_commit +
  * mla_decode_run with the same arguments and results (minus workspace_dev).
  *
  * The workspace is a fixed device array inside this library, of
