@@ -493,9 +493,13 @@ def main():
     if args.configs and rank == 0 and world == 1:
         configs = {}
         for name in ("membound", "compute", "b768_kv1024", "b768_kv2048", "ragged", "fp8"):
-            c = per_call_medians(name, stream)
-            c["hbm_frac"] = c["gbs"] / hbm_gbs
-            c["tensor_frac"] = c["tflops"] / bf16_tf
+            try:
+                c = per_call_medians(name, stream)
+                c["hbm_frac"] = c["gbs"] / hbm_gbs
+                c["tensor_frac"] = c["tflops"] / bf16_tf
+            except Exception as e:   # reported in the line; the step's own figures above stand
+                c = {"error": f"{type(e).__name__}: {e}"[:300]}
+                torch.cuda.empty_cache()
             configs[name] = c
 
     # ---- cpu baseline: the oracle on a bounded sample, host cores, rank 0 at N=1
