@@ -50,6 +50,9 @@ def peaks():
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, None, "fallback"
 
 
+NOMINAL_HBM_GBS = 7900.0   # GB300 HBM3e, nominal
+
+
 def kernel_source_hash() -> str:
     """Hash of the sources the attention kernels are built from (the prologue kernel, a
     separate translation unit, is not one of them)."""
@@ -522,6 +525,7 @@ def main():
                          "frac": achieved / hbm_gbs, "traffic": recorded_traffic(args.workload),
                          "kernel": ("mla_decode_narrow_kernel" if inp.h_q <= 32 else "mla_decode_pair_kernel"),
                          "peak_source": peak_src,
+                         "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
                          "kernel_us": attn_avg * 1e6},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
