@@ -212,3 +212,46 @@ def test_query_rows_argument_checks():
     sa, ua = mla.mla_plan_get_segments(a)
     sb, ub = mla.mla_plan_get_segments(b)
     assert np.array_equal(sa, sb) and np.array_equal(ua, ub)
+
+
+def test_query_rows_plan_fuzz():
+    """Random batches, heads, page sizes, cache types and qo_len: every row's causal prefix is
+    covered exactly once, in order, with consecutive partial slots for split rows."""
+    hyp = pytest.importorskip("hypothesis")
+    st = hyp.strategies
+
+    @hyp.settings(max_examples=60, deadline=None)
+    @hyp.given(lens=st.lists(st.integers(0, 3000), min_size=1, max_size=24), qo_len=st.integers(1, 5),
+               causal=st.booleans(), h_q=st.sampled_from([16, 32, 64, 128]), P=st.sampled_from([16, 32, 64]),
+               fp8=st.booleans(), sms=st.sampled_from([1, 7, 152]))
+    def check(lens, qo_len, causal, h_q, P, fp8, sms):
+        indptr, last = _lens_to_arrays(lens, P)
+        kvd = mla.MLA_KV_FP8_E4M3 if fp8 else mla.MLA_KV_BF16
+        plan = mla.mla_decode_plan_ex(torch.from_numpy(indptr), torch.from_numpy(last), len(lens), qo_len, causal,
+                                      h_q, P, sms, kvd)
+        segs, uptr = mla.mla_plan_get_segments(plan)
+        assert uptr[0] == 0 and uptr[-1] == len(segs) and all(np.diff(uptr) >= 0)
+        per_row = {}
+        for r, t0, t1, slot in segs:
+            per_row.setdefault(int(r), []).append((int(t0), int(t1), int(slot)))
+        n_split = 0
+        for b, L in enumerate(lens):
+            for j in range(qo_len):
+                r = b * qo_len + j
+                Lr = max(0, L - (qo_len - 1 - j)) if causal else L
+                pieces = sorted(per_row.pop(r))
+                if Lr == 0:
+                    assert pieces == [(0, 0, -1)]
+                    continue
+                assert pieces[0][0] == 0 and pieces[-1][1] == Lr
+                assert all(a[1] == c[0] for a, c in zip(pieces, pieces[1:]))
+                if len(pieces) > 1:
+                    slots = [p[2] for p in pieces]
+                    assert slots == list(range(slots[0], slots[0] + len(slots)))
+                    n_split += len(pieces)
+                else:
+                    assert pieces[0][2] == -1
+        assert not per_row
+        assert mla.mla_plan_num_partials(plan) == n_split
+
+    check()
