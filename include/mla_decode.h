@@ -171,7 +171,11 @@ int mla_plan_num_launches(mla_plan_t plan);
 
 /* Synchronise cuda_stream and read the workspace's status word: MLA_OK, or
  * MLA_ERR_DEVICE_TIMEOUT when a kernel gave up on a bounded wait (its outputs
- * are then undefined).  The word is cleared after reading. */
+ * are then undefined).  The word is cleared after reading.  workspace_dev NULL
+ * reads the status word of the fixed array mla_decode_run_noalloc uses on the
+ * current device; read it after that call and before the next one, which resets
+ * it.  Returns MLA_OK, MLA_ERR_DEVICE_TIMEOUT, MLA_ERR_INVALID_ARG (NULL plan)
+ * or MLA_ERR_CUDA. */
 mla_status_t mla_decode_device_status(mla_plan_t plan, void* workspace_dev, void* cuda_stream);
 
 /* Introspection (host only, for tests and tools). */
@@ -204,13 +208,16 @@ int mla_plan_get_segments(mla_plan_t plan, int32_t* segments, int32_t* unit_ptr)
  * loads the library until the process exits.  A plan whose
  * mla_decode_plan_workspace_bytes exceeds it is rejected with
  * MLA_ERR_WORKSPACE_TOO_SMALL.  Each call first copies the plan's work list (and
- * zeroed merge counters and status word) into the array on cuda_stream, then
- * launches the decode.  The first call on a device also looks up the array's device
- * address (cudaGetSymbolAddress); make that first call before any stream capture.
+ * zeroed merge counters and status word) into the array on cuda_stream, straight from
+ * the plan's own pageable host memory, then launches the decode.  The first call on a
+ * device also looks up the array's device address (cudaGetSymbolAddress) and keeps it
+ * for the life of the process; make that first call before any stream capture, and
+ * make no call after a cudaDeviceReset, which leaves the kept address stale.
  * All calls share the one array: calls whose work may overlap on the GPU (different
  * streams, or different host threads) race and corrupt each other's partials; order
- * them on one stream.  Returns the codes of mla_decode_run, or
- * MLA_ERR_WORKSPACE_TOO_SMALL. */
+ * them on one stream.  A bounded wait that ran out is reported by
+ * mla_decode_device_status(plan, NULL, stream), read before the next call.
+ * Returns the codes of mla_decode_run, or MLA_ERR_WORKSPACE_TOO_SMALL. */
 mla_status_t mla_decode_run_noalloc(mla_plan_t plan, const void* q_nope, const void* q_pe, const void* ckv_cache,
                                     const float* ckv_scale, const void* kpe_cache, int num_pages,
                                     const int32_t* kv_indices, const int32_t* kv_indptr,

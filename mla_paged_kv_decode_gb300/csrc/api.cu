@@ -282,6 +282,8 @@ mla_status_t check_run_args(mla_plan_t plan, const void* q_nope, const void* q_p
     return MLA_OK;
 }
 
+void* noalloc_scratch_address();   // the fixed array of mla_decode_run_noalloc (end of this file)
+
 }  // namespace
 
 extern "C" {
@@ -358,7 +360,10 @@ void mla_debug_set_trace(mla_plan_t plan, void* dev_buf) {
 int mla_plan_num_launches(mla_plan_t plan) { return (plan && !plan->d.segments.empty()) ? 1 : 0; }
 
 mla_status_t mla_decode_device_status(mla_plan_t plan, void* workspace_dev, void* cuda_stream) {
-    if (!plan || !workspace_dev) return MLA_ERR_INVALID_ARG;
+    if (!plan) return MLA_ERR_INVALID_ARG;
+    // NULL: the status word of the fixed array mla_decode_run_noalloc works in
+    if (!workspace_dev) workspace_dev = noalloc_scratch_address();
+    if (!workspace_dev) return MLA_ERR_CUDA;
     cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
     uint32_t word = 0;
     if (cudaMemcpyAsync(&word, static_cast<uint8_t*>(workspace_dev) + plan->d.layout.off_status, sizeof word,
@@ -436,7 +441,9 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes]
 std::mutex g_noalloc_mutex;
 void* g_noalloc_ptr[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (set up on first use).
+// Device address of the scratch array on the current device (set up on first use).  The address
+// is kept for the life of the process: after a cudaDeviceReset it is stale, and the calls that use
+// it (mla_decode_run_noalloc, mla_decode_device_status with no workspace) must not be made again.
 void* noalloc_scratch_address() {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
