@@ -107,24 +107,37 @@ __device__ __forceinline__ bool wait_phase_flag(uint64_t* bar, uint32_t parity, 
 }
 
 // Optional pipeline timeline (compiled in with -DMLA_TRACE): CTAs 0..3 record the
-// global timer at event `ev` of their tile `idx` into prm.trace[cta][ev][idx].
+// global timer at event `ev` of their tile `idx` into prm.trace[cta][ev][idx].  With
+// -DMLA_TRACE_CLOCK the stamps are the SM's cycle counter instead (finer, but comparable only
+// between stamps taken on one SM).
 #ifdef MLA_TRACE
+#ifdef MLA_TRACE_CLOCK
+#define MLA_TRACE_NOW() static_cast<uint64_t>(clock64())
+#else
+#define MLA_TRACE_NOW() global_timer_ns()
+#endif
 #define MLA_TRACE_EVENT(ev, idx)                                                              \
     do {                                                                                      \
         if (prm.trace && blockIdx.x < 2 && (idx) < 256)                                       \
-            prm.trace[(blockIdx.x * 8 + (ev)) * 256 + (idx)] = global_timer_ns();            \
+            prm.trace[(blockIdx.x * 8 + (ev)) * 256 + (idx)] = MLA_TRACE_NOW();              \
     } while (0)
 // CTA 0 only: a timestamp per unit of work (a ring slot fill, ...) in the area of CTAs 2 and 3,
 // lane `ln` (0..3) of 1024 entries each.
 #define MLA_TRACE_UNIT(ln, idx)                                                               \
     do {                                                                                      \
         if (prm.trace && blockIdx.x == 0 && (idx) < 1024)                                     \
-            prm.trace[2 * 8 * 256 + (ln) * 1024 + (idx)] = global_timer_ns();                 \
+            prm.trace[2 * 8 * 256 + (ln) * 1024 + (idx)] = MLA_TRACE_NOW();                   \
+    } while (0)
+// CTA 1 only: the same per-unit stamps, in 4 lanes of 1024 entries after the milestones.
+#define MLA_TRACE_UNIT1(ln, idx)                                                              \
+    do {                                                                                      \
+        if (prm.trace && blockIdx.x == 1 && (idx) < 1024)                                     \
+            prm.trace[4 * 8 * 256 + gridDim.x * 8 + (ln) * 1024 + (idx)] = MLA_TRACE_NOW();   \
     } while (0)
 // Every CTA also records 8 milestones (entry, producer done, ...) after the per-tile area.
 #define MLA_TRACE_CTA(k)                                                                      \
     do {                                                                                      \
-        if (prm.trace) prm.trace[4 * 8 * 256 + blockIdx.x * 8 + (k)] = global_timer_ns();     \
+        if (prm.trace) prm.trace[4 * 8 * 256 + blockIdx.x * 8 + (k)] = MLA_TRACE_NOW();       \
     } while (0)
 #else
 #define MLA_TRACE_EVENT(ev, idx) \
@@ -135,6 +148,9 @@ __device__ __forceinline__ bool wait_phase_flag(uint64_t* bar, uint32_t parity, 
     } while (0)
 #define MLA_TRACE_UNIT(ln, idx) \
     do {                        \
+    } while (0)
+#define MLA_TRACE_UNIT1(ln, idx) \
+    do {                         \
     } while (0)
 #endif
 

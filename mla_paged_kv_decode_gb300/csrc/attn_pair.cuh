@@ -41,23 +41,32 @@
 namespace mla {
 
 struct PairCfg {
-    static constexpr int kThreads = 256;          // 8 warps: producer, MMA, 2 idle, one warpgroup (4-7)
+    static constexpr int kThreads = 256;          // 8 warps: producers (0, 2, 3), MMA (1), one warpgroup (4-7)
+    // Copy issue: one issuing thread starts about one ring slot per ~0.45 us (measured on this GPU,
+    // whatever the box shape, from HBM or L2), so each CTA spreads its copies over three
+    // producer warps.  Producer p owns the ring slots s with s % (producers) == p, so every slot
+    // has one issuer and each producer can drain its own slots on its own.
+    static constexpr int kKProducers = 3;         // rank 0: warps 0, 2, 3
+    static constexpr int kVProducers = 2;         // rank 1: warps 0, 2
     static constexpr int kTile = kTileTokens;     // 128 tokens
     static constexpr int kChunkBytes = 128 * 128; // 128 rows x 128 B (64 bf16)
     // rank 0
-    static constexpr int kKSlots = 10;
-    static constexpr int kPBufBytes = 2 * kChunkBytes;                 // [2 token chunks][128 heads][128 B]
+    static constexpr int kKSlots = 9;             // one per chunk of a tile: slot = chunk, producer = chunk % 3
+    // A P buffer: the P tile [2 token chunks][128 heads][128 B], then the tile's per-head factors
+    // (PairHand); rank 0 stages one and hands it to rank 1 with a single bulk copy.
+    static constexpr int kPTileBytes = 2 * kChunkBytes;
+    static constexpr int kPBufBytes = kPTileBytes + 2048;              // 1024-aligned stride
     static constexpr int kOffQpe = 0;                                  // [128 heads][128 B] SW128
     static constexpr int kOffK = kOffQpe + kChunkBytes;                // K ring
     static constexpr int kOffPStage = kOffK + kKSlots * kChunkBytes;   // P of one tile, copied to rank 1
-    static constexpr int kSEnd = kOffPStage + kPBufBytes;              // 208 KB
+    static constexpr int kSEnd = kOffPStage + kPBufBytes;              // 194 KB
     // rank 1
-    static constexpr int kPBufs = 3;
+    static constexpr int kPBufs = 2;
     static constexpr int kOffP = 0;
     static constexpr int kVSlotBytes = 4 * 32 * 128;                   // [boxes][4 dim chunks][rows][128 B] = 32 tokens x 256 dims
-    static constexpr int kVSlots = 7;
+    static constexpr int kVSlots = 8;             // a whole tile's values; producer = slot % 2
     static constexpr int kOffV = kOffP + kPBufs * kPBufBytes;
-    static constexpr int kOEnd = kOffV + kVSlots * kVSlotBytes;        // 208 KB
+    static constexpr int kOEnd = kOffV + kVSlots * kVSlotBytes;        // 196 KB
     static constexpr int kOffMisc = kSEnd > kOEnd ? kSEnd : kOEnd;
     static constexpr int kMiscBytes = 12 * 1024;
     static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;
@@ -66,7 +75,26 @@ struct PairCfg {
     static constexpr uint32_t kTmemS = 256;    // rank 0: S buffers at 256, 384
     static constexpr uint32_t kIdescS = idesc_bf16(128, 128, false, false);
     static constexpr uint32_t kIdescPV = idesc_bf16(128, 256, false, true);
+    static_assert(kKSlots % kKProducers == 0 && kVSlots % kVProducers == 0, "each slot has one producer");
 };
+
+// Per-head factors of one tile, handed to rank 1 right after the tile's P in the same buffer.
+struct PairHand {
+    float alpha[128];   // the rescale factor for each head (1 if its running max did not move)
+    float fin_m[128];   // at a segment's last tile: running max (log2 units)
+    float fin_l[128];   // ... and row sum
+    int rescale[4];     // [0]: some head's running max moved
+};
+static_assert(PairCfg::kPTileBytes + sizeof(PairHand) <= PairCfg::kPBufBytes, "P buffer layout");
+constexpr uint32_t kPairHandBytes = PairCfg::kPTileBytes + sizeof(PairHand);   // one bulk copy per tile
+static_assert(kPairHandBytes % 16 == 0, "bulk copy size");
+
+__device__ __forceinline__ PairHand* pair_hand(uint8_t* pbuf) {
+    return reinterpret_cast<PairHand*>(pbuf + PairCfg::kPTileBytes);
+}
+
+// Producer index of a warp of the two-CTA kernel (warps 0, 2, 3), or -1.
+__device__ __forceinline__ int pair_producer(int warp) { return warp == 0 ? 0 : (warp == 2 || warp == 3 ? warp - 1 : -1); }
 
 // Same layout in both CTAs, so mapa_shared of a field's address reaches the partner's copy.
 struct PairMisc {
@@ -87,11 +115,6 @@ struct PairMisc {
     uint32_t tmem_base;
     int abort_flag;
     int merge_flag;
-    // per P buffer, staged in rank 0 and bulk-copied into rank 1 with the P tile:
-    alignas(16) int rescale[PairCfg::kPBufs][4];     // [0]: some head's running max moved
-    alignas(16) float alpha[PairCfg::kPBufs][128];   // the factor for each head (1 if unchanged)
-    alignas(16) float fin_m[PairCfg::kPBufs][128];   // at a segment's last tile: running max (log2 units)
-    alignas(16) float fin_l[PairCfg::kPBufs][128];   // ... and row sum
     float mrg_max[128], mrg_inv[128], mrg_w[8 * 128];
 };
 
@@ -202,8 +225,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
 
     if (rank == 0) {
         // ================================================================== S CTA
-        if (warp == 0) {
-            // ---------------------------------------------------------- TMA producer: q_pe, K chunks
+        if (pair_producer(warp) >= 0) {
+            // ---------------------------------------------------------- TMA producers: q_pe, K chunks
+            // producer pid issues the chunks of slots s % kKProducers == pid (and q_pe if pid == 0)
+            const int pid = pair_producer(warp);
             if (lane == 0) {
                 prefetch_tensormap(&tm_ckv);
                 prefetch_tensormap(&tm_kpe);
@@ -218,11 +243,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
             const int32_t* pages = nullptr;
             while (more && ok) {
                 if (new_seg) {
-                    if (lane == 0 && segc > 0)
+                    if (pid == 0 && lane == 0 && segc > 0)
                         ok = pair_wait(&misc->q_empty, (segc - 1) & 1, misc, partner_abort, prm.status, 41);
                     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                     if (!ok) break;
-                    if (lane == 0) {
+                    if (pid == 0 && lane == 0) {
                         mbar_arrive_expect_tx(&misc->q_full, 128 * 128);
                         // 128 rows from the request's first head: for 64 heads the rows past them
                         // belong to the next request (or lie past the tensor, filled with zeros) and
@@ -243,6 +268,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                 }
                 for (int c = 0; c < 9 && ok; ++c) {   // 8 ckv chunks of 64 dims, then kpe
                     const uint32_t s = kcount % C::kKSlots, use = kcount / C::kKSlots;
+                    if (static_cast<int>(s) % C::kKProducers != pid) {   // another producer's slot
+                        ++kcount;
+                        continue;
+                    }
                     if (lane == 0 && c == 8) MLA_TRACE_EVENT(0, kcount / 9);
                     if (lane == 0 && use > 0)
                         ok = pair_wait(&misc->k_empty[s], (use - 1) & 1, misc, partner_abort, prm.status, 42);
@@ -264,12 +293,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                     if (lane == 0) MLA_TRACE_UNIT(1, kcount);
                     ++kcount;
                 }
-                if (lane == 0) PAIR_PROGRESS(0, kcount);
+                if (pid == 0 && lane == 0) PAIR_PROGRESS(0, kcount);
                 more = cur.advance(new_seg);
             }
-            if (lane == 0) {   // let every copy land before the CTA can exit
+            if (lane == 0) {   // let every copy of this producer's slots land before the CTA can exit
                 const uint64_t t0 = global_timer_ns();
-                for (int s = 0; s < C::kKSlots; ++s) {
+                for (int s = pid; s < C::kKSlots; s += C::kKProducers) {
                     const uint32_t uses = kcount / C::kKSlots + (static_cast<uint32_t>(s) < kcount % C::kKSlots ? 1 : 0);
                     if (uses == 0) continue;
                     while (!mbar_try_wait(&misc->k_full[s], (uses - 1) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {}
@@ -283,8 +312,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                 TileCursorT<C::kTile> cur;
                 bool more = cur.init(prm.segments, seg_begin, seg_end);
                 bool new_seg = true;
-                const uint32_t qpe = smem_u32(smem + C::kOffQpe);
-                const uint32_t kbase = smem_u32(smem + C::kOffK);
+                // descriptors of slot 0 / q_pe at k = 0; a slot or a 16-dim step only moves the start
+                // address (in 16-byte units, no carry out of its field below 256 KB)
+                const uint64_t kdesc0 = umma_desc_sw128_c<16, 1024>(smem_u32(smem + C::kOffK));
+                const uint64_t qdesc0 = umma_desc_sw128_c<16, 1024>(smem_u32(smem + C::kOffQpe));
                 while (more && ok) {
                     const bool last = cur.last();
                     if (new_seg) {
@@ -297,22 +328,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                     MLA_TRACE_EVENT(1, tcount);
                     tc_fence_after();
                     const uint32_t d = tmem + C::kTmemS + buf * 128;
+                    // every tile fills each of the 9 slots once: chunk c is in slot c, its use number
+                    // is the tile count.  A slot is filled by TMA, so waiting on its barrier is enough to
+                    // order the MMAs' reads after the copy (the tcgen05 fence above, once per tile,
+                    // orders them after the softmax's reads of this S buffer).
+                    static_assert(C::kKSlots == 9, "one slot per chunk of a tile");
                     for (int c = 0; c < 9 && ok; ++c) {
-                        const uint32_t s = kcount % C::kKSlots;
-                        ok = pair_wait(&misc->k_full[s], (kcount / C::kKSlots) & 1, misc, partner_abort, prm.status, 45);
+                        ok = pair_wait(&misc->k_full[c], tcount & 1, misc, partner_abort, prm.status, 45);
                         if (!ok) break;
                         MLA_TRACE_UNIT(2, kcount);
-                        tc_fence_after();
-                        const uint32_t kb = kbase + s * C::kChunkBytes;
+                        const uint64_t bd = kdesc0 + static_cast<uint64_t>((c * C::kChunkBytes) >> 4);
+                        if (c < 8) {
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const uint64_t bd = umma_desc_sw128(kb + k * 32, 16, 1024);
-                            if (c < 8)
-                                umma_bf16_ts(d, tmem + C::kTmemQ + c * 32 + k * 8, bd, C::kIdescS, (c | k) != 0);
-                            else
-                                umma_bf16(d, umma_desc_sw128(qpe + k * 32, 16, 1024), bd, C::kIdescS, 1);
+                            for (int k = 0; k < 4; ++k)
+                                umma_bf16_ts(d, tmem + C::kTmemQ + c * 32 + k * 8, bd + 2 * k, C::kIdescS, (c | k) != 0);
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) umma_bf16(d, qdesc0 + 2 * k, bd + 2 * k, C::kIdescS, 1);
                         }
-                        umma_commit(&misc->k_empty[s]);
+                        umma_commit(&misc->k_empty[c]);
                         MLA_TRACE_UNIT(3, kcount);
                         ++kcount;
                     }
@@ -331,14 +365,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
             const uint32_t lane_base = static_cast<uint32_t>(warp - 4) * 32;
             const uint32_t o_p = mapa_shared(smem_u32(smem + C::kOffP), partner);
             const uint32_t o_pfull = mapa_shared(smem_u32(&misc->p_full[0]), partner);
-            const uint32_t o_alpha = mapa_shared(smem_u32(&misc->alpha[0][0]), partner);
-            const uint32_t o_finm = mapa_shared(smem_u32(&misc->fin_m[0][0]), partner);
-            const uint32_t o_finl = mapa_shared(smem_u32(&misc->fin_l[0][0]), partner);
-            const uint32_t o_resc = mapa_shared(smem_u32(&misc->rescale[0][0]), partner);
             uint8_t* pstage = smem + C::kOffPStage;
+            PairHand* stage_hand = pair_hand(pstage);
             const uint32_t pstage_row = smem_u32(pstage) + h * 128;
-            // bytes one tile hands to rank 1: P, then alpha, fin_m, fin_l rows and the rescale word
-            constexpr uint32_t kHandBytes = C::kPBufBytes + 3 * 128 * 4 + 16;
             uint32_t tcount = 0, segc = 0;
             bool ok = true;
             for (int si = seg_begin; si < seg_end && ok; ++si) {
@@ -432,22 +461,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                             st_shared_v4(pstage_row + ck * C::kChunkBytes + ((u ^ (h & 7)) << 4), w[0], w[1], w[2], w[3]);
                         }
                     }
-                    misc->alpha[pb][h] = alpha;
-                    misc->fin_m[pb][h] = m_run;
-                    misc->fin_l[pb][h] = l;
+                    stage_hand->alpha[h] = alpha;
+                    stage_hand->fin_m[h] = m_run;
+                    stage_hand->fin_l[h] = l;
                     fence_proxy_async_smem();   // this thread's staging writes -> the copy engine
                     if (h == 0) MLA_TRACE_EVENT(7, tcount);
                     const bool any = named_barrier_or(2, 128, resc);
                     if (h == 0) {
-                        misc->rescale[pb][0] = any ? 1 : 0;
+                        stage_hand->rescale[0] = any ? 1 : 0;
                         fence_proxy_async_smem();
                         const uint32_t bar = o_pfull + pb * 8;
-                        mbar_arrive_expect_tx_cluster(bar, kHandBytes);
-                        bulk_copy_to_cluster(o_p + pb * C::kPBufBytes, pstage, C::kPBufBytes, bar);
-                        bulk_copy_to_cluster(o_alpha + pb * 512, &misc->alpha[pb][0], 512, bar);
-                        bulk_copy_to_cluster(o_finm + pb * 512, &misc->fin_m[pb][0], 512, bar);
-                        bulk_copy_to_cluster(o_finl + pb * 512, &misc->fin_l[pb][0], 512, bar);
-                        bulk_copy_to_cluster(o_resc + pb * 16, &misc->rescale[pb][0], 16, bar);
+                        // P and the factors in one copy
+                        mbar_arrive_expect_tx_cluster(bar, kPairHandBytes);
+                        bulk_copy_to_cluster(o_p + pb * C::kPBufBytes, pstage, kPairHandBytes, bar);
                         bulk_commit_group();
                         MLA_TRACE_EVENT(4, tcount);
                     }
@@ -460,8 +486,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
         }
     } else {
         // ================================================================== O CTA
-        if (warp == 0) {
-            // ---------------------------------------------------------- TMA producer: V slots
+        if (pair_producer(warp) >= 0 && pair_producer(warp) < C::kVProducers) {
+            // ---------------------------------------------------------- TMA producers: V slots
+            // producer pid issues the slots s % kVProducers == pid
+            const int pid = pair_producer(warp);
             if (lane == 0) prefetch_tensormap(&tm_v);
             const int box_rows = P < 32 ? P : 32;
             uint32_t vcount = 0;
@@ -488,14 +516,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                 for (int half = 0; half < 2 && ok; ++half) {
                     for (int q = 0; q < nq && ok; ++q) {
                         const uint32_t s = vcount % C::kVSlots, use = vcount / C::kVSlots;
+                        if (static_cast<int>(s) % C::kVProducers != pid) {   // another producer's slot
+                            ++vcount;
+                            continue;
+                        }
                         if (lane == 0 && use > 0)
                             ok = pair_wait(&misc->v_empty[s], (use - 1) & 1, misc, partner_abort, prm.status, 51);
                         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                         if (!ok) break;
                         uint8_t* dst = smem + C::kOffV + s * C::kVSlotBytes;
+                        if (lane == 0) MLA_TRACE_UNIT1(3, vcount);
                         if (lane == 0) mbar_arrive_expect_tx(&misc->v_full[s], C::kVSlotBytes);
-                        if (lane == 0 && half == 0 && q == 0) MLA_TRACE_EVENT(0, vcount / (2 * nq));
-                        if (lane == 0 && half == 1 && q == nq - 1) MLA_TRACE_EVENT(1, vcount / (2 * nq));
+                        if (pid == 0 && lane == 0 && half == 0 && q == 0) MLA_TRACE_EVENT(0, vcount / (2 * nq));
+                        if (pid == 0 && lane == 0 && half == 1 && q == nq - 1) MLA_TRACE_EVENT(1, vcount / (2 * nq));
                         for (int bx = 0; bx < 32 / box_rows; ++bx) {
                             const int t = cur.t0 + q * 32 + bx * box_rows;
                             const int pg = __shfl_sync(0xffffffffu, win_page, (t / P - win_base) & 31);
@@ -506,12 +539,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                         ++vcount;
                     }
                 }
-                if (lane == 0) PAIR_PROGRESS(3, vcount);
+                if (pid == 0 && lane == 0) PAIR_PROGRESS(3, vcount);
                 more = cur.advance(new_seg);
             }
-            if (lane == 0) {
+            if (lane == 0) {   // this producer's slots
                 const uint64_t t0 = global_timer_ns();
-                for (int s = 0; s < C::kVSlots; ++s) {
+                for (int s = pid; s < C::kVSlots; s += C::kVProducers) {
                     const uint32_t uses = vcount / C::kVSlots + (static_cast<uint32_t>(s) < vcount % C::kVSlots ? 1 : 0);
                     if (uses == 0) continue;
                     while (!mbar_try_wait(&misc->v_full[s], (uses - 1) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {}
@@ -527,8 +560,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                 TileCursorT<C::kTile> cur;
                 bool more = cur.init(prm.segments, seg_begin, seg_end);
                 bool new_seg = true;
-                const uint32_t pbase = smem_u32(smem + C::kOffP);
-                const uint32_t vbase = smem_u32(smem + C::kOffV);
+                const uint64_t pdesc0 = umma_desc_sw128_c<16, 1024>(smem_u32(smem + C::kOffP));
+                const uint64_t vdesc0 = umma_desc_sw128(smem_u32(smem + C::kOffV), lbo, 1024);
+                // second 16-token step of a 32-token V slot: the next box (page size 16) or row 16
+                const uint32_t voff1 = (box_rows == 16 ? 4 * lbo : 16 * 128) >> 4;
                 while (more && ok) {
                     const bool first = cur.first();
                     const int ntok = cur.ntok();
@@ -537,7 +572,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                     if (ok && new_seg && segc > 0)
                         ok = pair_wait(&misc->epi_done, (segc - 1) & 1, misc, partner_abort, prm.status, 53);
                     if (new_seg) ++segc;
-                    if (ok && !first && *reinterpret_cast<volatile int*>(&misc->rescale[buf][0])) {
+                    if (ok && !first && *reinterpret_cast<volatile int*>(&pair_hand(smem + C::kOffP + buf * C::kPBufBytes)->rescale[0])) {
                         ok = pair_wait(&misc->corr_done, rcount & 1, misc, partner_abort, prm.status, 54);
                         ++rcount;
                     }
@@ -545,6 +580,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                     MLA_TRACE_EVENT(5, tcount);
                     fence_proxy_async_smem();
                     tc_fence_after();
+                    const uint64_t pdesc = pdesc0 + static_cast<uint64_t>((buf * C::kPBufBytes) >> 4);
                     const int nq = (ntok + 31) / 32;
                     const bool partial = (ntok & 15) != 0;
                     for (int half = 0; half < 2 && ok; ++half) {
@@ -552,24 +588,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                             const uint32_t s = vcount % C::kVSlots;
                             ok = pair_wait(&misc->v_full[s], (vcount / C::kVSlots) & 1, misc, partner_abort, prm.status, 56);
                             if (!ok) break;
+                            MLA_TRACE_UNIT1(0, vcount);
                             if (partial && q == nq - 1) {
                                 // the slot with the tile's last token: its rows past it are zeroed first
                                 mbar_arrive(&misc->vz_go[half]);
                                 ok = pair_wait(&misc->vz_done[half], zcount & 1, misc, partner_abort, prm.status, 55);
                                 if (!ok) break;
                                 fence_proxy_async_smem();
+                                tc_fence_after();
                             }
-                            tc_fence_after();
+                            // a TMA-filled slot: its barrier wait orders the MMAs' reads after the copy
+                            const uint64_t bslot = vdesc0 + static_cast<uint64_t>((s * C::kVSlotBytes) >> 4);
                             for (int k2 = 0; k2 < 2; ++k2) {
                                 const int kk = 2 * q + k2;   // 16-token step within the tile
                                 if (16 * kk >= ntok) break;
-                                const uint32_t a = pbase + buf * C::kPBufBytes + (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-                                const int r0 = 16 * k2;
-                                const uint32_t b = vbase + s * C::kVSlotBytes + (r0 / box_rows) * 4 * lbo + (r0 % box_rows) * 128;
-                                umma_bf16(tmem + 256 * half, umma_desc_sw128(a, 16, 1024), umma_desc_sw128(b, lbo, 1024),
-                                          C::kIdescPV, (first && kk == 0) ? 0u : 1u);
+                                const uint64_t ad = pdesc + static_cast<uint64_t>(((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4);
+                                umma_bf16(tmem + 256 * half, ad, bslot + (k2 ? voff1 : 0u), C::kIdescPV,
+                                          (first && kk == 0) ? 0u : 1u);
                             }
                             umma_commit(&misc->v_empty[s]);
+                            MLA_TRACE_UNIT1(1, vcount);
                             ++vcount;
                         }
                         if (half == 0) MLA_TRACE_EVENT(2, tcount);
@@ -613,10 +651,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                     if (!ok) break;
                     if (h == 0) MLA_TRACE_EVENT(3, tcount);
                     // everything rank 0 left with this P buffer is read before the buffer goes back
-                    const bool resc = !first && *reinterpret_cast<volatile int*>(&misc->rescale[buf][0]);
-                    const float alpha = misc->alpha[buf][h];
-                    const float fin_m = last ? misc->fin_m[buf][h] : 0.f;
-                    const float fin_l = last ? misc->fin_l[buf][h] : 1.f;
+                    const PairHand* hd = pair_hand(smem + C::kOffP + buf * C::kPBufBytes);
+                    const bool resc = !first && *reinterpret_cast<const volatile int*>(&hd->rescale[0]);
+                    const float alpha = hd->alpha[h];
+                    const float fin_m = last ? hd->fin_m[h] : 0.f;
+                    const float fin_l = last ? hd->fin_l[h] : 1.f;
                     // value rows [ntok, next multiple of 16) of the partial 32-token quarter of one half:
                     // stale or NaN page tails the step's MMA would otherwise read.  The MMA thread
                     // raises vz_go[half] once that slot has landed (it is the ring's consumer; these
