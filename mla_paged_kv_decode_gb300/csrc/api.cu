@@ -240,6 +240,7 @@ mla_status_t run_checked(mla_plan_t plan, const void* q_nope, const void* q_pe, 
     prm.part_lse = reinterpret_cast<float*>(ws + L.off_part_lse);
     prm.ckv_scale = ckv_scale;
     prm.counters = reinterpret_cast<int32_t*>(ws + L.off_counters);
+    prm.ready = prm.counters + static_cast<size_t>(d.num_split) * (d.h_q / 16);
     prm.status = reinterpret_cast<uint32_t*>(ws + L.off_status);
     prm.trace = trace;
     prm.scale_log2 = sm_scale * 1.4426950408889634f;

@@ -41,6 +41,7 @@ struct AttnParams {
     float* part_lse;              // [num_partials, h_q]
     const float* ckv_scale;       // e4m3 cache: fp32 scale per token [num_pages * page_size], else null
     int32_t* counters;            // arrivals per (split request, 16- or 32-head block)
+    int32_t* ready;               // narrow kernel: pieces of each counter whose partial is written
     uint32_t* status;
     uint64_t* trace;              // per-tile event timestamps when built with MLA_TRACE, else unused
     float scale_log2;             // sm_scale * log2(e)

@@ -57,6 +57,10 @@ struct NarrowCfg {
     // groups.  Launched at 168 registers a thread (65536 / 384); warpgroup 0 gives registers
     // back and the compute warpgroups take them (128 x 80 + 256 x 208 <= 384 x 168).
     static constexpr int kProducerWarps = 4;
+    // Warps 0 and 1 issue the copies: one issuing thread starts about one ring stage per ~0.45 us
+    // (measured on this GPU), so two of them keep more of the ring in flight.  Producer p owns
+    // the stages s with s % kIssuers == p, so every stage has one issuer.
+    static constexpr int kIssuers = 2;
     static constexpr int kThreads = 32 * (kProducerWarps + kComputeWarps);
     static constexpr uint32_t kProducerRegs = 80;
     static constexpr uint32_t kComputeRegs = 208;
@@ -178,8 +182,9 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
     if (warp < C::kProducerWarps) regs_dec<C::kProducerRegs>();
     else regs_inc<C::kComputeRegs>();
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
+    if (warp < C::kIssuers) {
+        // ------------------------------------------------------------ TMA producers
+        const int pid = warp;
         uint32_t scount = 0, tile_idx = 0;
         bool ok = true;
         TileCursorT<kNarrowTile> cur;
@@ -206,6 +211,10 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                     win_page = (win_base + lane <= seg_last_page) ? pages[win_base + lane] : 0;
                 }
                 const uint32_t s = scount % C::kStages, use = scount / C::kStages;
+                if (static_cast<int>(s) % C::kIssuers != pid) {   // the other producer's stage
+                    ++scount;
+                    continue;
+                }
                 uint64_t* bar_full = &misc->full[s];
                 if (lane == 0 && use > 0) ok = wait_phase_flag(&misc->empty[s], (use - 1) & 1, &misc->abort_flag, prm.status, 21);
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -214,7 +223,7 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                 // bytes per token: bf16 ckv + kpe = 1152
                 if (lane == 0)
                     mbar_arrive_expect_tx(bar_full, static_cast<uint32_t>(nbox * box_rows * (C::kStageLoadBytes / kNarrowStageTok)));
-                if (lane == 0) MLA_TRACE_EVENT(st == 0 ? 0 : 1, tile_idx);
+                if (lane == 0 && pid == 0) MLA_TRACE_EVENT(st == 0 ? 0 : 1, tile_idx);
                 for (int bx = 0; bx < nbox; ++bx) {
                     const int t = t_st + bx * box_rows;
                     const int pg = __shfl_sync(0xffffffffu, win_page, (t / P - win_base) & 31);
@@ -237,10 +246,10 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
             ++tile_idx;
             more = cur.advance(new_seg);
         }
-        if (lane == 0) {
-            MLA_TRACE_CTA(1);
+        if (lane == 0) {   // this producer's stages: every copy lands before the CTA can exit
+            if (pid == 0) MLA_TRACE_CTA(1);
             const uint64_t t0 = global_timer_ns();
-            for (int s = 0; s < C::kStages; ++s) {
+            for (int s = pid; s < C::kStages; s += C::kIssuers) {
                 const uint32_t uses = scount / C::kStages + (static_cast<uint32_t>(s) < scount % C::kStages ? 1 : 0);
                 if (uses == 0) continue;
                 while (!mbar_try_wait(&misc->full[s], (uses - 1) & 1) && global_timer_ns() - t0 < kWaitLimitNs) {}
@@ -464,6 +473,12 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
             }
             if (!ok) break;
             if (kr == 0 && lane == 0) MLA_TRACE_CTA(2 + grp);
+            // A split piece takes its arrival ticket now; the atomic's round trip overlaps the
+            // row sums and the token-group merge below, and only the ticket's use waits for it.
+            const int gt = kr * 32 + lane;   // 0..127 within the group
+            const int ctr = (sg.item * prm.head_groups + group_cta) * C::kHeadGroups + hgi;
+            int ticket = 0;
+            if (sg.slot >= 0 && tg == 0 && gt == 0) ticket = atomicAdd(&prm.counters[ctr], 1);
             // ---- row sums: quad, then the 4 warps of the group (each summed its own 8 tokens per tile)
             float l[2];
 #pragma unroll
@@ -561,30 +576,53 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                 }
             }
             if (sg.slot >= 0) {
-                // ---- split request: the last piece to arrive merges all of them in slot order
-                // (group 0 alone, or both token groups at the unit's last segment)
+                // ---- split request: the piece with the last ticket merges all of them in slot order
+                // (group 0 alone, or both token groups at the unit's last segment).  The others
+                // publish their partial (stores, fence, then the ready count); the last one waits
+                // until every other partial is published -- their CTAs hold tickets, so they are
+                // running and wait on nothing -- and reads its own partial back after the group
+                // barrier (same CTA), with no fence or second round trip on its path.
                 const uint32_t mbar = wide ? merge_bar : named_bar;
                 const uint32_t nthr = wide ? 256u : 128u;
-                if (tg == 0) __threadfence();
+                if (tg == 0 && gt == 0) misc->merge_flag[hgi] = (ticket == sg.n_slots - 1) ? 1 : 0;
                 named_barrier_sync(mbar, nthr);
-                const int gt = kr * 32 + lane;   // 0..127 within the group
-                const int ctr = (sg.item * prm.head_groups + group_cta) * C::kHeadGroups + hgi;
-                if (tg == 0 && gt == 0) {
-                    const int old = atomicAdd(&prm.counters[ctr], 1);
-                    misc->merge_flag[hgi] = (old == sg.n_slots - 1);
-                }
-                named_barrier_sync(mbar, nthr);
-                if (misc->merge_flag[hgi]) {
-                    if (tg == 0 && gt == 0) MLA_TRACE_CTA(4);
-                    __threadfence();
-                    if (wide)
-                        merge_split_pieces_wide16(prm, sg.b, sg.slot_begin, sg.n_slots, head0, tg * 128 + gt, merge_bar,
-                                                  named_bar, misc->mrg_max[hgi], misc->mrg_inv[hgi], misc->mrg_w[hgi]);
-                    else
-                        merge_split_pieces<16, 128>(prm, sg.b, sg.slot_begin, sg.n_slots, head0, gt, named_bar,
-                                                    misc->mrg_max[hgi], misc->mrg_inv[hgi], misc->mrg_w[hgi]);
-                    if (tg == 0 && gt == 0) prm.counters[ctr] = 0;
-                    if (tg == 0 && gt == 0) MLA_TRACE_CTA(5);
+                if (!misc->merge_flag[hgi]) {
+                    if (tg == 0) __threadfence();
+                    named_barrier_sync(mbar, nthr);
+                    if (tg == 0 && gt == 0) atomicAdd(&prm.ready[ctr], 1);
+                } else {
+                    if (tg == 0 && gt == 0) {
+                        // an acquiring read of the count: the other pieces' partials are visible to this
+                        // thread, and to the whole group after the barrier below
+                        MLA_TRACE_CTA(4);
+                        bool done = ld_acquire_gpu(prm.ready + ctr) >= sg.n_slots - 1;
+                        const uint64_t t0 = global_timer_ns();
+                        while (!done && !*reinterpret_cast<volatile int*>(&misc->abort_flag)) {
+                            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                                misc->abort_flag = 1;
+                                atomicCAS(prm.status, 0u, kStatusTimeout | 24u);
+                                break;
+                            }
+                            done = ld_acquire_gpu(prm.ready + ctr) >= sg.n_slots - 1;
+                        }
+                        misc->merge_flag[hgi] = done ? 1 : 2;
+                        MLA_TRACE_CTA(3);   // (debug builds) the other pieces are published
+                    }
+                    named_barrier_sync(mbar, nthr);
+                    if (misc->merge_flag[hgi] == 1) {
+                        if (wide)
+                            merge_split_pieces_wide16(prm, sg.b, sg.slot_begin, sg.n_slots, head0, tg * 128 + gt,
+                                                      merge_bar, named_bar, misc->mrg_max[hgi], misc->mrg_inv[hgi],
+                                                      misc->mrg_w[hgi]);
+                        else
+                            merge_split_pieces<16, 128>(prm, sg.b, sg.slot_begin, sg.n_slots, head0, gt, named_bar,
+                                                        misc->mrg_max[hgi], misc->mrg_inv[hgi], misc->mrg_w[hgi]);
+                    }
+                    if (tg == 0 && gt == 0) {
+                        prm.counters[ctr] = 0;
+                        prm.ready[ctr] = 0;
+                        MLA_TRACE_CTA(5);
+                    }
                 }
                 named_barrier_sync(mbar, nthr);
             }

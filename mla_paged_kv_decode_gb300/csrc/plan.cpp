@@ -181,7 +181,7 @@ int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int ba
     L.off_unit_ptr = 256;
     L.off_segments = align_up(L.off_unit_ptr + sizeof(int32_t) * p.unit_ptr.size(), 16);
     L.off_counters = align_up(L.off_segments + sizeof(Segment) * p.segments.size(), 16);
-    L.header_bytes = align_up(L.off_counters + sizeof(int32_t) * size_t(p.num_split) * (h_q / 16), 256);
+    L.header_bytes = align_up(L.off_counters + 2 * sizeof(int32_t) * size_t(p.num_split) * (h_q / 16), 256);
     L.off_part_lse = L.header_bytes;
     L.off_part_o = align_up(L.off_part_lse + sizeof(float) * size_t(p.num_partials) * h_q, 256);
     L.total_bytes = align_up(L.off_part_o + sizeof(float) * size_t(p.num_partials) * h_q * kDimCkv, 256);

@@ -13,7 +13,10 @@ constexpr int kNarrowTileTokens = 32;  // tokens per tile of the narrow-head (wa
 // Partition cost of a request start (after the first), in tiles: what a CTA that crosses
 // into another request pays for the second segment's prologue and epilogue, measured on
 // GB300 against the time of one tile.
-constexpr int kNarrowSegmentCost = 8;
+#ifndef MLA_NARROW_SEGMENT_COST
+#define MLA_NARROW_SEGMENT_COST 8
+#endif
+constexpr int kNarrowSegmentCost = MLA_NARROW_SEGMENT_COST;
 constexpr int kSegmentCost = 1;
 constexpr int kDimCkv = 512;
 constexpr int kDimKpe = 64;
@@ -34,7 +37,8 @@ struct PlanLayout {
     size_t off_status = 0;      // uint32 status word
     size_t off_unit_ptr = 0;    // int32 [num_units + 1]
     size_t off_segments = 0;    // Segment [num_segments]
-    size_t off_counters = 0;    // int32 [num_split_requests * h_q / 16], zero between runs
+    size_t off_counters = 0;    // int32 [2][num_split_requests * h_q / 16]: arrival tickets, then
+                                //   pieces whose partial is written (narrow kernel); zero between runs
     size_t header_bytes = 0;    // bytes copied by commit
     size_t off_part_lse = 0;    // fp32 [num_partials, h_q]
     size_t off_part_o = 0;      // fp32 [num_partials, h_q, 512]

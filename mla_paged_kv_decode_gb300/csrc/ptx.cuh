@@ -69,6 +69,14 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// Load with acquire semantics at GPU scope: later reads of this thread (and, after a CTA barrier,
+// of the CTA) observe what the writer released before the value it reads.
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
