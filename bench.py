@@ -227,6 +227,14 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def kv_dtype_of(inp):
+    """The cache type of a workloads.Inputs: bf16, e4m3 codes (uint8) or INT8 codes (int8)."""
+    import mla_paged_kv_decode_gb300 as mla
+    if inp.ckv_scale is None:
+        return mla.MLA_KV_BF16
+    return mla.MLA_KV_INT8 if inp.ckv.dtype == torch.int8 else mla.MLA_KV_FP8_E4M3
+
+
 def time_workload(inp, n, stream):
     """Seconds per decode step (one event pair around n steps after 5 warm-up steps)."""
     dec, step, keep = bench_device(inp, 0, 5, stream)
@@ -245,7 +253,7 @@ def plan_balance(plan, h_q: int, kv_dtype: int) -> dict:
     """Max / mean unit cost of a plan: a unit's cost is its tiles plus the plan's start cost per
     request it starts (the measure the planner equalises)."""
     import mla_paged_kv_decode_gb300 as mla
-    tile = 32 if (h_q <= 32 and kv_dtype == mla.MLA_KV_BF16) else 128
+    tile = 128 if (h_q >= 64 and kv_dtype != mla.MLA_KV_INT8) else 32   # tcgen05 kernels: 128-token tiles
     segs, uptr = mla.mla_plan_get_segments(plan)
     c = mla.mla_plan_segment_cost_tiles(plan)
     cost, tiles = [], []
@@ -260,11 +268,12 @@ def plan_balance(plan, h_q: int, kv_dtype: int) -> dict:
             "partials": mla.mla_plan_num_partials(plan)}
 
 
-def per_call_medians(name: str, stream, n: int = 100) -> dict:
+def per_call_medians(name: str, stream, n: int = 100, **overrides) -> dict:
     """One workload: the median of n single decodes timed one by one (an event pair around each
-    call on the launching stream), launched eagerly and as replays of a captured CUDA graph."""
+    call on the launching stream), launched eagerly and as replays of a captured CUDA graph.
+    ``overrides`` go to ``make_inputs`` (e.g. the INT8 cache for the 8-bit shape)."""
     import mla_paged_kv_decode_gb300 as mla
-    inp = make_inputs(WORKLOADS[name])
+    inp = make_inputs(WORKLOADS[name], **overrides)
     b, f = algorithmic_bytes(inp), algorithmic_flops(inp)
     dec, step, keep = bench_device(inp, 0, 5, stream)
     out, lse, d = keep
@@ -289,8 +298,11 @@ def per_call_medians(name: str, stream, n: int = 100) -> dict:
             g.replay()
     graph = timed(lambda: g.replay())
     st = dec.device_status(stream)
-    kvd = mla.MLA_KV_FP8_E4M3 if inp.ckv_scale is not None else mla.MLA_KV_BF16
-    res = {"desc": WORKLOADS[name].description, "us_eager_median": eager, "us_graph_median": graph,
+    kvd = kv_dtype_of(inp)
+    desc = WORKLOADS[name].description
+    if overrides.get("int8"):
+        desc = desc.replace("e4m3 ckv", "INT8 ckv")
+    res = {"desc": desc, "us_eager_median": eager, "us_graph_median": graph,
            "gbs": b / graph / 1e3, "tflops": f / graph / 1e6, "alg_bytes": b, "alg_flops": f,
            "tokens": int(inp.kv_lens.sum()), "calls": n, "status": st,
            "plan": plan_balance(dec.plan, inp.h_q, kvd)}
@@ -303,7 +315,7 @@ def bench_device(inp, steps, warmup, stream):
     """Device-timed steps with resident inputs.  Returns per-step and per-kernel times (s)."""
     import mla_paged_kv_decode_gb300 as mla
     d = inp.to("cuda")
-    kvd = mla.MLA_KV_FP8_E4M3 if inp.ckv_scale is not None else mla.MLA_KV_BF16
+    kvd = kv_dtype_of(inp)
     dec = mla.Decoder(inp.kv_indptr, inp.kv_last_page_len, inp.h_q, inp.page_size, kv_dtype=kvd, stream=stream)
     out = torch.empty(inp.batch, inp.h_q, 512, dtype=torch.float32, device="cuda")
     lse = torch.empty(inp.batch, inp.h_q, dtype=torch.float32, device="cuda")
@@ -485,25 +497,35 @@ def main():
         b16 = algorithmic_bytes(inp16)
         del inp16
         torch.cuda.empty_cache()
+        inpi = make_inputs(WORKLOADS["fp8"], fp8=False, int8=True)
+        ti = time_workload(inpi, n8, stream)
+        bi = algorithmic_bytes(inpi)
+        del inpi
+        torch.cuda.empty_cache()
         fp8 = {"workload": "fp8", "desc": WORKLOADS["fp8"].description, "us_per_step": t8 * 1e6,
                "gbs": b8 / t8 / 1e9, "hbm_frac": b8 / t8 / 1e9 / hbm_gbs, "tokens_per_s": tok / t8,
                "bf16_us_per_step": t16 * 1e6, "bf16_gbs": b16 / t16 / 1e9,
-               "speedup_vs_bf16": t16 / t8, "bytes_per_token": {"fp8": 644, "bf16": 1152},
-               "traffic": recorded_traffic("fp8")}
+               "speedup_vs_bf16": t16 / t8, "bytes_per_token": {"fp8": 644, "int8": 644, "bf16": 1152},
+               "traffic": recorded_traffic("fp8"),
+               "int8": {"us_per_step": ti * 1e6, "gbs": bi / ti / 1e9, "hbm_frac": bi / ti / 1e9 / hbm_gbs,
+                        "speedup_vs_bf16": t16 / ti}}
 
     # ---- every workload of the measurement table, one decode at a time: eager and graph replay
     configs = None
     if args.configs and rank == 0 and world == 1:
         configs = {}
-        for name in ("membound", "compute", "b768_kv1024", "b768_kv2048", "ragged", "fp8"):
+        for key, name, kw in (("membound", "membound", {}), ("compute", "compute", {}),
+                              ("b768_kv1024", "b768_kv1024", {}), ("b768_kv2048", "b768_kv2048", {}),
+                              ("ragged", "ragged", {}), ("fp8", "fp8", {}),
+                              ("int8", "fp8", {"fp8": False, "int8": True})):
             try:
-                c = per_call_medians(name, stream)
+                c = per_call_medians(name, stream, **kw)
                 c["hbm_frac"] = c["gbs"] / hbm_gbs
                 c["tensor_frac"] = c["tflops"] / bf16_tf
             except Exception as e:   # reported in the line; the step's own figures above stand
                 c = {"error": f"{type(e).__name__}: {e}"[:300]}
                 torch.cuda.empty_cache()
-            configs[name] = c
+            configs[key] = c
 
     # ---- cpu baseline: the oracle on a bounded sample, host cores, rank 0 at N=1
     cpu = None

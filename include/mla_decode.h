@@ -58,8 +58,10 @@ typedef enum {
 } mla_status_t;
 
 typedef enum {
-    MLA_KV_BF16 = 0,     /* ckv bf16 [num_pages, page_size, 512] */
-    MLA_KV_FP8_E4M3 = 1  /* ckv uint8 e4m3 codes [num_pages, page_size, 512] + fp32 scale [num_pages, page_size] */
+    MLA_KV_BF16 = 0,      /* ckv bf16 [num_pages, page_size, 512] */
+    MLA_KV_FP8_E4M3 = 1,  /* ckv uint8 e4m3 codes [num_pages, page_size, 512] + fp32 scale [num_pages, page_size] */
+    MLA_KV_INT8 = 2       /* ckv int8 codes (two's complement) [num_pages, page_size, 512] + fp32 scale
+                             [num_pages, page_size]; token t's latent is scale[t] * code[t, :] */
 } mla_kv_dtype_t;
 
 typedef enum {

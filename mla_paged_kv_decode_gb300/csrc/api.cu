@@ -16,6 +16,7 @@
 #include "attn.cuh"
 #include "attn_e4m3.cuh"
 #include "attn_narrow.cuh"
+#include "attn_narrow8.cuh"
 #include "attn_pair.cuh"
 #include "plan.h"
 
@@ -166,6 +167,18 @@ cudaError_t launch_narrow(const mla_plan_s* p, const CUtensorMap& ckv, const CUt
                       static_cast<const uint16_t*>(q_nope), static_cast<const uint16_t*>(q_pe));
 }
 
+template <int HG>
+cudaError_t launch_narrow8(const mla_plan_s* p, const MapCache& mc, const mla::AttnParams& prm, const void* q_nope,
+                           const void* q_pe, cudaStream_t stream) {
+    using C = mla::Narrow8Cfg<HG>;
+    cudaError_t e = cudaFuncSetAttribute(mla::mla_decode_narrow8_kernel<HG>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int grid = p->d.num_units * p->d.head_groups;
+    return launch_pdl(mla::mla_decode_narrow8_kernel<HG>, grid, C::kThreads, C::kSmemBytes, stream, mc.m_ckv, mc.m_kpe,
+                      mc.m_scale, prm, static_cast<const uint16_t*>(q_nope), static_cast<const uint16_t*>(q_pe));
+}
+
 cudaError_t launch_e4m3(const mla_plan_s* p, const MapCache& mc, const mla::AttnParams& prm, const void* q_nope,
                         const void* q_pe, cudaStream_t stream) {
     using C = mla::E4m3Cfg;
@@ -196,7 +209,7 @@ mla_status_t run_checked(mla_plan_t plan, const void* q_nope, const void* q_pe, 
                          const int32_t* kv_indptr, float sm_scale, void* out, float* lse, uint8_t* ws,
                          cudaStream_t stream, uint64_t* trace) {
     const auto& d = plan->d;
-    const bool f8 = d.kv_dtype == MLA_KV_FP8_E4M3;
+    const bool f8 = d.kv_dtype != MLA_KV_BF16;   // 8-bit codes
     const auto& L = d.layout;
     // tensor maps depend only on the buffer addresses: re-encode when they change
     MapCache& mc = plan->maps;
@@ -206,7 +219,7 @@ mla_status_t run_checked(mla_plan_t plan, const void* q_nope, const void* q_pe, 
         const uint64_t qrows = static_cast<uint64_t>(d.rows) * d.h_q;
         const uint32_t hg = static_cast<uint32_t>(d.heads_per_cta);
         // box rows: a whole page for the tcgen05 kernel, a 32-token ring stage at most for the narrow one
-        const uint32_t box = d.narrow ? std::min(d.page_size, mla::kNarrowStageTok) : d.page_size;
+        const uint32_t box = (d.narrow || d.narrow8) ? std::min(d.page_size, mla::kNarrowStageTok) : d.page_size;
         // the narrow kernel takes a whole 32-token stage of ckv in one 3-D box when a page holds it
         const bool chunked = d.narrow && box == static_cast<uint32_t>(mla::kNarrowStageTok);
         bool ok_ckv;
@@ -218,7 +231,7 @@ mla_status_t run_checked(mla_plan_t plan, const void* q_nope, const void* q_pe, 
         mc.valid = ok_ckv && make_map_bf16(&mc.m_kpe, kpe_cache, mla::kDimKpe, rows, box) &&
                    make_map_bf16(&mc.m_qp, q_pe, mla::kDimKpe, qrows, d.pair ? 128 : hg) &&
                    (!d.pair || make_map_v_half(&mc.m_v, ckv_cache, rows, std::min(d.page_size, 32))) &&
-                   (!d.e4m3 || make_map_scale(&mc.m_scale, ckv_scale, rows, static_cast<uint32_t>(d.page_size)));
+                   (!f8 || make_map_scale(&mc.m_scale, ckv_scale, rows, box));
         if (!mc.valid) return MLA_ERR_CUDA;
         mc.ckv = ckv_cache;
         mc.kpe = kpe_cache;
@@ -250,7 +263,10 @@ mla_status_t run_checked(mla_plan_t plan, const void* q_nope, const void* q_pe, 
     prm.num_pages = num_pages;
     prm.out_bf16 = d.out_dtype == MLA_OUT_BF16 ? 1 : 0;
     cudaError_t e;
-    if (d.e4m3) {
+    if (d.narrow8) {
+        e = d.heads_per_cta == 16 ? launch_narrow8<16>(plan, mc, prm, q_nope, q_pe, stream)
+                                  : launch_narrow8<32>(plan, mc, prm, q_nope, q_pe, stream);
+    } else if (d.e4m3) {
         e = launch_e4m3(plan, mc, prm, q_nope, q_pe, stream);
     } else if (d.narrow) {
         e = d.h_q == 16 ? launch_narrow<16>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream)
@@ -279,7 +295,7 @@ mla_status_t check_run_args(mla_plan_t plan, const void* q_nope, const void* q_p
     if (!std::isfinite(sm_scale)) return MLA_ERR_INVALID_ARG;
     if (static_cast<int64_t>(num_pages) * d.page_size >= (int64_t(1) << 31)) return MLA_ERR_INVALID_ARG;
     if (d.kv_dtype == MLA_KV_BF16 && ckv_scale != nullptr) return MLA_ERR_INVALID_ARG;
-    if (d.kv_dtype == MLA_KV_FP8_E4M3 && (ckv_scale == nullptr || !aligned16(ckv_scale))) return MLA_ERR_INVALID_ARG;
+    if (d.kv_dtype != MLA_KV_BF16 && (ckv_scale == nullptr || !aligned16(ckv_scale))) return MLA_ERR_INVALID_ARG;
     return MLA_OK;
 }
 

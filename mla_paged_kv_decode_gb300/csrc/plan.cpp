@@ -29,9 +29,13 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 }  // namespace
 
 int heads_per_cta_for(int h_q, int kv_dtype) {
-    // e4m3 cache: 16 heads per CTA; 32, 64 and 128 heads take 2, 4 or 8 CTAs per unit, each
-    // streaming the unit's pages (the repeats mostly from L2)
-    if (kv_dtype == 1) return (h_q == 16 || h_q == 32 || h_q == 64 || h_q == 128) ? 16 : 0;
+    const bool ok = h_q == 16 || h_q == 32 || h_q == 64 || h_q == 128;
+    // e4m3 cache: the tcgen05 e4m3 kernel, 16 heads per CTA (h_q / 16 CTAs per unit, each streaming
+    // the unit's pages, the repeats mostly from L2).  (The 8-bit warp-MMA kernel also serves e4m3
+    // codes; at 16 heads it measured 273 us against this kernel's 175 us on 64 x 16384 tokens.)
+    if (kv_dtype == 1) return ok ? 16 : 0;
+    // INT8 cache: the 8-bit narrow kernel, 32 heads per CTA above 32 heads
+    if (kv_dtype == 2) return ok ? (h_q <= 32 ? h_q : 32) : 0;
     switch (h_q) {
         case 16:
         case 32:
@@ -44,7 +48,7 @@ int heads_per_cta_for(int h_q, int kv_dtype) {
 int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int batch, int qo_len, bool causal,
                int h_q, int page_size, int num_sms, int kv_dtype, int out_dtype, PlanData* out) {
     if (!kv_indptr || !kv_last_page_len || !out || batch < 1 || num_sms < 1) return 1;
-    if (kv_dtype != 0 && kv_dtype != 1) return 1;
+    if (kv_dtype != 0 && kv_dtype != 1 && kv_dtype != 2) return 1;
     if (out_dtype != 0 && out_dtype != 1) return 1;
     if (qo_len < 1 || qo_len > kMaxQoLen) return 1;
     if (static_cast<int64_t>(batch) * qo_len * 128 >= (int64_t(1) << 31)) return 1;
@@ -53,9 +57,11 @@ int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int ba
     if (hg == 0) return 2;
     if (kv_indptr[0] != 0) return 1;
 
-    const bool e4m3 = kv_dtype == 1;
-    const bool narrow = h_q <= 32 && !e4m3;
-    const int tile_tok = narrow ? kNarrowTileTokens : kTileTokens;
+    const bool eight = kv_dtype == 1 || kv_dtype == 2;
+    const bool narrow = h_q <= 32 && !eight;
+    const bool narrow8 = kv_dtype == 2;
+    const bool e4m3 = kv_dtype == 1 && !narrow8;
+    const int tile_tok = (narrow || narrow8) ? kNarrowTileTokens : kTileTokens;
     const int rows = batch * qo_len;
     std::vector<int64_t> len(rows), tiles(rows);
     int64_t total_tiles = 0;
@@ -91,13 +97,14 @@ int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int ba
     p.head_groups = h_q / hg;
     p.tile_tokens = tile_tok;
     p.narrow = narrow;
-    p.pair = h_q >= 64 && !e4m3;
+    p.pair = h_q >= 64 && !eight;
     p.e4m3 = e4m3;
+    p.narrow8 = narrow8;
     const int ctas_per_unit = p.head_groups * (p.pair ? 2 : 1);
     int64_t units = std::max(1, num_sms / ctas_per_unit);
     units = std::min<int64_t>(units, std::max<int64_t>(total_tiles, 1));
     p.num_units = static_cast<int>(units);
-    p.segment_cost = narrow ? kNarrowSegmentCost : kSegmentCost;
+    p.segment_cost = (narrow || narrow8) ? kNarrowSegmentCost : kSegmentCost;
 
     // cost axis: row b occupies [start_b, start_b + c_b + tiles_b), its first c_b units
     // being the request-start cost (0 for the first non-empty row)

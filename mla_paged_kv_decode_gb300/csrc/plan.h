@@ -56,6 +56,8 @@ struct PlanData {
     bool narrow = false;              // bf16 cache, h_q <= 32: warp-MMA kernel
     bool pair = false;                // h_q 64/128, bf16 cache: two-CTA cluster kernel, 2 CTAs per unit
     bool e4m3 = false;                // e4m3 cache: tcgen05 kind::f8f6f4 kernel, 16 heads per CTA
+    bool narrow8 = false;             // INT8 cache: codes expanded to f16 in the CTA, warp-MMA kernel,
+                                      //   16 or 32 heads per CTA
     int segment_cost = 0;             // partition cost of a request start, in tiles
     std::vector<int32_t> unit_ptr;
     std::vector<Segment> segments;
@@ -71,8 +73,9 @@ int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int ba
                int h_q, int page_size, int num_sms, int kv_dtype, int out_dtype, PlanData* out);
 
 // Heads handled by one CTA for a given h_q and cache type (0 if unsupported): bf16 cache, all
-// of them (the narrow-head kernel for h_q <= 32, the two-CTA kernel for 64/128); e4m3 cache,
-// 16 (h_q / 16 CTAs per unit).
+// of them (the narrow-head kernel for h_q <= 32, the two-CTA kernel for 64/128); e4m3 cache, 16
+// (the tcgen05 e4m3 kernel, h_q / 16 CTAs per unit); INT8 cache, h_q up to 32 (the 8-bit
+// warp-MMA kernel, h_q / 32 CTAs per unit above).
 int heads_per_cta_for(int h_q, int kv_dtype);
 
 }  // namespace mla

@@ -22,10 +22,17 @@ def cos_dist(a: torch.Tensor, b: torch.Tensor) -> float:
     return float(1.0 - (a @ b) / (a.norm() * b.norm()))
 
 
+def kv_dtype_of(inp):
+    """The cache type of a workloads.Inputs: bf16, e4m3 codes (uint8) or INT8 codes (int8)."""
+    if inp.ckv_scale is None:
+        return mla.MLA_KV_BF16
+    return mla.MLA_KV_INT8 if inp.ckv.dtype == torch.int8 else mla.MLA_KV_FP8_E4M3
+
+
 def run_gpu(inp, sms=None, stream=None):
     """Plan + commit + run on cuda:0; returns (out, lse) on the CPU and the decoder."""
     d = inp.to("cuda")
-    kvd = mla.MLA_KV_FP8_E4M3 if inp.ckv_scale is not None else mla.MLA_KV_BF16
+    kvd = kv_dtype_of(inp)
     dec = mla.Decoder(inp.kv_indptr, inp.kv_last_page_len, inp.h_q, inp.page_size, kv_dtype=kvd, sms=sms,
                       stream=stream)
     out, lse = dec.run(d.q_nope, d.q_pe, d.ckv, d.kpe, d.kv_indices, d.kv_indptr, d.kv_last_page_len,

@@ -30,18 +30,28 @@ def _lens_to_arrays(lens, P):
 
 
 def _check_plan(lens, h_q, P, sms, kv_dtype=mla.MLA_KV_BF16):
-    e4m3 = kv_dtype == mla.MLA_KV_FP8_E4M3
-    # the kernel's tile: 32 tokens for the narrow (warp MMA) bf16 kernel, 128 for the tcgen05 ones
-    TILE = 32 if (h_q <= 32 and not e4m3) else 128
+    bf16 = kv_dtype == mla.MLA_KV_BF16
+    # the kernels: bf16 cache -- warp-MMA kernel up to 32 heads, two-CTA tcgen05 kernel above;
+    # e4m3 cache -- the tcgen05 e4m3 kernel (16 heads a CTA); INT8 cache -- the 8-bit warp-MMA
+    # kernel (up to 32 heads a CTA).  The tile is 32 tokens for the warp-MMA kernels, 128 for the
+    # tcgen05 ones.
+    tcgen05 = kv_dtype == mla.MLA_KV_FP8_E4M3 or (h_q >= 64 and bf16)
+    TILE = 128 if tcgen05 else 32
+    if bf16:
+        want_hg = h_q
+    elif kv_dtype == mla.MLA_KV_FP8_E4M3:
+        want_hg = 16
+    else:
+        want_hg = min(h_q, 32)
     indptr, last = _lens_to_arrays(lens, P)
     plan = mla.mla_decode_plan(torch.from_numpy(indptr), torch.from_numpy(last), len(lens), h_q, P, sms, kv_dtype)
     segs, uptr = mla.mla_plan_get_segments(plan)
     hg = mla.mla_plan_heads_per_cta(plan)
-    assert hg == (16 if e4m3 else h_q)
+    assert hg == want_hg
     groups = h_q // hg
     units = len(uptr) - 1
     assert units == mla.mla_plan_num_units(plan)
-    pair = 2 if (h_q >= 64 and not e4m3) else 1   # bf16 64/128 heads: a cluster of two CTAs per unit
+    pair = 2 if (h_q >= 64 and bf16) else 1   # bf16 64/128 heads: a cluster of two CTAs per unit
     assert mla.mla_plan_num_ctas(plan) == units * groups * pair
     assert units <= max(1, sms // (groups * pair))
     # coverage: each request's tokens exactly once, pieces in token order
@@ -127,7 +137,7 @@ def test_random_plans():
 
 
 def test_e4m3_plans():
-    """The 8-bit cache runs on the tcgen05 kernel: 128-token tiles, 16 heads per CTA."""
+    """The e4m3 cache runs on the tcgen05 kernel: 128-token tiles, 16 heads per CTA."""
     segs, uptr = _check_plan([16384] * 64, 16, 64, 152, mla.MLA_KV_FP8_E4M3)
     assert len(uptr) - 1 == 152
     segs, uptr = _check_plan([4096] * 8, 32, 64, 152, mla.MLA_KV_FP8_E4M3)
@@ -255,3 +265,19 @@ def test_query_rows_plan_fuzz():
         assert mla.mla_plan_num_partials(plan) == n_split
 
     check()
+
+
+def test_int8_plans():
+    """The INT8 cache runs on the 8-bit warp-MMA kernel: 32-token tiles, up to 32 heads per CTA
+    (64 and 128 heads: 2 or 4 CTAs per unit, each streaming the unit's pages)."""
+    segs, uptr = _check_plan([16384] * 64, 16, 64, 152, mla.MLA_KV_INT8)
+    assert len(uptr) - 1 == 152
+    for h_q, units in ((32, 152), (64, 76), (128, 38)):
+        segs, uptr = _check_plan([4096] * 16, h_q, 64, 152, mla.MLA_KV_INT8)
+        assert len(uptr) - 1 == units
+    rng = random.Random(7)
+    for _ in range(20):
+        B = rng.randint(1, 60)
+        lens = [rng.choice([0, 1, rng.randint(1, 300), rng.randint(1, 20000)]) for _ in range(B)]
+        _check_plan(lens, rng.choice([16, 32, 64, 128]), rng.choice([16, 32, 64]), rng.choice([1, 7, 64, 152]),
+                    mla.MLA_KV_INT8)
