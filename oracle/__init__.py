@@ -55,6 +55,8 @@ def _bind(lib):
                                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
     lib.oracle_e4m3_decode.restype = ctypes.c_double
     lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+    lib.oracle_f16_decode.restype = ctypes.c_double
+    lib.oracle_f16_decode.argtypes = [ctypes.c_uint16]
     lib.oracle_e4m3_encode.restype = ctypes.c_uint8
     lib.oracle_e4m3_encode.argtypes = [ctypes.c_double]
     return lib
@@ -73,7 +75,7 @@ def load(path: Optional[str] = None):
 
 
 def _u16(t: torch.Tensor) -> np.ndarray:
-    assert t.dtype == torch.bfloat16
+    assert t.dtype in (torch.bfloat16, torch.float16)
     return np.ascontiguousarray(t.contiguous().view(torch.int16).numpy().view(np.uint16))
 
 
@@ -90,12 +92,19 @@ def _ip(a: np.ndarray):
 
 
 def _cache_arrays(ckv, ckv_scale):
-    """(codes or bf16 bits, cache kind: 0 bf16, 1 e4m3 codes (uint8), 2 int8 codes, scales)."""
+    """(codes or 16-bit bits, cache kind: 0 bf16, 1 e4m3 codes (uint8), 2 int8 codes, 3 fp16, scales)."""
     if ckv.dtype in (torch.uint8, torch.int8):
         assert ckv_scale is not None, "8-bit cache needs its per-token scales"
         return np.ascontiguousarray(ckv.contiguous().view(torch.uint8).numpy()), \
             (1 if ckv.dtype == torch.uint8 else 2), np.ascontiguousarray(ckv_scale.contiguous().to(torch.float32).numpy())
-    return _u16(ckv), 0, None
+    return _u16(ckv), (3 if ckv.dtype == torch.float16 else 0), None
+
+
+def _check_16bit(q_nope, q_pe, ckv, kpe):
+    """fp16 inputs are all fp16 (the cache kind decides how q and kpe are read)."""
+    f16 = ckv.dtype == torch.float16
+    for t in (q_nope, q_pe, kpe):
+        assert (t.dtype == torch.float16) == f16, "q, ckv and kpe must all be fp16, or none of them"
 
 
 def mla_decode(q_nope, q_pe, ckv, kpe, kv_indices, kv_indptr, kv_last_page_len, sm_scale,
@@ -105,6 +114,7 @@ def mla_decode(q_nope, q_pe, ckv, kpe, kv_indices, kv_indptr, kv_last_page_len, 
     lib = lib or load()
     B, H, _ = q_nope.shape
     P = ckv.shape[1]
+    _check_16bit(q_nope, q_pe, ckv, kpe)
     qn, qp, kp = _u16(q_nope), _u16(q_pe), _u16(kpe)
     ck, is8, sc = _cache_arrays(ckv, ckv_scale)
     ind, iptr, last = _i32(kv_indices), _i32(kv_indptr), _i32(kv_last_page_len)
@@ -125,6 +135,7 @@ def mla_decode_range(b, t_begin, t_end, q_nope, q_pe, ckv, kpe, kv_indices, kv_i
     lib = lib or load()
     B, H, _ = q_nope.shape
     P = ckv.shape[1]
+    _check_16bit(q_nope, q_pe, ckv, kpe)
     qn, qp, kp = _u16(q_nope), _u16(q_pe), _u16(kpe)
     ck, is8, sc = _cache_arrays(ckv, ckv_scale)
     ind, iptr = _i32(kv_indices), _i32(kv_indptr)
@@ -239,6 +250,12 @@ def merge(o_parts, lse_parts, lib=None):
     lse = np.zeros((H,), dtype=np.float64)
     lib.oracle_merge(k, H, D, _ptr(o), _ptr(s), _ptr(out), _ptr(lse))
     return torch.from_numpy(out), torch.from_numpy(lse)
+
+
+def f16_decode(bits, lib=None) -> np.ndarray:
+    """IEEE binary16 bit patterns -> float64 (the oracle's own decoder)."""
+    lib = lib or load()
+    return np.array([lib.oracle_f16_decode(int(b)) for b in np.asarray(bits).ravel()], dtype=np.float64)
 
 
 def e4m3_decode(codes, lib=None) -> np.ndarray:

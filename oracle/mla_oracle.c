@@ -40,7 +40,12 @@
  *   subnormals at exponent field 0, no infinities, S.1111.111 is NaN,
  *   largest finite magnitude 448.
  *
- * bf16 inputs are decoded exactly to double; all arithmetic is fp64.
+ *   fp16 inputs ("bf16 / fp16" inputs of the decode kernel, FlashMLA PR #233): q_nope,
+ *   q_pe, ckv and kpe all hold IEEE binary16 values (1 sign, 5 exponent bits with bias
+ *   15, 10 mantissa bits, subnormals at exponent field 0, all-ones exponent for infinities
+ *   and NaN) instead of bfloat16.
+ *
+ * bf16 and fp16 inputs are decoded exactly to double; all arithmetic is fp64.
  * Requests run in parallel with OpenMP; the order of every sum is fixed.
  */
 #include <math.h>
@@ -65,6 +70,22 @@ static double bf16_bits_to_double(uint16_t h) {
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/* IEEE binary16 bits -> double, exactly. */
+double oracle_f16_decode(uint16_t h) {
+    int s = h >> 15;
+    int e = (h >> 10) & 0x1F;
+    int m = h & 0x3FF;
+    double v;
+    if (e == 0x1F) {
+        v = m ? NAN : INFINITY;
+    } else if (e == 0) {
+        v = ldexp((double)m, -24);            /* (m / 1024) * 2^(1 - 15) */
+    } else {
+        v = ldexp(1024.0 + (double)m, e - 25); /* (1 + m / 1024) * 2^(e - 15) */
+    }
+    return s ? -v : v;
 }
 
 double oracle_e4m3_decode(uint8_t code) {
@@ -100,13 +121,24 @@ uint8_t oracle_e4m3_encode(double x) {
     return sign | (uint8_t)best;
 }
 
-/* The cache as the oracle sees it: one token's ckv and kpe rows in fp64. */
+/* The cache as the oracle sees it: one token's ckv and kpe rows in fp64.  ckv_is_fp8 is the
+ * cache kind: 0 bf16, 1 e4m3 codes, 2 int8 codes, 3 fp16 (then q and kpe are fp16 too). */
 typedef struct {
     int page_size, ckv_is_fp8;
     const void* ckv;
     const float* ckv_scale;
     const uint16_t* kpe;
 } cache_view;
+
+/* A 16-bit input value (q or kpe, or a 16-bit ckv) in the cache's format. */
+static double in16(const cache_view* c, uint16_t bits) {
+#if ORACLE_PLANT == 5
+    (void)c;
+    return bf16_bits_to_double(bits);   /* planted: fp16 inputs read as bfloat16 */
+#else
+    return c->ckv_is_fp8 == 3 ? oracle_f16_decode(bits) : bf16_bits_to_double(bits);
+#endif
+}
 
 static void load_token(const cache_view* c, int page, int slot, double* ckv_row, double* kpe_row) {
     size_t tok = (size_t)page * (size_t)c->page_size + (size_t)slot;
@@ -124,10 +156,10 @@ static void load_token(const cache_view* c, int page, int slot, double* ckv_row,
         for (int i = 0; i < ORACLE_D_CKV; ++i) ckv_row[i] = s * (double)codes[i];
     } else {
         const uint16_t* row = (const uint16_t*)c->ckv + tok * ORACLE_D_CKV;
-        for (int i = 0; i < ORACLE_D_CKV; ++i) ckv_row[i] = bf16_bits_to_double(row[i]);
+        for (int i = 0; i < ORACLE_D_CKV; ++i) ckv_row[i] = in16(c, row[i]);
     }
     const uint16_t* krow = c->kpe + tok * ORACLE_D_KPE;
-    for (int j = 0; j < ORACLE_D_KPE; ++j) kpe_row[j] = bf16_bits_to_double(krow[j]);
+    for (int j = 0; j < ORACLE_D_KPE; ++j) kpe_row[j] = in16(c, krow[j]);
 }
 
 /* Token t of a request: its page and slot (standard paged layout). */
@@ -162,9 +194,9 @@ static int attend_range(int H, const cache_view* c,
     if (!err) {
         for (int h = 0; h < H; ++h) {
             for (int i = 0; i < ORACLE_D_CKV; ++i)
-                q[(size_t)h * DQ + i] = bf16_bits_to_double(q_nope_b[(size_t)h * ORACLE_D_CKV + i]);
+                q[(size_t)h * DQ + i] = in16(c, q_nope_b[(size_t)h * ORACLE_D_CKV + i]);
             for (int j = 0; j < ORACLE_D_KPE; ++j)
-                q[(size_t)h * DQ + ORACLE_D_CKV + j] = bf16_bits_to_double(q_pe_b[(size_t)h * ORACLE_D_KPE + j]);
+                q[(size_t)h * DQ + ORACLE_D_CKV + j] = in16(c, q_pe_b[(size_t)h * ORACLE_D_KPE + j]);
         }
         /* x[t,h] = sm_scale * (q_nope . ckv_t + q_pe . kpe_t) */
         for (int t = 0; t < L; ++t) {
@@ -227,7 +259,8 @@ static int request_len(int b, int P, const int32_t* kv_indptr, const int32_t* kv
 }
 
 /* Full decode.  q_nope [B,H,512] bf16 bits, q_pe [B,H,64] bf16 bits,
- * ckv [num_pages,P,512] (bf16 bits; e4m3 codes when ckv_is_fp8 == 1, int8 codes when 2),
+ * ckv [num_pages,P,512] (bf16 bits; e4m3 codes when ckv_is_fp8 == 1, int8 codes when 2; when 3
+ * fp16 bits, and q_nope, q_pe and kpe are fp16 bits too),
  * ckv_scale [num_pages,P] fp32 (8-bit cache only, else NULL),
  * kpe [num_pages,P,64] bf16 bits.  out [B,H,512], lse [B,H] in fp64.
  * threads <= 0 uses the OpenMP default.  Returns 0 on success. */

@@ -437,12 +437,48 @@ def test_non_causal_rows_with_equal_queries_are_equal():
         assert (out[j::qo_len] - o1).abs().max().item() <= 1e-13
 
 
+# ---------------------------------------------------------------- fp16 inputs
+
+def test_f16_decode_all_patterns(lib=None):
+    """The oracle's binary16 decoder against torch's float16 -> float64 conversion (a library
+    routine) on all 65,536 bit patterns, NaNs included."""
+    bits = np.arange(65536, dtype=np.uint16)
+    mine = oracle.f16_decode(bits, lib=lib)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.float16).to(torch.float64).numpy()
+    both_nan = np.isnan(mine) & np.isnan(ref)
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    assert np.array_equal(mine[~both_nan], ref[~both_nan])
+
+
+@pytest.mark.parametrize("H,P", [(4, 16), (16, 32)])
+def test_matches_brute_force_f16(H, P, lib=None):
+    """fp16 q, ckv and kpe: the C oracle against the torch fp64 brute force."""
+    inp = make_inputs(WORKLOADS["tiny"], kv_lens=[1, 9, 40, 70], batch=4, h_q=H, page_size=P, seed=24, f16=True)
+    assert inp.ckv.dtype == torch.float16 and inp.q_nope.dtype == torch.float16
+    out, lse = oracle.mla_decode(*_tiny_args(inp), lib=lib)
+    ref_out, ref_lse = brute_force(*_tiny_args(inp))
+    assert (out - ref_out).abs().max().item() <= 1e-12
+    assert (lse - ref_lse).abs().max().item() <= 1e-12
+
+
+def test_f16_single_token_returns_its_value_row(lib=None):
+    inp = make_inputs(WORKLOADS["tiny"], kv_lens=[1], batch=1, h_q=4, page_size=16, seed=25, f16=True)
+    out, lse = oracle.mla_decode(*_tiny_args(inp), lib=lib)
+    pg = int(inp.kv_indices[0])
+    v = inp.ckv[pg, 0].double()
+    assert torch.equal(out[0], v.unsqueeze(0).expand(4, 512))
+    q = torch.cat([inp.q_nope[0].double(), inp.q_pe[0].double()], dim=1)
+    k = torch.cat([v, inp.kpe[pg, 0].double()])
+    assert (lse[0] - inp.sm_scale * (q @ k)).abs().max().item() <= 1e-12
+
+
 # ---------------------------------------------------------------- the pins catch planted mistakes
 
-@pytest.mark.parametrize("plant", [1, 2, 3, 4])
+@pytest.mark.parametrize("plant", [1, 2, 3, 4, 5])
 def test_planted_mistakes_are_caught(plant, tmp_path):
     """Copies of the oracle with a dropped kpe term (1), min for max (2), reversed slots (3),
-    INT8 codes read unsigned (4): each must fail at least one pin above."""
+    INT8 codes read unsigned (4), fp16 inputs read as bfloat16 (5): each must fail at least one
+    pin above."""
     lib = oracle.load(oracle.build(str(tmp_path / f"liboracle_plant{plant}.so"), plant=plant))
     pins = [lambda: test_golden_closed_form("two_token_ln3.json", lib=lib),
             lambda: test_golden_closed_form("gather_kpe_sign.json", lib=lib),
@@ -450,7 +486,8 @@ def test_planted_mistakes_are_caught(plant, tmp_path):
             lambda: test_zero_scale_gives_mean_and_log_length(lib=lib),
             lambda: test_score_shift_moves_only_lse(lib=lib),
             lambda: test_dominant_score_selects_one_row(lib=lib),
-            lambda: test_int8_oracle_equals_bf16_oracle_on_exact_codes(lib=lib)]
+            lambda: test_int8_oracle_equals_bf16_oracle_on_exact_codes(lib=lib),
+            lambda: test_matches_brute_force_f16(4, 16, lib=lib)]
     failed = 0
     for pin in pins:
         try:

@@ -151,8 +151,9 @@ def quantize_int8_per_token(ckv_bf16: torch.Tensor):
 
 
 def make_inputs(w: Workload, *, kv_lens=None, batch=None, h_q=None, page_size=None,
-                pool_pages=None, seed=None, nan_fill=True, fp8=None, int8=False) -> Inputs:
-    """Draw one seeded batch.  Keyword overrides build smaller variants of a workload."""
+                pool_pages=None, seed=None, nan_fill=True, fp8=None, int8=False, f16=False) -> Inputs:
+    """Draw one seeded batch.  Keyword overrides build smaller variants of a workload.  ``f16``
+    rounds q_nope, q_pe, ckv and kpe to fp16 instead of bf16 (same draws, same order)."""
     B = batch if batch is not None else w.batch
     H = h_q if h_q is not None else w.h_q
     P = page_size if page_size is not None else w.page_size
@@ -182,10 +183,11 @@ def make_inputs(w: Workload, *, kv_lens=None, batch=None, h_q=None, page_size=No
     last = [(L - (n - 1) * P) if n > 0 else 0 for L, n in zip(kv_lens, n_pages)]
     kv_last_page_len = torch.tensor(last, dtype=torch.int32)
 
-    q_nope = torch.randn(B, H, D_CKV, generator=gen).to(torch.bfloat16)
-    q_pe = torch.randn(B, H, D_KPE, generator=gen).to(torch.bfloat16)
-    ckv = torch.randn(pool, P, D_CKV, generator=gen).to(torch.bfloat16)
-    kpe = torch.randn(pool, P, D_KPE, generator=gen).to(torch.bfloat16)
+    dt = torch.float16 if f16 else torch.bfloat16
+    q_nope = torch.randn(B, H, D_CKV, generator=gen).to(dt)
+    q_pe = torch.randn(B, H, D_KPE, generator=gen).to(dt)
+    ckv = torch.randn(pool, P, D_CKV, generator=gen).to(dt)
+    kpe = torch.randn(pool, P, D_KPE, generator=gen).to(dt)
 
     if nan_fill:
         valid = torch.zeros(pool, P, dtype=torch.bool)
