@@ -231,7 +231,7 @@ def kv_dtype_of(inp):
     """The cache type of a workloads.Inputs: bf16, e4m3 codes (uint8) or INT8 codes (int8)."""
     import mla_paged_kv_decode_gb300 as mla
     if inp.ckv_scale is None:
-        return mla.MLA_KV_BF16
+        return mla.MLA_KV_F16 if inp.ckv.dtype == torch.float16 else mla.MLA_KV_BF16
     return mla.MLA_KV_INT8 if inp.ckv.dtype == torch.int8 else mla.MLA_KV_FP8_E4M3
 
 

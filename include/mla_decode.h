@@ -60,8 +60,10 @@ typedef enum {
 typedef enum {
     MLA_KV_BF16 = 0,      /* ckv bf16 [num_pages, page_size, 512] */
     MLA_KV_FP8_E4M3 = 1,  /* ckv uint8 e4m3 codes [num_pages, page_size, 512] + fp32 scale [num_pages, page_size] */
-    MLA_KV_INT8 = 2       /* ckv int8 codes (two's complement) [num_pages, page_size, 512] + fp32 scale
+    MLA_KV_INT8 = 2,      /* ckv int8 codes (two's complement) [num_pages, page_size, 512] + fp32 scale
                              [num_pages, page_size]; token t's latent is scale[t] * code[t, :] */
+    MLA_KV_F16 = 3        /* fp16 inputs: ckv fp16 [num_pages, page_size, 512], and q_nope, q_pe and kpe
+                             are IEEE fp16 too (instead of bf16) */
 } mla_kv_dtype_t;
 
 typedef enum {
@@ -237,11 +239,16 @@ size_t mla_decode_noalloc_max_workspace_bytes(void);
  * t % page_size.  For each row:
  *   q_pe_out[r, h, :]      = rope(q_pe_in[r, h, :], t) for every head h
  *   kpe_cache[page, slot]  = rope(kpe_new[r, :], t)
- *   ckv_cache[page, slot]  = ckv_new[r, :]               (MLA_KV_BF16)
+ *   ckv_cache[page, slot]  = ckv_new[r, :]               (MLA_KV_BF16, MLA_KV_F16)
  *   or, MLA_KV_FP8_E4M3 (quantise on write, every step in fp32):
  *     s = max_i |ckv_new[r, i]| / 448, ckv_scale[page, slot] = s,
  *     ckv_cache[page, slot, i] = e4m3(clamp(ckv_new[r, i] / s, -448, 448)), rounded to
- *     nearest even (s = 0 and codes 0 when the token is all zeros).
+ *     nearest even (s = 0 and codes 0 when the token is all zeros);
+ *   or, MLA_KV_INT8: s = max_i |ckv_new[r, i]| / 127, ckv_scale[page, slot] = s,
+ *     ckv_cache[page, slot, i] = clamp(ckv_new[r, i] / s, -127, 127) rounded to nearest even
+ *     (s = 0 and codes 0 when the token is all zeros).
+ * With MLA_KV_F16 every 16-bit buffer here (q_pe_in/out, ckv_new, kpe_new, the caches) holds
+ * IEEE fp16 values and the rotation rounds to fp16; otherwise they are bf16.
  * q_nope needs no work: the decode reads [q_nope | q_pe] as two buffers.
  * rope(x, t) rotates 32 pairs of the 64 rope dims ("partial apply RoPE (only on first
  * 64-dimension)", "Benchmarking MLA", FlashInfer issue #700): pair i, (x, y) ->
@@ -251,7 +258,7 @@ size_t mla_decode_noalloc_max_workspace_bytes(void);
  *
  *   batch, qo_len      requests (>= 1) and new tokens per request (1 .. 64)
  *   h_q, page_size     1 .. 128 heads; 16, 32 or 64
- *   kv_dtype           the cache type (ckv_scale NULL for bf16, required for e4m3)
+ *   kv_dtype           the cache type (ckv_scale NULL for bf16 / fp16, required for e4m3 / INT8)
  *   q_pe_in, q_pe_out  device bf16 [batch * qo_len, h_q, 64]; may be the same buffer
  *   ckv_new, kpe_new   device bf16 [batch * qo_len, 512] (8-byte aligned), [batch * qo_len, 64]
  *   rope_cos_sin       device fp32 [max_pos, 64]

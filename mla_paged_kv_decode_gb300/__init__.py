@@ -13,7 +13,7 @@ import torch
 
 from ._binding import (  # noqa: F401
     EXPORTED, MLA_ERR_CUDA, MLA_ERR_DEVICE_TIMEOUT, MLA_ERR_INVALID_ARG, MLA_ERR_NOT_COMMITTED,
-    MLA_ERR_UNSUPPORTED, MLA_ERR_WORKSPACE_TOO_SMALL, MLA_KV_BF16, MLA_KV_FP8_E4M3, MLA_KV_INT8, MLA_OK, MLAError, Plan,
+    MLA_ERR_UNSUPPORTED, MLA_ERR_WORKSPACE_TOO_SMALL, MLA_KV_BF16, MLA_KV_FP8_E4M3, MLA_KV_INT8, MLA_KV_F16, MLA_OK, MLAError, Plan,
     library_path, load, mla_decode_device_status, mla_decode_plan, mla_decode_plan_commit,
     mla_decode_plan_workspace_bytes, mla_decode_run, mla_plan_get_segments, mla_plan_heads_per_cta,
     mla_plan_num_ctas, mla_plan_num_partials, mla_plan_num_segments, mla_status_string,

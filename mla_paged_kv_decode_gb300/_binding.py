@@ -27,6 +27,7 @@ MLA_ERR_NOT_COMMITTED = 6
 MLA_KV_BF16 = 0
 MLA_KV_FP8_E4M3 = 1
 MLA_KV_INT8 = 2
+MLA_KV_F16 = 3
 
 MLA_OUT_F32 = 0
 MLA_OUT_BF16 = 1

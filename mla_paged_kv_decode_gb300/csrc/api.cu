@@ -155,15 +155,15 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), int grid, int threads, int smem
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-template <int HG>
+template <int HG, bool F16>
 cudaError_t launch_narrow(const mla_plan_s* p, const CUtensorMap& ckv, const CUtensorMap& kpe, const mla::AttnParams& prm,
                           const void* q_nope, const void* q_pe, cudaStream_t stream) {
     using C = mla::NarrowCfg<HG>;
-    cudaError_t e = cudaFuncSetAttribute(mla::mla_decode_narrow_kernel<HG>,
+    cudaError_t e = cudaFuncSetAttribute(mla::mla_decode_narrow_kernel<HG, F16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int grid = p->d.num_units * p->d.head_groups;
-    return launch_pdl(mla::mla_decode_narrow_kernel<HG>, grid, C::kThreads, C::kSmemBytes, stream, ckv, kpe, prm,
+    return launch_pdl(mla::mla_decode_narrow_kernel<HG, F16>, grid, C::kThreads, C::kSmemBytes, stream, ckv, kpe, prm,
                       static_cast<const uint16_t*>(q_nope), static_cast<const uint16_t*>(q_pe));
 }
 
@@ -190,15 +190,15 @@ cudaError_t launch_e4m3(const mla_plan_s* p, const MapCache& mc, const mla::Attn
                       mc.m_scale, prm, static_cast<const uint16_t*>(q_nope), static_cast<const uint16_t*>(q_pe));
 }
 
-template <int HQ>
+template <int HQ, bool F16>
 cudaError_t launch_pair(const mla_plan_s* p, const MapCache& mc, const mla::AttnParams& prm, const void* q_nope,
                         cudaStream_t stream) {
     using C = mla::PairCfg;
-    cudaError_t e = cudaFuncSetAttribute(mla::mla_decode_pair_kernel<HQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(mla::mla_decode_pair_kernel<HQ, F16>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int grid = 2 * p->d.num_units;   // clusters of two CTAs (the kernel's cluster dimensions)
-    return launch_pdl(mla::mla_decode_pair_kernel<HQ>, grid, C::kThreads, C::kSmemBytes, stream, mc.m_ckv, mc.m_kpe,
+    return launch_pdl(mla::mla_decode_pair_kernel<HQ, F16>, grid, C::kThreads, C::kSmemBytes, stream, mc.m_ckv, mc.m_kpe,
                       mc.m_qp, mc.m_v, prm, static_cast<const uint16_t*>(q_nope));
 }
 
@@ -209,7 +209,7 @@ mla_status_t run_checked(mla_plan_t plan, const void* q_nope, const void* q_pe, 
                          const int32_t* kv_indptr, float sm_scale, void* out, float* lse, uint8_t* ws,
                          cudaStream_t stream, uint64_t* trace) {
     const auto& d = plan->d;
-    const bool f8 = d.kv_dtype != MLA_KV_BF16;   // 8-bit codes
+    const bool f8 = d.kv_dtype == MLA_KV_FP8_E4M3 || d.kv_dtype == MLA_KV_INT8;   // 8-bit codes
     const auto& L = d.layout;
     // tensor maps depend only on the buffer addresses: re-encode when they change
     MapCache& mc = plan->maps;
@@ -269,11 +269,19 @@ mla_status_t run_checked(mla_plan_t plan, const void* q_nope, const void* q_pe, 
     } else if (d.e4m3) {
         e = launch_e4m3(plan, mc, prm, q_nope, q_pe, stream);
     } else if (d.narrow) {
-        e = d.h_q == 16 ? launch_narrow<16>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream)
-                        : launch_narrow<32>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream);
+        if (d.f16)
+            e = d.h_q == 16 ? launch_narrow<16, true>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream)
+                            : launch_narrow<32, true>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream);
+        else
+            e = d.h_q == 16 ? launch_narrow<16, false>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream)
+                            : launch_narrow<32, false>(plan, mc.m_ckv, mc.m_kpe, prm, q_nope, q_pe, stream);
     } else if (d.pair) {
-        e = d.h_q == 128 ? launch_pair<128>(plan, mc, prm, q_nope, stream)
-                         : launch_pair<64>(plan, mc, prm, q_nope, stream);
+        if (d.f16)
+            e = d.h_q == 128 ? launch_pair<128, true>(plan, mc, prm, q_nope, stream)
+                             : launch_pair<64, true>(plan, mc, prm, q_nope, stream);
+        else
+            e = d.h_q == 128 ? launch_pair<128, false>(plan, mc, prm, q_nope, stream)
+                             : launch_pair<64, false>(plan, mc, prm, q_nope, stream);
     } else {
         return MLA_ERR_UNSUPPORTED;   // the plan admits no other head count
     }
@@ -294,8 +302,9 @@ mla_status_t check_run_args(mla_plan_t plan, const void* q_nope, const void* q_p
         return MLA_ERR_INVALID_ARG;
     if (!std::isfinite(sm_scale)) return MLA_ERR_INVALID_ARG;
     if (static_cast<int64_t>(num_pages) * d.page_size >= (int64_t(1) << 31)) return MLA_ERR_INVALID_ARG;
-    if (d.kv_dtype == MLA_KV_BF16 && ckv_scale != nullptr) return MLA_ERR_INVALID_ARG;
-    if (d.kv_dtype != MLA_KV_BF16 && (ckv_scale == nullptr || !aligned16(ckv_scale))) return MLA_ERR_INVALID_ARG;
+    const bool eight = d.kv_dtype == MLA_KV_FP8_E4M3 || d.kv_dtype == MLA_KV_INT8;
+    if (!eight && ckv_scale != nullptr) return MLA_ERR_INVALID_ARG;
+    if (eight && (ckv_scale == nullptr || !aligned16(ckv_scale))) return MLA_ERR_INVALID_ARG;
     return MLA_OK;
 }
 

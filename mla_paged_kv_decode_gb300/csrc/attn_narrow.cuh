@@ -36,6 +36,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "attn.cuh"
 #include "plan.h"
@@ -124,13 +125,43 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+__device__ __forceinline__ void mma_f16_16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// The 16-bit input format of the narrow kernel: bf16, or (F16) IEEE fp16 q, ckv and kpe.  P
+// takes the same format (the MMA's operands share one type); it lies in [0, 2^8].
+template <bool F16>
+__device__ __forceinline__ void mma16_16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    if constexpr (F16)
+        mma_f16_16816(c, a, b0, b1);
+    else
+        mma_bf16_16816(c, a, b0, b1);
+}
+
+template <bool F16>
+__device__ __forceinline__ uint32_t pack16(float lo, float hi) {
+    if constexpr (F16)
+        return pack_f16(lo, hi);
+    else
+        return pack_bf16(lo, hi);
+}
+
 // Address of the 16-byte unit holding (row, dims 8u..8u+7) of a 64-dim chunk stored as
 // rows of 128 bytes with the 128-byte swizzle (unit index XOR row % 8).
 __device__ __forceinline__ uint32_t sw_unit(uint32_t chunk_base, uint32_t row, uint32_t unit) {
     return chunk_base + row * 128 + ((unit ^ (row & 7)) << 4);
 }
 
-template <int HG>
+template <int HG, bool F16 = false>
 __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
     mla_decode_narrow_kernel(const __grid_constant__ CUtensorMap tm_ckv, const __grid_constant__ CUtensorMap tm_kpe,
                              const AttnParams prm, const uint16_t* __restrict__ q_nope,
@@ -354,8 +385,8 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
 #pragma unroll
                     for (int np = 0; np < 2; ++np) {
                         if (np * 16 < ntok) {
-                            mma_bf16_16816(sc[2 * np], qa[ks], bf[np][0], bf[np][1]);
-                            mma_bf16_16816(sc[2 * np + 1], qa[ks], bf[np][2], bf[np][3]);
+                            mma16_16816<F16>(sc[2 * np], qa[ks], bf[np][0], bf[np][1]);
+                            mma16_16816<F16>(sc[2 * np + 1], qa[ks], bf[np][2], bf[np][3]);
                         }
                     }
                 }
@@ -428,7 +459,7 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                     const float p3 = fast_exp2(fmaf(s4[3], prm.scale_log2, -m_run[1]));
                     l_part[0] += p0 + p1;
                     l_part[1] += p2 + p3;
-                    const uint32_t w0 = pack_bf16(p0, p1), w1 = pack_bf16(p2, p3);
+                    const uint32_t w0 = pack16<F16>(p0, p1), w1 = pack16<F16>(p2, p3);
                     *reinterpret_cast<uint32_t*>(pbuf + g * C::kPRowBytes + (kr * 8 + 2 * c4) * 2) = w0;
                     *reinterpret_cast<uint32_t*>(pbuf + (g + 8) * C::kPRowBytes + (kr * 8 + 2 * c4) * 2) = w1;
                 }
@@ -456,8 +487,8 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                     }
 #pragma unroll
                     for (int dp = 0; dp < 8; ++dp) {
-                        mma_bf16_16816(o[2 * dp], pa[kt], vf[dp][0], vf[dp][1]);
-                        mma_bf16_16816(o[2 * dp + 1], pa[kt], vf[dp][2], vf[dp][3]);
+                        mma16_16816<F16>(o[2 * dp], pa[kt], vf[dp][0], vf[dp][1]);
+                        mma16_16816<F16>(o[2 * dp + 1], pa[kt], vf[dp][2], vf[dp][3]);
                     }
                 }
                 __syncwarp();

@@ -94,18 +94,6 @@ struct Narrow8Misc {
     float tg_c;                      // ... and its running scale maximum
 };
 
-__device__ __forceinline__ void mma_f16_16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
-    __half2 v = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-}
-
 // Four INT8 codes (one 32-bit word, first code in the lowest byte) -> four f16 values, exactly:
 // b + 128 as an unsigned byte u, placed under the f16 exponent of 1024 (0x64), reads 1024 + u;
 // subtracting 1152 leaves b (f16 holds every integer below 2048).

@@ -33,6 +33,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "attn.cuh"
 #include "plan.h"
@@ -156,7 +157,9 @@ __device__ __forceinline__ bool pair_wait(uint64_t* bar, uint32_t parity, PairMi
     }
 }
 
-template <int HQ>   // query heads: 128, or 64 with the MMAs' M padded to 128
+// HQ: query heads, 128, or 64 with the MMAs' M padded to 128.  F16: IEEE fp16 q, ckv and kpe
+// (and P) instead of bf16; the MMAs take the matching operand format.
+template <int HQ, bool F16 = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1)
     mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tm_ckv, const __grid_constant__ CUtensorMap tm_kpe,
                            const __grid_constant__ CUtensorMap tm_qpe, const __grid_constant__ CUtensorMap tm_v,
@@ -175,6 +178,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
     const int seg_end = prm.unit_ptr[unit + 1];
     const int P = prm.page_size;
     static_assert(HQ == 64 || HQ == 128, "the two-CTA kernel serves 64 or 128 heads");
+    constexpr uint32_t kIdS = F16 ? idesc_f16(128, 128, false, false) : C::kIdescS;
+    constexpr uint32_t kIdPV = F16 ? idesc_f16(128, 256, false, true) : C::kIdescPV;
     constexpr int hq = HQ;
     const uint32_t partner_abort = mapa_shared(smem_u32(&misc->abort_flag), partner);
 
@@ -341,10 +346,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                         if (c < 8) {
 #pragma unroll
                             for (int k = 0; k < 4; ++k)
-                                umma_bf16_ts(d, tmem + C::kTmemQ + c * 32 + k * 8, bd + 2 * k, C::kIdescS, (c | k) != 0);
+                                umma_bf16_ts(d, tmem + C::kTmemQ + c * 32 + k * 8, bd + 2 * k, kIdS, (c | k) != 0);
                         } else {
 #pragma unroll
-                            for (int k = 0; k < 4; ++k) umma_bf16(d, qdesc0 + 2 * k, bd + 2 * k, C::kIdescS, 1);
+                            for (int k = 0; k < 4; ++k) umma_bf16(d, qdesc0 + 2 * k, bd + 2 * k, kIdS, 1);
                         }
                         umma_commit(&misc->k_empty[c]);
                         MLA_TRACE_UNIT(3, kcount);
@@ -455,8 +460,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                                 const float p0 = fast_exp2(fmaf(s[t], prm.scale_log2, -m_run));
                                 const float p1 = fast_exp2(fmaf(s[t + 1], prm.scale_log2, -m_run));
                                 l += p0 + p1;
-                                __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
-                                w[e] = *reinterpret_cast<uint32_t*>(&v);
+                                if constexpr (F16) {
+                                    __half2 v = __floats2half2_rn(p0, p1);
+                                    w[e] = *reinterpret_cast<uint32_t*>(&v);
+                                } else {
+                                    __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
+                                    w[e] = *reinterpret_cast<uint32_t*>(&v);
+                                }
                             }
                             st_shared_v4(pstage_row + ck * C::kChunkBytes + ((u ^ (h & 7)) << 4), w[0], w[1], w[2], w[3]);
                         }
@@ -603,7 +613,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                                 const int kk = 2 * q + k2;   // 16-token step within the tile
                                 if (16 * kk >= ntok) break;
                                 const uint64_t ad = pdesc + static_cast<uint64_t>(((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4);
-                                umma_bf16(tmem + 256 * half, ad, bslot + (k2 ? voff1 : 0u), C::kIdescPV,
+                                umma_bf16(tmem + 256 * half, ad, bslot + (k2 ? voff1 : 0u), kIdPV,
                                           (first && kk == 0) ? 0u : 1u);
                             }
                             umma_commit(&misc->v_empty[s]);

@@ -48,7 +48,7 @@ int heads_per_cta_for(int h_q, int kv_dtype) {
 int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int batch, int qo_len, bool causal,
                int h_q, int page_size, int num_sms, int kv_dtype, int out_dtype, PlanData* out) {
     if (!kv_indptr || !kv_last_page_len || !out || batch < 1 || num_sms < 1) return 1;
-    if (kv_dtype != 0 && kv_dtype != 1 && kv_dtype != 2) return 1;
+    if (kv_dtype < 0 || kv_dtype > 3) return 1;
     if (out_dtype != 0 && out_dtype != 1) return 1;
     if (qo_len < 1 || qo_len > kMaxQoLen) return 1;
     if (static_cast<int64_t>(batch) * qo_len * 128 >= (int64_t(1) << 31)) return 1;
@@ -100,6 +100,7 @@ int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int ba
     p.pair = h_q >= 64 && !eight;
     p.e4m3 = e4m3;
     p.narrow8 = narrow8;
+    p.f16 = kv_dtype == 3;
     const int ctas_per_unit = p.head_groups * (p.pair ? 2 : 1);
     int64_t units = std::max(1, num_sms / ctas_per_unit);
     units = std::min<int64_t>(units, std::max<int64_t>(total_tiles, 1));

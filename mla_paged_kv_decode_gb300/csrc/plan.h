@@ -58,6 +58,7 @@ struct PlanData {
     bool e4m3 = false;                // e4m3 cache: tcgen05 kind::f8f6f4 kernel, 16 heads per CTA
     bool narrow8 = false;             // INT8 cache: codes expanded to f16 in the CTA, warp-MMA kernel,
                                       //   16 or 32 heads per CTA
+    bool f16 = false;                 // fp16 q, ckv and kpe (narrow or two-CTA kernel) instead of bf16
     int segment_cost = 0;             // partition cost of a request start, in tiles
     std::vector<int32_t> unit_ptr;
     std::vector<Segment> segments;

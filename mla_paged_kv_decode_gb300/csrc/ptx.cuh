@@ -196,7 +196,8 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate, issued by one thread.
+// D[tmem] (+)= A[smem] * B[smem]^T, 16-bit inputs (bf16, or f16: the instruction descriptor says
+// which), fp32 accumulate, issued by one thread.
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                           uint32_t accumulate) {
     asm volatile(
@@ -207,7 +208,7 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
         : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]^T, bf16 inputs, fp32 accumulate: A is M rows in TMEM lanes
+// D[tmem] (+)= A[tmem] * B[smem]^T, 16-bit inputs (as above), fp32 accumulate: A is M rows in TMEM lanes
 // with two bf16 per 32-bit column (a 16-wide k-step spans 8 columns).
 __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                              uint32_t accumulate) {
@@ -333,6 +334,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
     return (1u << 4)                                  // D format: f32
            | (1u << 7)                                // A format: bf16
            | (1u << 10)                               // B format: bf16
+           | ((a_mn_major ? 1u : 0u) << 15)           // A major-ness
+           | ((b_mn_major ? 1u : 0u) << 16)           // B major-ness
+           | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
+}
+
+// Instruction descriptor for kind::f16 with f16 A/B (format code 0) and fp32 accumulation.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn_major, bool b_mn_major) {
+    return (1u << 4)                                  // D format: f32
            | ((a_mn_major ? 1u : 0u) << 15)           // A major-ness
            | ((b_mn_major ? 1u : 0u) << 16)           // B major-ness
            | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8

@@ -202,9 +202,10 @@ def decode_prologue(q_pe, ckv_new, kpe_new, rope_cos_sin, kv_indices, kv_indptr,
     and leaves the inputs untouched.  Row r = b * qo_len + j is new token j of request b, at
     position t = L_b - qo_len + j (the new tokens are the last qo_len of the cache), page
     kv_indices[kv_indptr[b] + t // P], slot t % P; a row with t < 0 or t >= max_pos is skipped.
-    q_pe and kpe are rotated (``rope_f64``, then rounded to bf16); ckv is copied, or for the
-    8-bit cache quantised with s = absmax / 448 and codes e4m3(x / s), both in fp32 (the
-    precision the quantised code is decided in), ``e4m3_encode`` rounding to nearest even."""
+    q_pe and kpe are rotated (``rope_f64``, then rounded to their own 16-bit type); ckv is copied,
+    or for the e4m3 cache quantised with s = absmax / 448 and codes e4m3(x / s), both in fp32 (the
+    precision the quantised code is decided in), ``e4m3_encode`` rounding to nearest even, or for
+    the INT8 cache with s = absmax / 127 and codes x / s rounded half to even within +-127."""
     lib = lib or load()
     P = ckv_cache.shape[1]
     num_pages = ckv_cache.shape[0]
@@ -220,13 +221,23 @@ def decode_prologue(q_pe, ckv_new, kpe_new, rope_cos_sin, kv_indices, kv_indptr,
         if t < 0 or t >= max_pos:
             continue
         c, s = rope_cos_sin[t, :32], rope_cos_sin[t, 32:]
-        q_out[r] = rope_f64(q_pe[r], c, s, interleaved).to(torch.bfloat16)
+        q_out[r] = rope_f64(q_pe[r], c, s, interleaved).to(q_pe.dtype)
         page = int(kv_indices[indptr[b] + t // P])
         if not 0 <= page < num_pages:
             continue
         slot = t % P
-        kpe[page, slot] = rope_f64(kpe_new[r], c, s, interleaved).to(torch.bfloat16)
-        if ckv.dtype == torch.uint8:
+        kpe[page, slot] = rope_f64(kpe_new[r], c, s, interleaved).to(kpe.dtype)
+        if ckv.dtype == torch.int8:
+            # INT8: s = absmax / 127 and codes x / s rounded half to even, in fp32
+            x = ckv_new[r].to(torch.float32).numpy()
+            scale = np.float32(np.abs(x).max()) / np.float32(127.0)
+            if scale > 0:
+                y = np.rint((x / scale).astype(np.float32))
+                ckv[page, slot] = torch.from_numpy(np.clip(y, -127, 127).astype(np.int8))
+            else:
+                ckv[page, slot] = 0
+            sc[page, slot] = float(scale)
+        elif ckv.dtype == torch.uint8:
             x = ckv_new[r].to(torch.float32).numpy()
             scale = np.float32(np.abs(x).max()) / np.float32(448.0)
             if scale > 0:

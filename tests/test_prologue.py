@@ -9,12 +9,13 @@ import pytest
 import torch
 
 import oracle
-from workloads import WORKLOADS, make_inputs, new_tokens, quantize_e4m3_per_token, rope_table
+from workloads import (WORKLOADS, make_inputs, new_tokens, quantize_e4m3_per_token, quantize_int8_per_token,
+                       rope_table)
 
 
-def _inputs(lens, H=4, P=16, seed=90, fp8=False):
+def _inputs(lens, H=4, P=16, seed=90, fp8=False, int8=False, f16=False):
     return make_inputs(WORKLOADS["tiny"], kv_lens=list(lens), batch=len(lens), h_q=H, page_size=P, seed=seed,
-                       fp8=fp8)
+                       fp8=fp8, int8=int8, f16=f16)
 
 
 def _run(inp, qo_len, table, interleaved, seed=91):
@@ -84,6 +85,42 @@ def test_quantise_on_write_matches_the_cache_quantiser():
         assert sc[pg, sl].item() == scale[b, 0].item(), b
     pg, sl = _slot(inp, 2, 63)
     assert sc[pg, sl].item() == 0.0 and (ckv[pg, sl] == 0).all()
+
+
+def test_int8_quantise_on_write_matches_the_cache_quantiser():
+    """The INT8 write equals quantize_int8_per_token (torch's round-half-even) on the same token:
+    identical codes and scales; an all-zero token gets scale 0 and zero codes."""
+    inp = _inputs([5, 33, 64, 100], int8=True)
+    q_pe, ckv_new, kpe_new = new_tokens(inp, 1, seed=93)
+    ckv_new[1] = 0
+    _, ckv, _, sc = oracle.decode_prologue(q_pe, ckv_new, kpe_new, rope_table(128), inp.kv_indices, inp.kv_indptr,
+                                           inp.kv_last_page_len, 1, False, inp.ckv, inp.kpe, ckv_scale=inp.ckv_scale)
+    codes, scale = quantize_int8_per_token(ckv_new.unsqueeze(1))
+    for b, L in enumerate(inp.kv_lens.tolist()):
+        pg, sl = _slot(inp, b, L - 1)
+        assert torch.equal(ckv[pg, sl], codes[b, 0]), b
+        assert sc[pg, sl].item() == scale[b, 0].item(), b
+    pg, sl = _slot(inp, 1, 32)
+    assert sc[pg, sl].item() == 0.0 and (ckv[pg, sl] == 0).all()
+
+
+def test_f16_prologue_rounds_to_f16():
+    """fp16 inputs: the rotation is rounded to fp16 (a quarter turn maps (a, b) to (-b, a)
+    exactly, so the written kpe is exact), and the latent is copied bit for bit."""
+    inp = _inputs([3, 40], f16=True)
+    q_pe, ckv_new, kpe_new = new_tokens(inp, 1, seed=94, f16=True)
+    table = torch.zeros(64, 64)
+    table[:, 32:] = 1.0   # cos 0, sin 1 at every position: a quarter turn
+    q_out, ckv, kpe, _ = oracle.decode_prologue(q_pe, ckv_new, kpe_new, table, inp.kv_indices, inp.kv_indptr,
+                                                inp.kv_last_page_len, 1, False, inp.ckv, inp.kpe)
+    assert q_out.dtype == torch.float16 and kpe.dtype == torch.float16
+    for b, L in enumerate(inp.kv_lens.tolist()):
+        pg, sl = _slot(inp, b, L - 1)
+        a, bb = kpe_new[b, :32], kpe_new[b, 32:]
+        assert torch.equal(kpe[pg, sl], torch.cat([-bb, a]))
+        assert torch.equal(ckv[pg, sl].view(torch.int16), ckv_new[b].view(torch.int16))
+    a, bb = q_pe[..., :32], q_pe[..., 32:]
+    assert torch.equal(q_out, torch.cat([-bb, a], dim=-1))
 
 
 @pytest.mark.parametrize("qo_len", [1, 3])

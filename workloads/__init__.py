@@ -243,15 +243,16 @@ def rope_table(max_pos: int, base: float = 10000.0) -> torch.Tensor:
     return torch.cat([torch.cos(ang), torch.sin(ang)], dim=1).to(torch.float32)
 
 
-def new_tokens(inp: Inputs, qo_len: int, seed: int):
+def new_tokens(inp: Inputs, qo_len: int, seed: int, f16: bool = False):
     """The new tokens' inputs to the prologue, from their own seeded generator: pre-rotation
     q_pe [B * qo_len, H, 64], latent ckv [B * qo_len, 512] and pre-rotation kpe [B * qo_len, 64],
-    all bf16."""
+    all bf16 (fp16 with ``f16``)."""
     gen = torch.Generator().manual_seed(seed)
     R = inp.batch * qo_len
-    q_pe = torch.randn(R, inp.h_q, D_KPE, generator=gen).to(torch.bfloat16)
-    ckv = torch.randn(R, D_CKV, generator=gen).to(torch.bfloat16)
-    kpe = torch.randn(R, D_KPE, generator=gen).to(torch.bfloat16)
+    dt = torch.float16 if f16 else torch.bfloat16
+    q_pe = torch.randn(R, inp.h_q, D_KPE, generator=gen).to(dt)
+    ckv = torch.randn(R, D_CKV, generator=gen).to(dt)
+    kpe = torch.randn(R, D_KPE, generator=gen).to(dt)
     return q_pe, ckv, kpe
 
 
