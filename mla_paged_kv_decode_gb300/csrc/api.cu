@@ -35,6 +35,7 @@ struct mla_plan_s {
     std::vector<uint8_t> image;   // header bytes copied to the workspace by commit
     void* pinned = nullptr;       // pinned staging copy of `image`
     std::vector<void*> committed; // workspaces this plan has been committed to
+    int test_withhold = 0;        // test builds (MLA_TEST_HOOKS) only
 };
 
 namespace {
@@ -262,6 +263,7 @@ mla_status_t run_checked(mla_plan_t plan, const void* q_nope, const void* q_pe, 
     prm.head_groups = d.head_groups;
     prm.num_pages = num_pages;
     prm.out_bf16 = d.out_dtype == MLA_OUT_BF16 ? 1 : 0;
+    prm.test_withhold = plan->test_withhold;
     cudaError_t e;
     if (d.narrow8) {
         e = d.heads_per_cta == 16 ? launch_narrow8<16>(plan, mc, prm, q_nope, q_pe, stream)
@@ -380,6 +382,14 @@ mla_status_t mla_decode_run(mla_plan_t plan, const void* q_nope, const void* q_p
 // Debug builds only: device buffer of 4 * 8 * 256 uint64 timestamps filled by the next runs.
 void mla_debug_set_trace(mla_plan_t plan, void* dev_buf) {
     if (plan) plan->trace = static_cast<uint64_t*>(dev_buf);
+}
+#endif
+
+#ifdef MLA_TEST_HOOKS
+// Test builds only: with withhold != 0 the bf16 narrow-head kernel's CTA 0 never fills its first
+// ring stage, so a consumer's bounded wait runs out (a failure made without any fault).
+void mla_debug_set_withhold(mla_plan_t plan, int withhold) {
+    if (plan) plan->test_withhold = withhold;
 }
 #endif
 

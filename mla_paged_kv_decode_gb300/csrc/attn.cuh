@@ -26,7 +26,11 @@
 namespace mla {
 
 constexpr uint32_t kStatusTimeout = 0x100u;       // OR-ed with the wait site id
-constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s without progress before giving up
+// Time without progress before a wait gives up: 4 s (a test build may set a shorter limit).
+#ifndef MLA_WAIT_LIMIT_NS
+#define MLA_WAIT_LIMIT_NS 4000000000ull
+#endif
+constexpr uint64_t kWaitLimitNs = MLA_WAIT_LIMIT_NS;
 
 struct AttnParams {
     const int32_t* unit_ptr;      // [num_units + 1]
@@ -50,6 +54,7 @@ struct AttnParams {
     int head_groups;
     int num_pages;                // pages in the cache buffers
     int out_bf16;                 // the final output is bf16 (partials stay fp32)
+    int test_withhold;            // test builds (MLA_TEST_HOOKS) only: CTA 0 withholds its first stage
 };
 
 // A destination of fp32 results: a buffer base and its element type.  The final output may

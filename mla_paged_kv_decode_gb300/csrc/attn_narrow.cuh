@@ -250,6 +250,13 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                 if (lane == 0 && use > 0) ok = wait_phase_flag(&misc->empty[s], (use - 1) & 1, &misc->abort_flag, prm.status, 21);
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) break;
+#ifdef MLA_TEST_HOOKS
+                // test builds: CTA 0 never fills its first stage, so the bounded wait on it runs out
+                if (prm.test_withhold && blockIdx.x == 0 && scount == 0) {
+                    ++scount;
+                    continue;
+                }
+#endif
                 uint8_t* dst = stage_base + s * C::kStageBytes;
                 // bytes per token: bf16 ckv + kpe = 1152
                 if (lane == 0)
