@@ -336,6 +336,61 @@ def bench_device(inp, steps, warmup, stream):
     return dec, step, (out, lse, d)
 
 
+def packed_e2e(inp, d, dec, stream):
+    """The end-to-end step: the inputs of one decode packed in one pinned host buffer (q_nope,
+    q_pe, kv_indices, kv_indptr, kv_last_page_len, each at a 256-byte boundary) mirrored by one
+    device buffer whose views the decode reads, and out + lse in one device buffer mirrored by one
+    pinned host buffer.  Captured as a CUDA graph: H2D copy, mla_decode_run, D2H copy.  Returns the
+    step, the bytes each way, and a check that the host copy of the result equals the device's."""
+    import mla_paged_kv_decode_gb300 as mla
+    align = lambda n: (n + 255) // 256 * 256
+    srcs = [inp.q_nope, inp.q_pe, inp.kv_indices.to(torch.int32), inp.kv_indptr.to(torch.int32),
+            inp.kv_last_page_len.to(torch.int32)]
+    offs, total = [], 0
+    for t in srcs:
+        offs.append(total)
+        total += align(t.numel() * t.element_size())
+    host_in = torch.empty(total, dtype=torch.uint8).pin_memory()
+    dev_in = torch.empty(total, dtype=torch.uint8, device="cuda")
+    views = []
+    for t, o in zip(srcs, offs):
+        n = t.numel() * t.element_size()
+        host_in[o:o + n].copy_(t.contiguous().view(-1).view(torch.uint8))
+        views.append(dev_in[o:o + n].view(t.dtype).view(t.shape))
+    q_nope, q_pe, kv_indices, kv_indptr, kv_last = views
+    n_out = inp.batch * inp.h_q * 512 * 4
+    n_lse = inp.batch * inp.h_q * 4
+    dev_out = torch.empty(n_out + n_lse, dtype=torch.uint8, device="cuda")
+    host_out = torch.empty(n_out + n_lse, dtype=torch.uint8).pin_memory()
+    out = dev_out[:n_out].view(torch.float32).view(inp.batch, inp.h_q, 512)
+    lse = dev_out[n_out:].view(torch.float32).view(inp.batch, inp.h_q)
+
+    def body():
+        dev_in.copy_(host_in, non_blocking=True)
+        mla.mla_decode_run(dec.plan, q_nope, q_pe, d.ckv, d.ckv_scale, d.kpe, kv_indices, kv_indptr, kv_last,
+                           inp.sm_scale, out, lse, dec.workspace, stream=stream)
+        host_out.copy_(dev_out, non_blocking=True)
+
+    with torch.cuda.stream(stream):   # warm-up outside the capture (tensor maps for these buffers)
+        body()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        body()
+
+    def step():
+        with torch.cuda.stream(stream):
+            g.replay()
+        stream.synchronize()
+
+    def check():
+        step()
+        return bool(torch.equal(host_out[:n_out].view(torch.float32), out.cpu().view(-1).view(torch.float32)))
+
+    return {"step": step, "h2d": total, "d2h": n_out + n_lse, "check": check, "graph": g,
+            "keep": (host_in, dev_in, dev_out, host_out)}
+
+
 def profile_only(args):
     """warmup + steps decodes of one workload through the library, checked, for ncu captures."""
     import mla_paged_kv_decode_gb300 as mla
@@ -432,38 +487,27 @@ def main():
     attn_avg = total_s / args.steps
     achieved = alg_bytes / attn_avg / 1e9
 
-    # ---- end to end through the public API with host buffers: per step H2D of the
-    # step's inputs (q_nope, q_pe and the page table) from pinned memory, run, D2H of out + lse
+    # ---- end to end through the public API with host buffers.  The step's inputs (q_nope, q_pe
+    # and the page table) live in one pinned host buffer laid out as one device buffer, and out +
+    # lse in one device buffer laid out as one pinned host buffer, so a step is one H2D copy, the
+    # decode and one D2H copy, all three captured in a CUDA graph (the decode call is graph-safe):
+    # per step one graph launch and one host synchronisation.
     out, lse, d = keep
-    host_in = [t.cpu().pin_memory() for t in (inp.q_nope, inp.q_pe, inp.kv_indices, inp.kv_indptr,
-                                               inp.kv_last_page_len)]
-    dev_in = [d.q_nope, d.q_pe, d.kv_indices, d.kv_indptr, d.kv_last_page_len]
-    host_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory(),
-                torch.empty(lse.shape, dtype=lse.dtype).pin_memory()]
-    h2d = sum(t.numel() * t.element_size() for t in host_in)
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    e2e = packed_e2e(inp, d, dec, stream)
     e2e_steps = max(10, min(args.steps, 500))
-
-    def e2e_step():
-        with torch.cuda.stream(stream):
-            for hsrc, ddst in zip(host_in, dev_in):
-                ddst.copy_(hsrc, non_blocking=True)
-            mla.mla_decode_run(dec.plan, d.q_nope, d.q_pe, d.ckv, d.ckv_scale, d.kpe, d.kv_indices, d.kv_indptr,
-                               d.kv_last_page_len, inp.sm_scale, out, lse, dec.workspace, stream=stream)
-            host_out[0].copy_(out, non_blocking=True)
-            host_out[1].copy_(lse, non_blocking=True)
-        stream.synchronize()
-
     for _ in range(3):
-        e2e_step()
+        e2e["step"]()
     if world > 1:
         torch.distributed.barrier()
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
-        e2e_step()
+        e2e["step"]()
     e2e_s = (time.perf_counter() - t0) / e2e_steps
     e2e_s = max_over_ranks(e2e_s, world, "cuda")
     e2e_value = alg_bytes * world / e2e_s / 1e9
+    h2d, d2h = e2e["h2d"], e2e["d2h"]
+    e2e_ok = e2e["check"]()
+    del e2e
 
     # ---- secondary: compute-shaped workload (TFLOPS), device-timed the same way
     secondary = None
@@ -551,7 +595,9 @@ def main():
                          "kernel_us": attn_avg * 1e6},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "steps": e2e_steps, "note": "per step: H2D q + page table, decode, D2H out + lse; KV resident"},
+                    "steps": e2e_steps, "copies_checked": e2e_ok,
+                    "note": "per step: one H2D copy of q + page table from pinned memory, the decode, one D2H "
+                            "copy of out + lse, as one CUDA graph replay and a host sync; KV resident"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
             "secondary": secondary,
