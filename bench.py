@@ -250,20 +250,20 @@ def time_workload(inp, n, stream):
 
 
 def plan_balance(plan, h_q: int, kv_dtype: int) -> dict:
-    """Max / mean unit cost of a plan: a unit's cost is its tiles plus the plan's start cost per
-    request it starts (the measure the planner equalises)."""
+    """Max / mean unit cost of a plan: a unit's cost is its tiles plus the plan's segment cost per
+    segment after its first (the measure whose maximum the planner minimises)."""
     import mla_paged_kv_decode_gb300 as mla
     tile = 128 if (h_q >= 64 and kv_dtype != mla.MLA_KV_INT8) else 32   # tcgen05 kernels: 128-token tiles
     segs, uptr = mla.mla_plan_get_segments(plan)
     c = mla.mla_plan_segment_cost_tiles(plan)
     cost, tiles = [], []
     for u in range(len(uptr) - 1):
-        s = segs[uptr[u]:uptr[u + 1]]
-        nt = sum((int(t1) - int(t0) + tile - 1) // tile for _, t0, t1, _ in s if t1 > t0)
+        s = [x for x in segs[uptr[u]:uptr[u + 1]] if x[2] > x[1]]
+        nt = sum((int(t1) - int(t0) + tile - 1) // tile for _, t0, t1, _ in s)
         tiles.append(nt)
-        cost.append(nt + c * sum(1 for _, t0, t1, _ in s if t1 > t0 and t0 == 0))
+        cost.append(nt + c * max(0, len(s) - 1))
     ratio = lambda v: (max(v) * len(v) / sum(v)) if sum(v) else None
-    return {"units": len(cost), "tile": tile, "start_cost_tiles": c, "cost_max_over_mean": ratio(cost),
+    return {"units": len(cost), "tile": tile, "segment_cost_tiles": c, "cost_max_over_mean": ratio(cost),
             "tiles_max_over_mean": ratio(tiles), "segments": int(len(segs)),
             "partials": mla.mla_plan_num_partials(plan)}
 

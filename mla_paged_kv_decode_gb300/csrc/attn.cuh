@@ -145,12 +145,25 @@ __device__ __forceinline__ bool wait_phase_flag(uint64_t* bar, uint32_t parity, 
     do {                                                                                      \
         if (prm.trace) prm.trace[4 * 8 * 256 + blockIdx.x * 8 + (k)] = MLA_TRACE_NOW();       \
     } while (0)
+// A second set of 8 milestones per CTA (after CTA 1's unit lanes); the stamp is read after
+// `dep` is available, so it marks the arrival of the loads `dep` depends on.
+#define MLA_TRACE_CTA2(k, dep)                                                                \
+    do {                                                                                      \
+        if (prm.trace) {                                                                      \
+            uint64_t t_;                                                                      \
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_) : "f"(dep));                 \
+            prm.trace[4 * 8 * 256 + gridDim.x * 8 + 4 * 1024 + blockIdx.x * 8 + (k)] = t_;    \
+        }                                                                                     \
+    } while (0)
 #else
 #define MLA_TRACE_EVENT(ev, idx) \
     do {                         \
     } while (0)
 #define MLA_TRACE_CTA(k) \
     do {                 \
+    } while (0)
+#define MLA_TRACE_CTA2(k, dep) \
+    do {                       \
     } while (0)
 #define MLA_TRACE_UNIT(ln, idx) \
     do {                        \
@@ -384,6 +397,7 @@ __device__ __forceinline__ void merge_split_pieces_wide16(const AttnParams& prm,
             for (int h = 0; h < kHB; ++h)
                 v[i][h] = (p0 + i < n_slots) ? __ldcg(piece_o(p0 + i, hb + h)) : make_float4(0.f, 0.f, 0.f, 0.f);
     };
+    if (tid == 0) MLA_TRACE_CTA2(0, 0.f);
     load_block(0);   // in flight during the lse pass
     if (tid < 128) {
         const int h = tid / kTph, sub = tid % kTph;
@@ -403,6 +417,7 @@ __device__ __forceinline__ void merge_split_pieces_wide16(const AttnParams& prm,
         }
     }
     named_barrier_sync(bar256, 256);
+    if (tid == 0) MLA_TRACE_CTA2(1, s_w[0]);
     float4 acc[kHB];
 #pragma unroll
     for (int h = 0; h < kHB; ++h) acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -422,10 +437,12 @@ __device__ __forceinline__ void merge_split_pieces_wide16(const AttnParams& prm,
             }
         }
     }
+    if (tid == 0) MLA_TRACE_CTA2(2, acc[0].x);
     const OutDst od = final_out(prm);
     const size_t o0 = (static_cast<size_t>(b) * hq + head0) * kDimCkv + 4 * t;
 #pragma unroll
     for (int h = 0; h < kHB; ++h) st_out4(od, o0 + static_cast<size_t>(hb + h) * kDimCkv, acc[h]);
+    if (tid == 0) MLA_TRACE_CTA2(3, 0.f);
 }
 
 // Walks the non-empty segments of one CTA slot tile by tile.

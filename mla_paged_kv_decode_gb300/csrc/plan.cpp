@@ -5,11 +5,11 @@
 // here is the plainest one that balances SMs: lay every request's tokens end
 // to end in request order, cut the sequence into tiles of the kernel's tile size
 // (32 tokens for the bf16 cache with 16/32 heads, 128 otherwise; a request's last tile may
-// be short), and cut the sequence into U contiguous ranges of equal cost, one
-// per CTA slot.  A tile costs 1; every request start after the first also costs
-// kSegmentCost tiles, because a CTA that crosses into a new request pays a second
-// segment prologue and epilogue (query load, merge of its warp groups, output or
-// partial write).  A request whose tiles land in more than one slot becomes
+// be short), and cut the sequence into U contiguous ranges, one per CTA slot, that
+// minimise the largest range cost.  A tile costs 1; every segment of a range after its
+// first also costs the kernel's segment cost in tiles, because a CTA that moves on to
+// another request pays a second segment prologue and epilogue (query load, merge of its
+// warp groups, output or partial write).  A request whose tiles land in more than one slot becomes
 // several split pieces, each writing a partial (out, lse); the CTA finishing the
 // last piece merges them in slot order.
 //
@@ -107,45 +107,59 @@ int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int ba
     p.num_units = static_cast<int>(units);
     p.segment_cost = (narrow || narrow8) ? kNarrowSegmentCost : kSegmentCost;
 
-    // cost axis: row b occupies [start_b, start_b + c_b + tiles_b), its first c_b units
-    // being the request-start cost (0 for the first non-empty row)
-    int64_t total_cost = 0;
-    bool first = true;
-    for (int b = 0; b < rows; ++b) {
-        if (tiles[b] == 0) continue;
-        total_cost += (first ? 0 : p.segment_cost) + tiles[b];
-        first = false;
-    }
-    // unit u owns cost positions [bound(u), bound(u+1))
-    auto bound = [&](int64_t u) { return u * total_cost / units; };
-
-    std::vector<std::vector<Segment>> per_unit(units);
+    // A unit's cost is its tiles plus segment_cost for every segment after its first (each
+    // further segment pays a query load, an epilogue and a partial write or a merge).  fill(T)
+    // walks the rows in order and gives each unit tiles until one more segment would pass T;
+    // it returns the number of units used.  Giving a unit more tiles never adds to a later
+    // unit's cost, so the smallest T with fill(T) <= units is the smallest maximum cost any
+    // contiguous partition reaches.
+    const int64_t c = p.segment_cost;
+    std::vector<std::vector<Segment>> per_unit;
     std::vector<int> pieces(rows, 0);
-    int64_t cost_base = 0;
-    int64_t u = 0;
-    first = true;
-    for (int b = 0; b < rows; ++b) {
-        if (tiles[b] == 0) continue;
-        const int64_t r0 = cost_base + (first ? 0 : p.segment_cost);   // cost position of tile 0
-        const int64_t r1 = r0 + tiles[b];
-        first = false;
-        for (int64_t t0 = r0; t0 < r1;) {
-            while (bound(u + 1) <= t0) ++u;
-            const int64_t end = std::min<int64_t>(r1, bound(u + 1));
-            Segment s{};
-            s.b = b;
-            s.kv = b / qo_len;
-            s.t_begin = static_cast<int32_t>((t0 - r0) * tile_tok);
-            s.t_end = static_cast<int32_t>(std::min<int64_t>((end - r0) * tile_tok, len[b]));
-            s.slot = -1;
-            s.item = -1;
-            per_unit[u].push_back(s);
-            ++pieces[b];
-            t0 = end;
+    auto fill = [&](int64_t T, bool record) -> int64_t {
+        int64_t used = 0, cost = 0, segs = 0;
+        for (int b = 0; b < rows; ++b) {
+            for (int64_t t = 0; t < tiles[b];) {
+                int64_t room = used == 0 ? 0 : T - cost - (segs > 0 ? c : 0);
+                if (room < 1) {
+                    ++used;
+                    cost = 0;
+                    segs = 0;
+                    room = T;
+                    if (record) per_unit.emplace_back();
+                }
+                const int64_t k = std::min(tiles[b] - t, room);
+                if (record) {
+                    Segment sg{};
+                    sg.b = b;
+                    sg.kv = b / qo_len;
+                    sg.t_begin = static_cast<int32_t>(t * tile_tok);
+                    sg.t_end = static_cast<int32_t>(std::min<int64_t>((t + k) * tile_tok, len[b]));
+                    sg.slot = -1;
+                    sg.item = -1;
+                    per_unit.back().push_back(sg);
+                    ++pieces[b];
+                }
+                cost += k + (segs > 0 ? c : 0);
+                ++segs;
+                t += k;
+            }
         }
-        cost_base = r1;
+        return used;
+    };
+    int64_t lo = 1, hi = total_tiles + c * rows + 1;   // fill(hi) is 1 (or 0 with no tiles)
+    while (lo < hi) {
+        const int64_t mid = lo + (hi - lo) / 2;
+        if (fill(mid, false) <= units)
+            hi = mid;
+        else
+            lo = mid + 1;
     }
-
+    fill(lo, true);
+    // the units the fill used (the cost bound may leave the last ones without tiles)
+    units = std::max<int64_t>(1, static_cast<int64_t>(per_unit.size()));
+    per_unit.resize(static_cast<size_t>(units));
+    p.num_units = static_cast<int>(units);
     // partial slots: a split request's pieces get consecutive slots in token order
     std::vector<int> slot_begin(rows, -1);
     int next_slot = 0;

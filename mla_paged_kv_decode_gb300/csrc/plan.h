@@ -10,11 +10,11 @@ namespace mla {
 
 constexpr int kTileTokens = 128;   // tokens per tile of the tcgen05 kernels (64/128 heads, e4m3 cache)
 constexpr int kNarrowTileTokens = 32;  // tokens per tile of the narrow-head (warp MMA) kernel
-// Partition cost of a request start (after the first), in tiles: what a CTA that crosses
-// into another request pays for the second segment's prologue and epilogue, measured on
+// Partition cost of a unit's every segment after its first, in tiles: what a CTA that moves
+// on to another request pays for the further segment's prologue and epilogue, measured on
 // GB300 against the time of one tile.
 #ifndef MLA_NARROW_SEGMENT_COST
-#define MLA_NARROW_SEGMENT_COST 8
+#define MLA_NARROW_SEGMENT_COST 4
 #endif
 constexpr int kNarrowSegmentCost = MLA_NARROW_SEGMENT_COST;
 constexpr int kSegmentCost = 1;

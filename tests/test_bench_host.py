@@ -45,7 +45,7 @@ def test_plan_balance_of_the_membound_plan():
     last = torch.full((B,), P, dtype=torch.int32)
     plan = mla.mla_decode_plan(indptr, last, B, 16, P, 152)
     bal = bench.plan_balance(plan, 16, mla.MLA_KV_BF16)
-    assert bal["units"] == 152 and bal["tile"] == 32 and bal["start_cost_tiles"] == 8
+    assert bal["units"] <= 152 and bal["tile"] == 32 and bal["segment_cost_tiles"] == 4
     assert 1.0 <= bal["tiles_max_over_mean"] <= 1.1
     assert bal["partials"] == mla.mla_plan_num_partials(plan)
     assert bal["segments"] == mla.mla_plan_num_segments(plan)
