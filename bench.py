@@ -397,7 +397,12 @@ def profile_only(args):
     torch.cuda.set_device(0)
     mla.load()
     w = WORKLOADS[args.workload]
-    inp = make_inputs(w) if args.kv_len is None else make_inputs(w, kv_lens=[args.kv_len] * w.batch, batch=w.batch)
+    kw = {} if args.kv_len is None else {"kv_lens": [args.kv_len] * w.batch, "batch": w.batch}
+    if args.cache == "int8":
+        kw.update(fp8=False, int8=True)
+    elif args.cache == "bf16":
+        kw.update(fp8=False)
+    inp = make_inputs(w, **kw)
     stream = torch.cuda.Stream()
     dec, step, keep = bench_device(inp, args.steps, args.warmup, stream)
     with torch.cuda.stream(stream):
@@ -407,7 +412,8 @@ def profile_only(args):
     st = mla.mla_decode_device_status(dec.plan, dec.workspace, stream)
     out = keep[0]
     assert st == 0 and bool(torch.isfinite(out).all()), f"status {st}"
-    print(f"profile-only: {args.workload} batch {inp.batch} h_q {inp.h_q} launches {args.warmup + args.steps} ok")
+    print(f"profile-only: {args.workload} ({args.cache} cache) batch {inp.batch} h_q {inp.h_q} "
+          f"launches {args.warmup + args.steps} ok")
 
 
 def main():
@@ -426,6 +432,8 @@ def main():
     ap.add_argument("--profile-only", action="store_true",
                     help="run warmup + steps decodes of --workload on the device and exit, no timing or JSON "
                          "(the program the profiles' ncu commands capture)")
+    ap.add_argument("--cache", default="workload", choices=["workload", "bf16", "int8"],
+                    help="with --profile-only: the workload's own cache, or the same shape with a bf16 or INT8 cache")
     ap.add_argument("--kv-len", type=int, default=None,
                     help="with --profile-only: every request's kv_len (a smaller case of the workload)")
     args = ap.parse_args()
@@ -552,7 +560,7 @@ def main():
                "speedup_vs_bf16": t16 / t8, "bytes_per_token": {"fp8": 644, "int8": 644, "bf16": 1152},
                "traffic": recorded_traffic("fp8"),
                "int8": {"us_per_step": ti * 1e6, "gbs": bi / ti / 1e9, "hbm_frac": bi / ti / 1e9 / hbm_gbs,
-                        "speedup_vs_bf16": t16 / ti}}
+                        "speedup_vs_bf16": t16 / ti, "traffic": recorded_traffic("int8")}}
 
     # ---- every workload of the measurement table, one decode at a time: eager and graph replay
     configs = None
