@@ -391,6 +391,46 @@ def packed_e2e(inp, d, dec, stream):
             "keep": (host_in, dev_in, dev_out, host_out)}
 
 
+def bench_layer(batches=(1, 8, 32, 64), kv_len: int = 4096, reps: int = 30) -> dict:
+    """Row f4: one MLA decode layer (DeepSeek-V2-Lite-shaped: 2048 wide, 16 heads; synthetic
+    weights) as one CUDA graph -- q and kv projections (cuBLAS), the prologue (RoPE and the new
+    token's cache write), the decode, the value and output projections -- at kv_len cached
+    tokens per request (the new token the last), page 64, bf16 and e4m3 caches.  Each replay
+    is timed by its own event pair after L2 is flushed (a 512 MB write), as a layer of a deep
+    model finds its weights and cache cold; the median per batch size."""
+    import mla_paged_kv_decode_gb300 as mla
+    from mla_paged_kv_decode_gb300.layer import DecodeLayer, LayerWeights
+    from workloads import layer_hidden, layer_weights, rope_table
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device="cuda")
+    w = LayerWeights(**vars(layer_weights(7))).to("cuda")
+    rope = rope_table(kv_len + 1)
+    res = {"shape": "hidden 2048, 16 heads, q_nope 128, q_pe 64, latent 512, v 128; page 64", "kv_len": kv_len,
+           "timing": "CUDA graph replay, median of %d, L2 flushed before each" % reps, "us_per_layer": {}}
+    for cache, fp8 in (("bf16", False), ("e4m3", True)):
+        res["us_per_layer"][cache] = {}
+        for b in batches:
+            inp = make_inputs(WORKLOADS["membound"], kv_lens=[kv_len] * b, batch=b, fp8=fp8)
+            d = inp.to("cuda")
+            layer = DecodeLayer(w, inp.kv_indptr, inp.kv_last_page_len, inp.page_size, rope,
+                                kv_dtype=mla.MLA_KV_FP8_E4M3 if fp8 else mla.MLA_KV_BF16)
+            x = layer_hidden(b, 8).cuda()
+            layer.capture(x, d.ckv, d.kpe, d.kv_indices, d.kv_indptr, d.kv_last_page_len, ckv_scale=d.ckv_scale)
+            ts = []
+            for i in range(reps + 3):
+                flush.fill_(i & 0xFF)
+                a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                layer.replay()
+                e.record()
+                torch.cuda.synchronize()
+                if i >= 3:
+                    ts.append(a.elapsed_time(e) * 1e3)
+            assert mla.mla_decode_device_status(layer.plan, layer.workspace) == mla.MLA_OK
+            res["us_per_layer"][cache][str(b)] = sorted(ts)[len(ts) // 2]
+            del layer, d, inp
+    return res
+
+
 def profile_only(args):
     """warmup + steps decodes of one workload through the library, checked, for ncu captures."""
     import mla_paged_kv_decode_gb300 as mla
@@ -426,6 +466,8 @@ def main():
     ap.add_argument("--secondary", default="compute", help="second workload to report (TFLOPS), or 'none'")
     ap.add_argument("--sample-requests", type=int, default=16)
     ap.add_argument("--fp8", type=int, default=1, help="also time the 8-bit cache workload against bf16 (1/0)")
+    ap.add_argument("--layer", type=int, default=1,
+                    help="also time one decode layer as a CUDA graph at batch 1, 8, 32, 64 (1/0)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--configs", type=int, default=1,
                     help="also report every workload's per-call median, eager and CUDA-graph replay (1/0)")
@@ -562,6 +604,9 @@ def main():
                "int8": {"us_per_step": ti * 1e6, "gbs": bi / ti / 1e9, "hbm_frac": bi / ti / 1e9 / hbm_gbs,
                         "speedup_vs_bf16": t16 / ti, "traffic": recorded_traffic("int8")}}
 
+    # ---- row f4: one decode layer as a CUDA graph
+    layer = bench_layer() if (args.layer and rank == 0 and world == 1) else None
+
     # ---- every workload of the measurement table, one decode at a time: eager and graph replay
     configs = None
     if args.configs and rank == 0 and world == 1:
@@ -610,6 +655,7 @@ def main():
             "clocks": clocks,
             "secondary": secondary,
             "fp8": fp8,
+            "layer": layer,
             "configs": configs,
         }
         print(json.dumps(line), flush=True)

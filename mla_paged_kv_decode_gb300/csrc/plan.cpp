@@ -116,9 +116,12 @@ int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int ba
     const int64_t c = p.segment_cost;
     std::vector<std::vector<Segment>> per_unit;
     std::vector<int> pieces(rows, 0);
+    int64_t fill_max_pieces = 0;   // (set by fill) the most pieces any request was cut into
     auto fill = [&](int64_t T, bool record) -> int64_t {
         int64_t used = 0, cost = 0, segs = 0;
+        fill_max_pieces = 0;
         for (int b = 0; b < rows; ++b) {
+            int64_t np = 0;
             for (int64_t t = 0; t < tiles[b];) {
                 int64_t room = used == 0 ? 0 : T - cost - (segs > 0 ? c : 0);
                 if (room < 1) {
@@ -143,19 +146,44 @@ int build_plan(const int32_t* kv_indptr, const int32_t* kv_last_page_len, int ba
                 cost += k + (segs > 0 ? c : 0);
                 ++segs;
                 t += k;
+                ++np;
             }
+            fill_max_pieces = std::max(fill_max_pieces, np);
         }
         return used;
     };
-    int64_t lo = 1, hi = total_tiles + c * rows + 1;   // fill(hi) is 1 (or 0 with no tiles)
-    while (lo < hi) {
-        const int64_t mid = lo + (hi - lo) / 2;
-        if (fill(mid, false) <= units)
-            hi = mid;
-        else
-            lo = mid + 1;
+    auto min_bound = [&](int64_t U) {   // the smallest T with fill(T) <= U
+        int64_t lo = 1, hi = total_tiles + c * rows + 1;   // fill(hi) is 1 (or 0 with no tiles)
+        while (lo < hi) {
+            const int64_t mid = lo + (hi - lo) / 2;
+            if (fill(mid, false) <= U)
+                hi = mid;
+            else
+                lo = mid + 1;
+        }
+        return lo;
+    };
+    // A split request is merged by its last piece after every piece is done, reading the
+    // others' partials: about merge_q / 4 tiles' time per piece.  With few
+    // requests, cutting them over every SM makes that merge the longest step (one 4096-token
+    // request over 128 SMs: 128 pieces), so the plan weighs a unit count U by
+    // bound(U) + merge cost x (most pieces of a request at U) over U = units * k / 16 and takes
+    // the cheapest (the full count on ties).
+    const double merge_q = (e4m3 ? kMergeCostQuarterTilesE4m3 : kMergeCostQuarterTiles) / 4.0;
+    int64_t best_T = min_bound(units), best_U = units;
+    double best_score = static_cast<double>(best_T) + (fill_max_pieces > 1 ? merge_q * fill_max_pieces : 0.0);
+    for (int k = 15; k >= 1; --k) {
+        const int64_t U = std::max<int64_t>(1, units * k / 16);
+        if (U >= best_U && U != 1) continue;
+        const int64_t T = min_bound(U);
+        const double score = static_cast<double>(T) + (fill_max_pieces > 1 ? merge_q * fill_max_pieces : 0.0);
+        if (score < best_score) {
+            best_score = score;
+            best_T = T;
+            best_U = U;
+        }
     }
-    fill(lo, true);
+    fill(best_T, true);
     // the units the fill used (the cost bound may leave the last ones without tiles)
     units = std::max<int64_t>(1, static_cast<int64_t>(per_unit.size()));
     per_unit.resize(static_cast<size_t>(units));

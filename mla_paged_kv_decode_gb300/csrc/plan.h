@@ -18,6 +18,11 @@ constexpr int kNarrowTileTokens = 32;  // tokens per tile of the narrow-head (wa
 #endif
 constexpr int kNarrowSegmentCost = MLA_NARROW_SEGMENT_COST;
 constexpr int kSegmentCost = 1;
+// The last piece's merge of a split request, in quarter tiles per piece: about a tile's time for
+// the warp-MMA kernels (32-token tiles) and the two-CTA kernel (a 128-head piece is 256 KB), a
+// quarter tile for the e4m3 kernel (128-token tiles, 16-head pieces of 32 KB).
+constexpr int kMergeCostQuarterTiles = 4;
+constexpr int kMergeCostQuarterTilesE4m3 = 1;
 constexpr int kDimCkv = 512;
 constexpr int kDimKpe = 64;
 

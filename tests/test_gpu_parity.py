@@ -79,10 +79,13 @@ def test_single_request_64_heads(L):
     assert_parity(out, lse, *oracle.decode_inputs(inp))
 
 
-def test_one_long_request_split_over_every_sm():
+def test_one_long_request_split_into_many_pieces():
+    """A lone 32768-token request: the plan cuts it into a few tens of pieces (it weighs their
+    merge against the streaming time), more than 8, so the last piece merges them in several
+    rounds of 8."""
     inp = _small([32768], 16, 16, seed=8)
     out, lse, dec, _ = run_gpu(inp)
-    assert mla.mla_plan_num_partials(dec.plan) > 100
+    assert mla.mla_plan_num_partials(dec.plan) > 16
     assert_parity(out, lse, *oracle.decode_inputs(inp))
 
 

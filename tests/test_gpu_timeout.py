@@ -7,8 +7,9 @@ MLA_ERR_DEVICE_TIMEOUT.  This test builds a test copy of the library with a 2 ms
 hook that makes the narrow-head kernel's CTA 0 withhold the copy of its first ring stage -- a
 barrier nothing completes -- and checks:
 
-* the run returns, the status word names the site of the wait that ran out, and
-  mla_decode_device_status reports MLA_ERR_DEVICE_TIMEOUT (and clears the word);
+* the run returns, the status word names the site of a wait that ran out because of the
+  withheld stage (whichever reached the limit first), and mla_decode_device_status reports
+  MLA_ERR_DEVICE_TIMEOUT (and clears the word);
 * after a re-commit (which resets the workspace's counters) a run without the hook gives the
   same bits as a clean run, and the status is MLA_OK;
 * the same for mla_decode_run_noalloc, whose status word is read with a NULL workspace.
@@ -24,8 +25,11 @@ from workloads import WORKLOADS, make_inputs
 
 pytestmark = pytest.mark.gpu
 
-SITE_FULL_WAIT = 22    # a compute group waiting for its stage to land
-SITE_READY_WAIT = 24   # a last-arriving piece waiting for the other pieces' partials
+# the waits the withheld stage can make run out; the first to reach the limit records its site
+SITES = (21,   # the producer waiting for the withheld stage's release before refilling it
+         22,   # a compute group waiting for the stage to land
+         23,   # the other token group waiting for the stage's release before its own tile
+         24)   # a last-arriving piece (in any CTA) waiting for the other pieces' partials
 
 
 @pytest.fixture(scope="module")
@@ -78,7 +82,7 @@ def test_withheld_stage_times_out_and_the_next_run_is_clean(lib):
         lib.mla_debug_set_withhold(handle, 1)
         run()
         word = int(ws[:4].view(torch.int32).item())
-        assert word in (0x100 | SITE_FULL_WAIT, 0x100 | SITE_READY_WAIT), hex(word)
+        assert word in tuple(0x100 | site for site in SITES), hex(word)
         assert lib.mla_decode_device_status(handle, _vp(ws), stream) == mla.MLA_ERR_DEVICE_TIMEOUT
         assert int(ws[:4].view(torch.int32).item()) == 0   # read once, then cleared
 

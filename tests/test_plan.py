@@ -107,8 +107,10 @@ def _check_plan(lens, h_q, P, sms, kv_dtype=mla.MLA_KV_BF16):
     assert mla.mla_plan_num_partials(plan) == n_split
     # balance: a unit's cost is its tiles plus c for every segment after its first.  The plan's
     # largest unit cost must be the smallest any contiguous partition of the request order into
-    # at most the available units reaches: no partition with a smaller maximum exists
-    # (_fits, an exhaustive-by-greedy feasibility test), and every unit holds tiles.
+    # at most the units it uses reaches: no partition with a smaller maximum exists (_fits, an
+    # exhaustive-by-greedy feasibility test), and every unit holds tiles.  (The plan may use
+    # fewer units than the GPU has, when cutting few requests over every SM would make their
+    # merges the longest step.)
     c = mla.mla_plan_segment_cost_tiles(plan)
     assert c >= 0
     tiles, cost = [], []
@@ -122,8 +124,7 @@ def _check_plan(lens, h_q, P, sms, kv_dtype=mla.MLA_KV_BF16):
     assert sum(tiles) == total
     if total:
         assert min(tiles) >= 1
-        avail = min(max(1, sms // (groups * pair)), total)
-        assert not _fits([t for t in row_tiles if t], max(cost) - 1, c, avail), (max(cost), c)
+        assert not _fits([t for t in row_tiles if t], max(cost) - 1, c, units), (max(cost), c)
     # workspace holds every partial
     assert plan.workspace_bytes >= n_split * h_q * (512 + 1) * 4
     return segs, uptr
@@ -301,3 +302,18 @@ def test_int8_plans():
         lens = [rng.choice([0, 1, rng.randint(1, 300), rng.randint(1, 20000)]) for _ in range(B)]
         _check_plan(lens, rng.choice([16, 32, 64, 128]), rng.choice([16, 32, 64]), rng.choice([1, 7, 64, 152]),
                     mla.MLA_KV_INT8)
+
+
+def test_few_long_requests_are_not_cut_over_every_sm():
+    """One 4096-token request at 16 heads is 128 tiles: cut over 128 SMs, its last piece would
+    merge 128 partials.  The plan weighs the merge (about a tile per piece) against the
+    streaming time and cuts it into far fewer pieces; a full batch still uses every SM."""
+    for lens, h_q, kv in (([4096], 16, mla.MLA_KV_BF16), ([32768], 128, mla.MLA_KV_BF16),
+                          ([4096], 16, mla.MLA_KV_FP8_E4M3)):
+        segs, uptr = _check_plan(lens, h_q, 64, 152, kv)
+        pieces = sum(1 for b, t0, t1, _ in segs if t1 > t0)
+        tile = 32 if (h_q <= 32 and kv == mla.MLA_KV_BF16) else 128
+        tiles = (lens[0] + tile - 1) // tile
+        assert 2 <= pieces <= 2 * int(tiles ** 0.5) + 2, (lens, h_q, pieces)
+    segs, uptr = _check_plan([4096] * 64, 16, 64, 152)
+    assert len(uptr) - 1 >= 148

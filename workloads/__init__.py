@@ -269,3 +269,30 @@ def algorithmic_bytes(inp: Inputs) -> int:
 def algorithmic_flops(inp: Inputs) -> int:
     """2*H*L*(576 + 512): the QK^T and PV contractions; exp is not counted."""
     return 2 * inp.h_q * int(inp.kv_lens.sum()) * (D_CKV + D_KPE + D_CKV)
+
+
+def layer_weights(seed: int, d_model: int = 2048, heads: int = 16, d_nope: int = 128, d_v: int = 128):
+    """Synthetic weights of one MLA decode layer (DeepSeek-V2-Lite's sizes by default), bf16 on
+    the CPU, from their own seeded generator: w_q [D, H, d_nope + 64], w_kv [D, 512],
+    w_kpe [D, 64], w_uk [H, d_nope, 512], w_uv [H, 512, d_v], w_o [H * d_v, D]; each drawn
+    gaussian and divided by the square root of its input width, so activations stay O(1)."""
+    gen = torch.Generator().manual_seed(seed)
+
+    def draw(*shape, fan_in):
+        return (torch.randn(*shape, generator=gen) / fan_in ** 0.5).to(torch.bfloat16)
+
+    import types
+    return types.SimpleNamespace(
+        w_q=draw(d_model, heads, d_nope + D_KPE, fan_in=d_model),
+        w_kv=draw(d_model, D_CKV, fan_in=d_model),
+        w_kpe=draw(d_model, D_KPE, fan_in=d_model),
+        w_uk=draw(heads, d_nope, D_CKV, fan_in=d_nope),
+        w_uv=draw(heads, D_CKV, d_v, fan_in=D_CKV),
+        w_o=draw(heads * d_v, d_model, fan_in=heads * d_v),
+    )
+
+
+def layer_hidden(batch: int, seed: int, d_model: int = 2048) -> torch.Tensor:
+    """The new tokens' hidden states x [B, D], bf16, from their own seeded generator."""
+    gen = torch.Generator().manual_seed(seed)
+    return torch.randn(batch, d_model, generator=gen).to(torch.bfloat16)
