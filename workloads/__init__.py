@@ -223,14 +223,15 @@ def make_inputs(w: Workload, *, kv_lens=None, batch=None, h_q=None, page_size=No
                   torch.tensor(kv_lens, dtype=torch.int64), ckv_scale, ckv_bf16)
 
 
-def query_rows(inp: Inputs, qo_len: int, seed: int):
+def query_rows(inp: Inputs, qo_len: int, seed: int, f16: bool = False):
     """Queries for qo_len new tokens per request, from their own seeded generator:
-    (q_nope [B * qo_len, H, 512], q_pe [B * qo_len, H, 64]) bf16, row b * qo_len + j being
-    token j of request b."""
+    (q_nope [B * qo_len, H, 512], q_pe [B * qo_len, H, 64]) bf16 (fp16 with ``f16``), row
+    b * qo_len + j being token j of request b."""
     gen = torch.Generator().manual_seed(seed)
     R = inp.batch * qo_len
-    q_nope = torch.randn(R, inp.h_q, D_CKV, generator=gen).to(torch.bfloat16)
-    q_pe = torch.randn(R, inp.h_q, D_KPE, generator=gen).to(torch.bfloat16)
+    dt = torch.float16 if f16 else torch.bfloat16
+    q_nope = torch.randn(R, inp.h_q, D_CKV, generator=gen).to(dt)
+    q_pe = torch.randn(R, inp.h_q, D_KPE, generator=gen).to(dt)
     return q_nope, q_pe
 
 
