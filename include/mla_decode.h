@@ -215,8 +215,8 @@ int mla_plan_get_segments(mla_plan_t plan, int32_t* segments, int32_t* unit_ptr)
  * zeroed merge counters and status word) into the array on cuda_stream, straight from
  * the plan's own pageable host memory, then launches the decode.  The first call on a
  * device also looks up the array's device address (cudaGetSymbolAddress) and keeps it
- * for the life of the process; make that first call before any stream capture, and
- * make no call after a cudaDeviceReset, which leaves the kept address stale.
+ * for the life of the process; make no call after a cudaDeviceReset, which leaves the
+ * kept address stale.
  * All calls share the one array: calls whose work may overlap on the GPU (different
  * streams, or different host threads) race and corrupt each other's partials; order
  * them on one stream.  A bounded wait that ran out is reported by
