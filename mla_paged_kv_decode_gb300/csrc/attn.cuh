@@ -191,22 +191,31 @@ __device__ __forceinline__ float warp_sum(float v) {
 //     M = max_i lse_i,  w_i = exp(lse_i - M) / sum_j exp(lse_j - M),
 //     out = sum_i w_i o_i,  lse = M + ln sum_j exp(lse_j - M).
 // Every sum runs in a fixed order (pieces in slot order, fixed shuffle trees), so reruns
-// give identical bits.  The loads are issued in batches (all heads of a piece at once) so
-// the merge costs a few memory round trips rather than one per (piece, head).
+// give identical bits.  The loads are issued in batches (several pieces and heads at once)
+// so the merge costs a few memory round trips rather than one per (piece, head).
 // NTHR threads (tid 0..NTHR-1) call it together and synchronise on named barrier `bar`.
-// Scratch in shared memory: s_max[NH], s_inv[NH], s_w[8 * NH] (and NTHR >= 8 * 16).
+// Scratch in shared memory: s_max[NH], s_inv[NH], s_w[max(8 * NH, 128)].
 //
-// This general form takes five or more dependent rounds of L2 loads (the lse, the weights,
-// then each piece); merge_split_pieces below serves up to 8 pieces in two or three.
+// This general form serves any number of pieces.  Its outputs go by chunks of 8 pieces
+// (their weights staged in shared memory) and, beyond 16 heads or with 256 threads, by blocks
+// of 8 heads, each chunk's loads in rounds of 4 pieces x 8 heads (2 pieces for 16 heads, whose
+// two 8-head blocks run side by side on 256 threads); 128 threads and 16 heads load one piece
+// of all 16 heads a round.
+// Every output sums the same products in the same order (pieces in slot order, from 0) with
+// 128 or 256 threads, so the two forms give identical bits.  The up-to-8 form below takes
+// fewer rounds.
 template <int NH, int NTHR>
 __device__ __forceinline__ void merge_split_pieces_chunked(const AttnParams& prm, int b, int slot_begin, int n_slots,
                                                            int head0, int tid, uint32_t bar, float* s_max,
                                                            float* s_inv, float* s_w) {
-    static_assert(NTHR == 128 && NH % 16 == 0 && NTHR % NH == 0, "merge layout");
-    constexpr int kTph = NTHR / NH;    // threads per head in the lse pass
-    constexpr int kChunk = NTHR / 16;  // pieces whose weights are staged at a time (8)
+    static_assert(NH % 16 == 0 && (NTHR == 128 || (NTHR == 256 && NH == 16)), "merge layout");
+    constexpr int kTph = 128 / NH;     // threads per head in the lse pass (threads 0..127)
+    constexpr int kBlocks = NTHR / 128;   // 8-head blocks merged side by side
+    // pieces per round of loads: 4 for the many heads of the two-CTA kernel (its threads hold 255
+    // registers), 2 for 16 heads on 256 threads (within the warp-MMA kernels' registers)
+    constexpr int kHB = 8, kPB = NH > 16 ? 4 : 2, kChunk = 8;
     const size_t hq = static_cast<size_t>(prm.h_q);
-    {
+    if (tid < 128) {
         // ---- lse pass: thread (h, sub) scans pieces sub, sub + kTph, ... with a running (max, sum)
         const int h = tid / kTph, sub = tid % kTph;
         float m = -INFINITY, s = 0.f;
@@ -236,30 +245,30 @@ __device__ __forceinline__ void merge_split_pieces_chunked(const AttnParams& prm
         }
     }
     named_barrier_sync(bar, NTHR);
-    // ---- outputs: thread tid owns dims [4 tid, 4 tid + 4) of every head
     const OutDst od = final_out(prm);
-    const size_t o0 = (static_cast<size_t>(b) * hq + head0) * kDimCkv + 4 * tid;
-#pragma unroll 1
-    for (int hb = 0; hb < NH; hb += 16) {
+    const int t = tid & 127, g = tid >> 7;
+    const size_t o0 = (static_cast<size_t>(b) * hq + head0) * kDimCkv + 4 * t;
+    if constexpr (NH == 16 && NTHR == 128) {
+        // ---- outputs, 128 threads and 16 heads: thread t owns dims [4 t, 4 t + 4) of every head,
+        // one piece (all 16 heads) per round of loads, within the warp-MMA kernels' registers
         float4 acc[16];
 #pragma unroll
         for (int h = 0; h < 16; ++h) acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
         for (int c0 = 0; c0 < n_slots; c0 += kChunk) {
             {
-                const int i = tid / 16, h = tid % 16;   // weight of piece c0 + i for head hb + h
+                const int i = tid / 16, h = tid % 16;   // weight of piece c0 + i for head h
                 float w = 0.f;
                 if (c0 + i < n_slots)
-                    w = expf(__ldcg(prm.part_lse + (slot_begin + c0 + i) * hq + head0 + hb + h) - s_max[hb + h]) *
-                        s_inv[hb + h];
+                    w = expf(__ldcg(prm.part_lse + (slot_begin + c0 + i) * hq + head0 + h) - s_max[h]) * s_inv[h];
                 s_w[tid] = w;
             }
             named_barrier_sync(bar, NTHR);
             const int n = min(kChunk, n_slots - c0);
 #pragma unroll 1
             for (int i = 0; i < n; ++i) {
-                const float4* src =
-                    reinterpret_cast<const float4*>(prm.part_o + ((slot_begin + c0 + i) * hq + head0 + hb) * kDimCkv) + tid;
+                const float4* src = reinterpret_cast<const float4*>(prm.part_o + ((slot_begin + c0 + i) * hq + head0) *
+                                                                                    kDimCkv) + t;
                 float4 v[16];
 #pragma unroll
                 for (int h = 0; h < 16; ++h) v[h] = __ldcg(src + h * (kDimCkv / 4));
@@ -275,7 +284,58 @@ __device__ __forceinline__ void merge_split_pieces_chunked(const AttnParams& prm
             named_barrier_sync(bar, NTHR);   // s_w is rewritten next
         }
 #pragma unroll
-        for (int h = 0; h < 16; ++h) st_out4(od, o0 + static_cast<size_t>(hb + h) * kDimCkv, acc[h]);
+        for (int h = 0; h < 16; ++h) st_out4(od, o0 + static_cast<size_t>(h) * kDimCkv, acc[h]);
+    } else {
+    // ---- outputs: thread t owns dims [4 t, 4 t + 4) of its block's 8 heads
+#pragma unroll 1
+    for (int hb0 = 0; hb0 < NH; hb0 += kHB * kBlocks) {
+        const int hb = hb0 + g * kHB;   // this thread's first head
+        float4 acc[kHB];
+#pragma unroll
+        for (int h = 0; h < kHB; ++h) acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+        for (int c0 = 0; c0 < n_slots; c0 += kChunk) {
+            if (tid < kBlocks * kChunk * kHB) {   // weight of piece c0 + i for head hb0 + 8 gb + h
+                const int gb = tid / (kChunk * kHB), i = (tid / kHB) % kChunk, h = tid % kHB;
+                const int head = hb0 + gb * kHB + h;
+                float w = 0.f;
+                if (c0 + i < n_slots)
+                    w = expf(__ldcg(prm.part_lse + (slot_begin + c0 + i) * hq + head0 + head) - s_max[head]) *
+                        s_inv[head];
+                s_w[tid] = w;
+            }
+            named_barrier_sync(bar, NTHR);
+            const int cn = min(kChunk, n_slots - c0);
+#pragma unroll 1
+            for (int p0 = 0; p0 < cn; p0 += kPB) {
+                float4 v[kPB][kHB];
+#pragma unroll
+                for (int i = 0; i < kPB; ++i)
+#pragma unroll
+                    for (int h = 0; h < kHB; ++h)
+                        v[i][h] = (p0 + i < cn)
+                                      ? __ldcg(reinterpret_cast<const float4*>(
+                                                   prm.part_o + ((slot_begin + c0 + p0 + i) * hq + head0 + hb + h) *
+                                                                    kDimCkv) + t)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int i = 0; i < kPB; ++i) {
+                    if (p0 + i >= cn) break;
+#pragma unroll
+                    for (int h = 0; h < kHB; ++h) {
+                        const float w = s_w[(g * kChunk + p0 + i) * kHB + h];
+                        acc[h].x = fmaf(w, v[i][h].x, acc[h].x);
+                        acc[h].y = fmaf(w, v[i][h].y, acc[h].y);
+                        acc[h].z = fmaf(w, v[i][h].z, acc[h].z);
+                        acc[h].w = fmaf(w, v[i][h].w, acc[h].w);
+                    }
+                }
+            }
+            named_barrier_sync(bar, NTHR);   // s_w is rewritten next
+        }
+#pragma unroll
+        for (int h = 0; h < kHB; ++h) st_out4(od, o0 + static_cast<size_t>(hb + h) * kDimCkv, acc[h]);
+    }
     }
 }
 
@@ -380,8 +440,7 @@ __device__ __forceinline__ void merge_split_pieces_wide16(const AttnParams& prm,
                                                           float* s_max, float* s_inv, float* s_w) {
     constexpr int NH = 16, kMax = 8, kTph = 8, kHB = 8, kPB = 4;
     if (n_slots > kMax) {
-        if (tid < 128)
-            merge_split_pieces_chunked<NH, 128>(prm, b, slot_begin, n_slots, head0, tid, bar128, s_max, s_inv, s_w);
+        merge_split_pieces_chunked<NH, 256>(prm, b, slot_begin, n_slots, head0, tid, bar256, s_max, s_inv, s_w);
         return;
     }
     const size_t hq = static_cast<size_t>(prm.h_q);

@@ -70,6 +70,10 @@ __device__ __forceinline__ void rope_pair(const uint16_t* src, uint16_t* dst, in
 }
 
 __global__ void __launch_bounds__(kThreads) mla_decode_prologue_kernel(PrologueParams p) {
+    // The decode that usually follows is launched with programmatic dependent launch: this
+    // lets its CTAs start their set-up now; they read the cache only after this grid has
+    // completed and its writes are visible (their griddepcontrol.wait).
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int r = blockIdx.x;
     const int tid = threadIdx.x;
     const int b = r / p.qo_len, j = r % p.qo_len;
