@@ -83,17 +83,20 @@ bool make_map_ckv_chunked(CUtensorMap* map, const void* base, uint64_t rows, uin
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Value view of the ckv cache for the 128-head kernel: dims (64 dims, rows, 8 chunks) with
-// strides (2 B, 1024 B, 128 B); a box (64, box_rows, 4) copies box_rows rows of 256 dims as
-// [4 chunks][box_rows][128 B] with the 128-byte swizzle (the MN-major value operand).
-bool make_map_v_half(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
+// Key view of the ckv cache for the 128-head kernel: dims (64 dims, 8 rows, 8 chunks, rows / 8
+// row groups) with strides (2 B, 1024 B, 128 B, 8192 B); a box (64, 8, 4, page / 8) copies one
+// page's rows of 4 chunks (256 dims) as [row group][chunk][8 rows][128 B] with the 128-byte
+// swizzle, so consecutive pages' boxes make one K-major operand of 4 chunks whose 8-row groups
+// lie 4 KB apart.  The values read the same view: chunks 4 * half.. as the MN-major operand,
+// 64-dim groups 1 KB apart and 8-token groups 4 KB apart.
+bool make_map_ckv_rg4(CUtensorMap* map, const void* base, uint64_t rows, uint32_t page) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
-    cuuint64_t dims[3] = {64, rows, 8};
-    cuuint64_t strides[2] = {mla::kDimCkv * 2, 128};
-    cuuint32_t box[3] = {64, box_rows, 4};
-    cuuint32_t es[3] = {1, 1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+    cuuint64_t dims[4] = {64, 8, 8, rows / 8};
+    cuuint64_t strides[3] = {mla::kDimCkv * 2, 128, 8 * mla::kDimCkv * 2};
+    cuuint32_t box[4] = {64, 8, 4, page / 8};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -226,12 +229,14 @@ mla_status_t run_checked(mla_plan_t plan, const void* q_nope, const void* q_pe, 
         bool ok_ckv;
         if (f8)
             ok_ckv = make_map_codes(&mc.m_ckv, ckv_cache, rows, box);
+        else if (d.pair)
+            ok_ckv = make_map_ckv_rg4(&mc.m_ckv, ckv_cache, rows, static_cast<uint32_t>(d.page_size));
         else
             ok_ckv = chunked ? make_map_ckv_chunked(&mc.m_ckv, ckv_cache, rows, box)
                              : make_map_bf16(&mc.m_ckv, ckv_cache, mla::kDimCkv, rows, box);
         mc.valid = ok_ckv && make_map_bf16(&mc.m_kpe, kpe_cache, mla::kDimKpe, rows, box) &&
                    make_map_bf16(&mc.m_qp, q_pe, mla::kDimKpe, qrows, d.pair ? 128 : hg) &&
-                   (!d.pair || make_map_v_half(&mc.m_v, ckv_cache, rows, std::min(d.page_size, 32))) &&
+                   (!d.pair || make_map_ckv_rg4(&mc.m_v, ckv_cache, rows, static_cast<uint32_t>(d.page_size))) &&
                    (!f8 || make_map_scale(&mc.m_scale, ckv_scale, rows, box));
         if (!mc.valid) return MLA_ERR_CUDA;
         mc.ckv = ckv_cache;

@@ -52,20 +52,27 @@ struct PairCfg {
     static constexpr int kTile = kTileTokens;     // 128 tokens
     static constexpr int kChunkBytes = 128 * 128; // 128 rows x 128 B (64 bf16)
     // rank 0
-    static constexpr int kKSlots = 9;             // one per chunk of a tile: slot = chunk, producer = chunk % 3
+    // K of a tile in 3 slots, one per producer: chunks 0-3 and 4-7 of the latent (64 KB each, one
+    // 4-D box of 4 chunks per page: [row group][chunk][8 rows][128 B], 8-row groups 4 KB apart),
+    // then the rope chunk (16 KB, one 2-D box per page).  Large boxes: one SM's copy engine moves
+    // ~1.5x the bytes per microsecond of 8 KB boxes for the same bytes in flight (measured).
+    static constexpr int kKSlots = 3;
+    static constexpr int kKSlotBytes = 4 * kChunkBytes;   // latent slots; the rope slot uses kChunkBytes
     // A P buffer: the P tile [2 token chunks][128 heads][128 B], then the tile's per-head factors
     // (PairHand); rank 0 stages one and hands it to rank 1 with a single bulk copy.
     static constexpr int kPTileBytes = 2 * kChunkBytes;
     static constexpr int kPBufBytes = kPTileBytes + 2048;              // 1024-aligned stride
     static constexpr int kOffQpe = 0;                                  // [128 heads][128 B] SW128
     static constexpr int kOffK = kOffQpe + kChunkBytes;                // K ring
-    static constexpr int kOffPStage = kOffK + kKSlots * kChunkBytes;   // P of one tile, copied to rank 1
+    static constexpr int kOffPStage = kOffK + 9 * kChunkBytes;         // P of one tile, copied to rank 1
     static constexpr int kSEnd = kOffPStage + kPBufBytes;              // 194 KB
     // rank 1
     static constexpr int kPBufs = 2;
     static constexpr int kOffP = 0;
-    static constexpr int kVSlotBytes = 4 * 32 * 128;                   // [boxes][4 dim chunks][rows][128 B] = 32 tokens x 256 dims
-    static constexpr int kVSlots = 8;             // a whole tile's values; producer = slot % 2
+    // a V slot: 64 tokens x 256 dims as [row group][4 chunks][8 rows][128 B] (4-D page boxes, the
+    // MN-major value operand: 64-dim groups 1 KB apart, 8-token groups 4 KB apart)
+    static constexpr int kVSlotBytes = 64 * 4 * 128;
+    static constexpr int kVSlots = 4;             // a whole tile's values; producer = slot % 2
     static constexpr int kOffV = kOffP + kPBufs * kPBufBytes;
     static constexpr int kOEnd = kOffV + kVSlots * kVSlotBytes;        // 196 KB
     static constexpr int kOffMisc = kSEnd > kOEnd ? kSEnd : kOEnd;
@@ -271,30 +278,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                     win_base = first_page;
                     win_page = (win_base + lane <= seg_last_page) ? pages[win_base + lane] : 0;
                 }
-                for (int c = 0; c < 9 && ok; ++c) {   // 8 ckv chunks of 64 dims, then kpe
+                for (int sl = 0; sl < C::kKSlots && ok; ++sl) {   // latent chunks 0-3, 4-7, then kpe
                     const uint32_t s = kcount % C::kKSlots, use = kcount / C::kKSlots;
                     if (static_cast<int>(s) % C::kKProducers != pid) {   // another producer's slot
                         ++kcount;
                         continue;
                     }
-                    if (lane == 0 && c == 8) MLA_TRACE_EVENT(0, kcount / 9);
+                    if (lane == 0 && sl == 2) MLA_TRACE_EVENT(0, kcount / C::kKSlots);
                     if (lane == 0 && use > 0)
                         ok = pair_wait(&misc->k_empty[s], (use - 1) & 1, misc, partner_abort, prm.status, 42);
                     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                     if (!ok) break;
                     if (lane == 0) MLA_TRACE_UNIT(0, kcount);
-                    uint8_t* dst = smem + C::kOffK + s * C::kChunkBytes;
-                    if (lane == 0) mbar_arrive_expect_tx(&misc->k_full[s], static_cast<uint32_t>(nbox * P * 128));
+                    uint8_t* dst = smem + C::kOffK + s * C::kKSlotBytes;
+                    const uint32_t row_bytes = sl < 2 ? 4 * 128 : 128;   // bytes a token brings into the slot
+                    if (lane == 0) mbar_arrive_expect_tx(&misc->k_full[s], static_cast<uint32_t>(nbox * P) * row_bytes);
                     for (int bx = 0; bx < nbox; ++bx) {
                         const int pg = __shfl_sync(0xffffffffu, win_page, (first_page + bx - win_base) & 31);
                         if (lane == 0) {
-                            if (c < 8)
-                                tma_load_2d(dst + bx * P * 128, &tm_ckv, &misc->k_full[s], c * 64, pg * P);
+                            if (sl < 2)
+                                tma_load_4d(dst + bx * P * row_bytes, &tm_ckv, &misc->k_full[s], 0, 0, 4 * sl,
+                                            pg * (P / 8));
                             else
-                                tma_load_2d(dst + bx * P * 128, &tm_kpe, &misc->k_full[s], 0, pg * P);
+                                tma_load_2d(dst + bx * P * row_bytes, &tm_kpe, &misc->k_full[s], 0, pg * P);
                         }
                     }
-                    if (lane == 0 && c == 0) MLA_TRACE_EVENT(5, kcount / 9);
+                    if (lane == 0 && sl == 0) MLA_TRACE_EVENT(5, kcount / C::kKSlots);
                     if (lane == 0) MLA_TRACE_UNIT(1, kcount);
                     ++kcount;
                 }
@@ -319,7 +328,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                 bool new_seg = true;
                 // descriptors of slot 0 / q_pe at k = 0; a slot or a 16-dim step only moves the start
                 // address (in 16-byte units, no carry out of its field below 256 KB)
-                const uint64_t kdesc0 = umma_desc_sw128_c<16, 1024>(smem_u32(smem + C::kOffK));
+                // latent chunks: 8-row groups 4 KB apart (4 chunks of a row group side by side)
+                const uint64_t kdesc0 = umma_desc_sw128_c<16, 4096>(smem_u32(smem + C::kOffK));
+                const uint64_t rdesc0 = umma_desc_sw128_c<16, 1024>(smem_u32(smem + C::kOffK + 2 * C::kKSlotBytes));
                 const uint64_t qdesc0 = umma_desc_sw128_c<16, 1024>(smem_u32(smem + C::kOffQpe));
                 while (more && ok) {
                     const bool last = cur.last();
@@ -333,27 +344,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                     MLA_TRACE_EVENT(1, tcount);
                     tc_fence_after();
                     const uint32_t d = tmem + C::kTmemS + buf * 128;
-                    // every tile fills each of the 9 slots once: chunk c is in slot c, its use number
-                    // is the tile count.  A slot is filled by TMA, so waiting on its barrier is enough to
-                    // order the MMAs' reads after the copy (the tcgen05 fence above, once per tile,
-                    // orders them after the softmax's reads of this S buffer).
-                    static_assert(C::kKSlots == 9, "one slot per chunk of a tile");
+                    // every tile fills each of the 3 slots once (chunks 0-3, 4-7, the rope chunk): a
+                    // slot's use number is the tile count.  A slot is filled by TMA, so waiting on its
+                    // barrier is enough to order the MMAs' reads after the copy (the tcgen05 fence
+                    // above, once per tile, orders them after the softmax's reads of this S buffer).
+                    static_assert(C::kKSlots == 3, "latent chunks 0-3, 4-7, then the rope chunk");
                     for (int c = 0; c < 9 && ok; ++c) {
-                        ok = pair_wait(&misc->k_full[c], tcount & 1, misc, partner_abort, prm.status, 45);
-                        if (!ok) break;
-                        MLA_TRACE_UNIT(2, kcount);
-                        const uint64_t bd = kdesc0 + static_cast<uint64_t>((c * C::kChunkBytes) >> 4);
+                        const int sl = c < 8 ? c >> 2 : 2;
+                        if ((c & 3) == 0) {   // first chunk of a slot: wait for it to land
+                            ok = pair_wait(&misc->k_full[sl], tcount & 1, misc, partner_abort, prm.status, 45);
+                            if (!ok) break;
+                            MLA_TRACE_UNIT(2, kcount);
+                        }
                         if (c < 8) {
+                            const uint64_t bd = kdesc0 + static_cast<uint64_t>((sl * C::kKSlotBytes + (c & 3) * 1024) >> 4);
 #pragma unroll
                             for (int k = 0; k < 4; ++k)
                                 umma_bf16_ts(d, tmem + C::kTmemQ + c * 32 + k * 8, bd + 2 * k, kIdS, (c | k) != 0);
                         } else {
 #pragma unroll
-                            for (int k = 0; k < 4; ++k) umma_bf16(d, qdesc0 + 2 * k, bd + 2 * k, kIdS, 1);
+                            for (int k = 0; k < 4; ++k) umma_bf16(d, qdesc0 + 2 * k, rdesc0 + 2 * k, kIdS, 1);
                         }
-                        umma_commit(&misc->k_empty[c]);
-                        MLA_TRACE_UNIT(3, kcount);
-                        ++kcount;
+                        if ((c & 3) == 3 || c == 8) {   // last chunk of a slot: release it
+                            umma_commit(&misc->k_empty[sl]);
+                            MLA_TRACE_UNIT(3, kcount);
+                            ++kcount;
+                        }
                     }
                     if (!ok) break;
                     umma_commit(&misc->s_full[buf]);
@@ -501,7 +517,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
             // producer pid issues the slots s % kVProducers == pid
             const int pid = pair_producer(warp);
             if (lane == 0) prefetch_tensormap(&tm_v);
-            const int box_rows = P < 32 ? P : 32;
             uint32_t vcount = 0;
             bool ok = true;
             TileCursorT<C::kTile> cur;
@@ -515,16 +530,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                     win_base = -(1 << 30);
                 }
                 const int ntok = cur.ntok();
-                const int nq = (ntok + 31) / 32;
+                const int nv = (ntok + 63) / 64;   // 64-token V slots per half
                 const int first_page = cur.t0 / P;
-                const int last_page = (cur.t0 + nq * 32 - 1) / P;
+                const int last_page = (cur.t0 + nv * 64 - 1) / P;
                 if (last_page + 1 > win_base + 32 || first_page < win_base) {
                     const int seg_last_page = (cur.sg.t_end - 1) / P;
                     win_base = first_page;
                     win_page = (win_base + lane <= seg_last_page) ? pages[win_base + lane] : 0;
                 }
                 for (int half = 0; half < 2 && ok; ++half) {
-                    for (int q = 0; q < nq && ok; ++q) {
+                    for (int q = 0; q < nv && ok; ++q) {
                         const uint32_t s = vcount % C::kVSlots, use = vcount / C::kVSlots;
                         if (static_cast<int>(s) % C::kVProducers != pid) {   // another producer's slot
                             ++vcount;
@@ -537,14 +552,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                         uint8_t* dst = smem + C::kOffV + s * C::kVSlotBytes;
                         if (lane == 0) MLA_TRACE_UNIT1(3, vcount);
                         if (lane == 0) mbar_arrive_expect_tx(&misc->v_full[s], C::kVSlotBytes);
-                        if (pid == 0 && lane == 0 && half == 0 && q == 0) MLA_TRACE_EVENT(0, vcount / (2 * nq));
-                        if (pid == 0 && lane == 0 && half == 1 && q == nq - 1) MLA_TRACE_EVENT(1, vcount / (2 * nq));
-                        for (int bx = 0; bx < 32 / box_rows; ++bx) {
-                            const int t = cur.t0 + q * 32 + bx * box_rows;
+                        if (pid == 0 && lane == 0 && half == 0 && q == 0) MLA_TRACE_EVENT(0, vcount / (2 * nv));
+                        if (pid == 0 && lane == 0 && half == 1 && q == nv - 1) MLA_TRACE_EVENT(1, vcount / (2 * nv));
+                        // whole pages (a slot starts on a page boundary); past the request's last page
+                        // the page table window gives page 0, whose rows feed no MMA step
+                        for (int bx = 0; bx < 64 / P; ++bx) {
+                            const int t = cur.t0 + q * 64 + bx * P;
                             const int pg = __shfl_sync(0xffffffffu, win_page, (t / P - win_base) & 31);
                             if (lane == 0)
-                                tma_load_3d(dst + bx * 4 * box_rows * 128, &tm_v, &misc->v_full[s], 0, pg * P + (t % P),
-                                            4 * half);
+                                tma_load_4d(dst + bx * P * 512, &tm_v, &misc->v_full[s], 0, 0, 4 * half, pg * (P / 8));
                         }
                         ++vcount;
                     }
@@ -563,17 +579,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
         } else if (warp == 1) {
             // ---------------------------------------------------------- MMA issuer: O += P V
             if (lane == 0) {
-                const int box_rows = P < 32 ? P : 32;
-                const uint32_t lbo = static_cast<uint32_t>(box_rows) * 128;
                 uint32_t tcount = 0, vcount = 0, segc = 0, rcount = 0, zcount = 0;
                 bool ok = true;
                 TileCursorT<C::kTile> cur;
                 bool more = cur.init(prm.segments, seg_begin, seg_end);
                 bool new_seg = true;
                 const uint64_t pdesc0 = umma_desc_sw128_c<16, 1024>(smem_u32(smem + C::kOffP));
-                const uint64_t vdesc0 = umma_desc_sw128(smem_u32(smem + C::kOffV), lbo, 1024);
-                // second 16-token step of a 32-token V slot: the next box (page size 16) or row 16
-                const uint32_t voff1 = (box_rows == 16 ? 4 * lbo : 16 * 128) >> 4;
+                const uint64_t vdesc0 = umma_desc_sw128_c<1024, 4096>(smem_u32(smem + C::kOffV));
                 while (more && ok) {
                     const bool first = cur.first();
                     const int ntok = cur.ntok();
@@ -591,15 +603,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                     fence_proxy_async_smem();
                     tc_fence_after();
                     const uint64_t pdesc = pdesc0 + static_cast<uint64_t>((buf * C::kPBufBytes) >> 4);
-                    const int nq = (ntok + 31) / 32;
+                    const int nv = (ntok + 63) / 64;
                     const bool partial = (ntok & 15) != 0;
                     for (int half = 0; half < 2 && ok; ++half) {
-                        for (int q = 0; q < nq && ok; ++q) {
+                        for (int q = 0; q < nv && ok; ++q) {
                             const uint32_t s = vcount % C::kVSlots;
                             ok = pair_wait(&misc->v_full[s], (vcount / C::kVSlots) & 1, misc, partner_abort, prm.status, 56);
                             if (!ok) break;
                             MLA_TRACE_UNIT1(0, vcount);
-                            if (partial && q == nq - 1) {
+                            if (partial && q == nv - 1) {
                                 // the slot with the tile's last token: its rows past it are zeroed first
                                 mbar_arrive(&misc->vz_go[half]);
                                 ok = pair_wait(&misc->vz_done[half], zcount & 1, misc, partner_abort, prm.status, 55);
@@ -609,11 +621,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                             }
                             // a TMA-filled slot: its barrier wait orders the MMAs' reads after the copy
                             const uint64_t bslot = vdesc0 + static_cast<uint64_t>((s * C::kVSlotBytes) >> 4);
-                            for (int k2 = 0; k2 < 2; ++k2) {
-                                const int kk = 2 * q + k2;   // 16-token step within the tile
+                            for (int k4 = 0; k4 < 4; ++k4) {
+                                const int kk = 4 * q + k4;   // 16-token step within the tile
                                 if (16 * kk >= ntok) break;
                                 const uint64_t ad = pdesc + static_cast<uint64_t>(((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4);
-                                umma_bf16(tmem + 256 * half, ad, bslot + (k2 ? voff1 : 0u), kIdPV,
+                                umma_bf16(tmem + 256 * half, ad, bslot + static_cast<uint64_t>((k4 * 8192) >> 4), kIdPV,
                                           (first && kk == 0) ? 0u : 1u);
                             }
                             umma_commit(&misc->v_empty[s]);
@@ -636,7 +648,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
             const int h = threadIdx.x - 128;
             const uint32_t lane_base = static_cast<uint32_t>(warp - 4) * 32;
             const uint32_t s_pempty = mapa_shared(smem_u32(&misc->p_empty[0]), partner);
-            const int box_rows = P < 32 ? P : 32;
             // requests with no tokens: out = 0, lse = -inf
             for (int si = seg_begin; si < seg_end; ++si) {
                 const Segment sg = prm.segments[si];
@@ -654,7 +665,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                 for (int t0 = sg.t_begin; t0 < sg.t_end && ok; t0 += C::kTile) {
                     const int ntok = min(C::kTile, sg.t_end - t0);
                     const bool first = t0 == sg.t_begin, last = t0 + C::kTile >= sg.t_end;
-                    const int nq = (ntok + 31) / 32;
+                    const int nv = (ntok + 63) / 64;
                     const uint32_t buf = tcount % C::kPBufs, ub = tcount / C::kPBufs;
                     ok = pair_wait<true>(&misc->p_full[buf], ub & 1, misc, partner_abort, prm.status, 61);
                     ok = !named_barrier_or(1, 128, !ok || aborted());
@@ -666,20 +677,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                     const float alpha = hd->alpha[h];
                     const float fin_m = last ? hd->fin_m[h] : 0.f;
                     const float fin_l = last ? hd->fin_l[h] : 1.f;
-                    // value rows [ntok, next multiple of 16) of the partial 32-token quarter of one half:
+                    // value rows [ntok, next multiple of 16) of the partial 64-token slot of one half:
                     // stale or NaN page tails the step's MMA would otherwise read.  The MMA thread
                     // raises vz_go[half] once that slot has landed (it is the ring's consumer; these
                     // warps could not tell the slot's phase apart from its previous use's).
                     auto zero_half = [&](int half) {
-                        const int qz = ntok >> 5, r_lo = ntok & 31, r_hi = (r_lo + 15) & ~15;
-                        const uint32_t vi = vcount + half * nq + qz;
+                        const int qz = ntok >> 6, r_lo = ntok & 63, r_hi = (r_lo + 15) & ~15;
+                        const uint32_t vi = vcount + half * nv + qz;
                         ok = pair_wait(&misc->vz_go[half], zcount & 1, misc, partner_abort, prm.status, 62);
                         if (ok) {
                             uint8_t* slot = smem + C::kOffV + (vi % C::kVSlots) * C::kVSlotBytes;
                             for (int i = h; i < (r_hi - r_lo) * 32; i += 128) {
                                 const int r = r_lo + i / 32, c = (i / 8) & 3, u = i & 7;
-                                *reinterpret_cast<uint4*>(slot + (r / box_rows) * 4 * box_rows * 128 + c * box_rows * 128 +
-                                                          (r % box_rows) * 128 + u * 16) = make_uint4(0, 0, 0, 0);
+                                *reinterpret_cast<uint4*>(slot + (r >> 3) * 4096 + c * 1024 + (r & 7) * 128 + u * 16) =
+                                    make_uint4(0, 0, 0, 0);
                             }
                         }
                         fence_proxy_async_smem();
@@ -713,7 +724,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::kThreads, 1
                         if (!ok) break;
                         ++zcount;
                     }
-                    vcount += 2 * nq;
+                    vcount += 2 * nv;
                     // this tile's O += P V done: its P buffer goes back to rank 0
                     ok = pair_wait(&misc->pv_done[buf], ub & 1, misc, partner_abort, prm.status, 63);
                     ok = !named_barrier_or(1, 128, !ok || aborted());
