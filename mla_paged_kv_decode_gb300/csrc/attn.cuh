@@ -122,10 +122,16 @@ __device__ __forceinline__ bool wait_phase_flag(uint64_t* bar, uint32_t parity, 
 #else
 #define MLA_TRACE_NOW() global_timer_ns()
 #endif
+// the two CTAs whose per-tile events are recorded: MLA_TRACE_FIRST and the next one
+#ifndef MLA_TRACE_FIRST
+#define MLA_TRACE_FIRST 0
+#endif
 #define MLA_TRACE_EVENT(ev, idx)                                                              \
     do {                                                                                      \
-        if (prm.trace && blockIdx.x < 2 && (idx) < 256)                                       \
-            prm.trace[(blockIdx.x * 8 + (ev)) * 256 + (idx)] = MLA_TRACE_NOW();              \
+        if (prm.trace && blockIdx.x >= MLA_TRACE_FIRST && blockIdx.x < MLA_TRACE_FIRST + 2 && \
+            (idx) < 256)                                                                      \
+            prm.trace[((blockIdx.x - MLA_TRACE_FIRST) * 8 + (ev)) * 256 + (idx)] =            \
+                MLA_TRACE_NOW();                                                              \
     } while (0)
 // CTA 0 only: a timestamp per unit of work (a ring slot fill, ...) in the area of CTAs 2 and 3,
 // lane `ln` (0..3) of 1024 entries each.

@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                 // bytes per token: bf16 ckv + kpe = 1152
                 if (lane == 0)
                     mbar_arrive_expect_tx(bar_full, static_cast<uint32_t>(nbox * box_rows * (C::kStageLoadBytes / kNarrowStageTok)));
-                if (lane == 0 && pid == 0) MLA_TRACE_EVENT(st == 0 ? 0 : 1, tile_idx);
+                if (lane == 0) MLA_TRACE_EVENT(pid, tile_idx);
                 for (int bx = 0; bx < nbox; ++bx) {
                     const int t = t_st + bx * box_rows;
                     const int pg = __shfl_sync(0xffffffffu, win_page, (t / P - win_base) & 31);
@@ -338,6 +338,14 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                 continue;
             }
             load_q(sg.b);
+#ifdef MLA_TRACE
+            if (prm.trace && blockIdx.x == MLA_TRACE_FIRST && kr == 0 && lane == 0 && si - seg_begin < 1024) {
+                uint64_t t_;   // stamped once this thread's query words have arrived
+                asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_) : "r"(qa[8][3]), "r"(qa[0][0]));
+                prm.trace[2 * 8 * 256 + (tg * 2 + 1) * 1024 + (si - seg_begin)] = t_;
+            }
+#endif
+
             float o[16][4];
 #pragma unroll
             for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
@@ -370,7 +378,7 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                 const uint32_t st_addr = stage0 + sl * C::kStageBytes;
                 ok = !named_barrier_or(named_bar, 128, !ok || *reinterpret_cast<volatile int*>(&misc->abort_flag));
                 if (!ok) break;
-                if (cw == 0 && lane == 0) MLA_TRACE_EVENT(2, (uint32_t)tile_in_seg);
+                if (kr == 0 && lane == 0) MLA_TRACE_EVENT(tg ? 6 : 2, scount);
                 // ---- partial scores over this warp's 144 dims for the 4 n8 token tiles
                 float sc[4][4];
 #pragma unroll
@@ -413,7 +421,7 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                     }
                 }
                 named_barrier_sync(named_bar, 128);
-                if (cw == 0 && lane == 0) MLA_TRACE_EVENT(3, (uint32_t)tile_in_seg);
+                if (cw == 0 && lane == 0) MLA_TRACE_EVENT(3, scount);
                 float s4[4];   // scores of (row g, tokens 8kr + 2c4, +1) and (row g + 8, same tokens)
                 {
                     const float4* src = reinterpret_cast<const float4*>(part);
@@ -478,7 +486,7 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                     const int pcol = kt * 16 + ((lane & 16) ? 8 : 0);
                     ldsm_x4(smem_u32(pbuf) + prow * C::kPRowBytes + pcol * 2, pa[kt][0], pa[kt][1], pa[kt][2], pa[kt][3]);
                 }
-                if (cw == 0 && lane == 0) MLA_TRACE_EVENT(4, (uint32_t)tile_in_seg);
+                if (cw == 0 && lane == 0) MLA_TRACE_EVENT(4, scount);
                 // ---- O[16 x 128 dims of this warp] += P V
 #pragma unroll
                 for (int kt = 0; kt < 2; ++kt) {
@@ -499,10 +507,11 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                     }
                 }
                 __syncwarp();
-                if (cw == 0 && lane == 0) MLA_TRACE_EVENT(5, (uint32_t)tile_in_seg);
+                if (kr == 0 && lane == 0) MLA_TRACE_EVENT(tg ? 7 : 5, scount);
                 if (lane == 0) mbar_arrive(&misc->empty[sl]);
                 ++scount;
             }
+
             if (C::kTokenGroups == 2) {
                 // Both token groups meet at every segment end, also after a bounded wait ran out,
                 // and leave together: neither can then block in the cross-group barriers below
@@ -583,6 +592,10 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                     named_barrier_sync(merge_bar, 256);   // the buffer is rewritten next
                 }
             }
+#ifdef MLA_TRACE
+            if (prm.trace && blockIdx.x == MLA_TRACE_FIRST && kr == 0 && lane == 0 && si - seg_begin < 1024)
+                prm.trace[2 * 8 * 256 + (tg * 2) * 1024 + (si - seg_begin)] = global_timer_ns();
+#endif
             // At the unit's last segment token group 1 has no more tiles: if the segment is a
             // split piece it stays to merge with group 0 (256 threads, one round of loads)
             const bool wide = C::kTokenGroups == 2 && sg.slot >= 0 && si == seg_end - 1;
