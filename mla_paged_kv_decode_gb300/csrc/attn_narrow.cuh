@@ -100,6 +100,20 @@ struct NarrowMisc {
     float tg_m[16], tg_l[16];   // token-group merge: running max and row sum of group 1
 };
 
+// Debug builds (MLA_TRACE): a timestamp at step k of a segment switch of the traced CTA, per
+// token group, in the per-unit area of the trace buffer.
+#ifdef MLA_TRACE
+#define NARROW_STAMP(k)                                                                                   \
+    do {                                                                                                  \
+        if (prm.trace && blockIdx.x == MLA_TRACE_FIRST && kr == 0 && lane == 0 && si - seg_begin < 16)     \
+            prm.trace[2 * 8 * 256 + (tg * 16 + (k)) * 16 + (si - seg_begin)] = global_timer_ns();         \
+    } while (0)
+#else
+#define NARROW_STAMP(k) \
+    do {                \
+    } while (0)
+#endif
+
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
@@ -339,10 +353,10 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
             }
             load_q(sg.b);
 #ifdef MLA_TRACE
-            if (prm.trace && blockIdx.x == MLA_TRACE_FIRST && kr == 0 && lane == 0 && si - seg_begin < 1024) {
+            if (prm.trace && blockIdx.x == MLA_TRACE_FIRST && kr == 0 && lane == 0 && si - seg_begin < 16) {
                 uint64_t t_;   // stamped once this thread's query words have arrived
                 asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_) : "r"(qa[8][3]), "r"(qa[0][0]));
-                prm.trace[2 * 8 * 256 + (tg * 2 + 1) * 1024 + (si - seg_begin)] = t_;
+                prm.trace[2 * 8 * 256 + (tg * 16 + 1) * 16 + (si - seg_begin)] = t_;
             }
 #endif
 
@@ -519,6 +533,7 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                 ok = !named_barrier_or(merge_bar, 256, !ok || *reinterpret_cast<volatile int*>(&misc->abort_flag));
             }
             if (!ok) break;
+            NARROW_STAMP(6);   // both token groups at the segment end
             if (kr == 0 && lane == 0) MLA_TRACE_CTA(2 + grp);
             // A split piece takes its arrival ticket now; the atomic's round trip overlaps the
             // row sums and the token-group merge below, and only the ticket's use waits for it.
@@ -545,6 +560,7 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                 const int row = g + 8 * r;
                 l[r] = (rowmax[row] + rowmax[16 + row]) + (rowmax[32 + row] + rowmax[48 + row]);
             }
+            NARROW_STAMP(5);   // row sums
             if (C::kTokenGroups == 2) {
                 // ---- merge the two token groups: group 1 passes (O, m, l) to group 0 through shared
                 // memory (the partial-score buffers of both groups, two halves of O), group 0 combines
@@ -592,10 +608,7 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                     named_barrier_sync(merge_bar, 256);   // the buffer is rewritten next
                 }
             }
-#ifdef MLA_TRACE
-            if (prm.trace && blockIdx.x == MLA_TRACE_FIRST && kr == 0 && lane == 0 && si - seg_begin < 1024)
-                prm.trace[2 * 8 * 256 + (tg * 2) * 1024 + (si - seg_begin)] = global_timer_ns();
-#endif
+            NARROW_STAMP(0);   // token groups merged
             // At the unit's last segment token group 1 has no more tiles: if the segment is a
             // split piece it stays to merge with group 0 (256 threads, one round of loads)
             const bool wide = C::kTokenGroups == 2 && sg.slot >= 0 && si == seg_end - 1;
@@ -625,6 +638,7 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                     lbase[g] = (m_run[0] + log2f(l[0])) * 0.69314718055994530942f;
                     lbase[g + 8] = (m_run[1] + log2f(l[1])) * 0.69314718055994530942f;
                 }
+                NARROW_STAMP(2);   // epilogue stores issued
             }
             if (sg.slot >= 0) {
                 // ---- split request: the piece with the last ticket merges all of them in slot order
@@ -637,8 +651,10 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                 const uint32_t nthr = wide ? 256u : 128u;
                 if (tg == 0 && gt == 0) misc->merge_flag[hgi] = (ticket == sg.n_slots - 1) ? 1 : 0;
                 named_barrier_sync(mbar, nthr);
+                NARROW_STAMP(3);   // ticket known
                 if (!misc->merge_flag[hgi]) {
                     if (tg == 0) __threadfence();
+                    NARROW_STAMP(7);   // partial stores fenced
                     named_barrier_sync(mbar, nthr);
                     if (tg == 0 && gt == 0) atomicAdd(&prm.ready[ctr], 1);
                 } else {
@@ -676,6 +692,7 @@ __global__ void __launch_bounds__(NarrowCfg<HG>::kThreads, 1)
                     }
                 }
                 named_barrier_sync(mbar, nthr);
+                NARROW_STAMP(4);   // published or merged
             }
         }
     }
