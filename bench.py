@@ -20,6 +20,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -53,16 +54,25 @@ def peaks():
 NOMINAL_HBM_GBS = 7900.0   # GB300 HBM3e, nominal
 
 
+def strip_comments(src: str) -> str:
+    """C/C++ source without its comments, trailing blanks and empty lines (the sources hold
+    no comment marker inside a string literal)."""
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    lines = (re.sub(r"//.*", "", ln).rstrip() for ln in src.splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def kernel_source_hash() -> str:
-    """Hash of the sources the attention kernels are built from (the prologue kernel, a
-    separate translation unit, is not one of them)."""
+    """Hash of the code the attention kernels are built from, comments left out (the prologue
+    kernel, a separate translation unit, is not one of them): a change of the compiled code
+    changes it, an edit of a comment does not."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_paged_kv_decode_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f == "prologue.cu":
             continue
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(f.encode() + strip_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -3,11 +3,12 @@
 // with warp-level mma.sync (m16n8k16, bf16 in, fp32 accumulate).
 //
 // Why warp MMA here: the score contraction of a 16-head request has 16 rows per query, and a
-// tcgen05.mma costs ~97 SM cycles per instruction whatever its N up to 128 (measured on this
-// GPU), so tcgen05 tiles of 16 heads and 128 tokens would need ~68 instructions per tile of
-// bf16 operands.  The warp MMA has no such floor: 16 heads x 1088 MACs per cached token is
-// ~17 cycles per token per SM, against the ~49 cycles per token an SM may spend at full HBM
-// bandwidth.  The 64/128-head path (attn_pair.cuh) and the e4m3 cache (attn_e4m3.cuh) run
+// tcgen05.mma of M 128 has a floor (one of N 64 costs about what one of N 128 does, ~64 SM
+// cycles, measured on this GPU), so tcgen05 tiles of 128 tokens x 16 heads would take 68
+// instructions per tile (~34 cycles per token at that floor) with TMEM round trips for the
+// softmax in between.  The warp MMA has no such floor: 16 heads x 1088 MACs per cached token
+// is ~17 cycles per token per SM, against the ~49 cycles per token an SM may spend at full
+// HBM bandwidth.  The 64/128-head path (attn_pair.cuh) and the e4m3 cache (attn_e4m3.cuh) run
 // on tcgen05.
 //
 // Absorbed MLA decode is MQA with one KV head: key [ckv | kpe] (576), value ckv (512)

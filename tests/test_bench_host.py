@@ -59,6 +59,14 @@ def test_source_hash_covers_the_attention_sources_only():
     assert h == bench.kernel_source_hash()        # deterministic
 
 
+def test_source_hash_ignores_comments_only():
+    a = "int f(int x) {  // scale\n    return 2 * x;\n}\n"
+    b = "// doubles x\nint f(int x) {\n    return 2 * x;  /* twice */\n}\n\n"
+    c = "int f(int x) {\n    return 3 * x;\n}\n"
+    assert bench.strip_comments(a) == bench.strip_comments(b) == "int f(int x) {\n    return 2 * x;\n}"
+    assert bench.strip_comments(c) != bench.strip_comments(a)
+
+
 def test_cpu_baseline_line():
     from workloads import WORKLOADS, make_inputs
     inp = make_inputs(WORKLOADS["tiny"])
