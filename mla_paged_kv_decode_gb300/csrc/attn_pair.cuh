@@ -10,14 +10,16 @@
 //
 //   rank 0 ("S CTA"):  q_nope sits in TMEM (256 columns, the A operand), q_pe in shared
 //     memory; S = Q K^T is accumulated into one of two 128-column TMEM buffers by
-//     36 MMAs (M 128, N 128, K 16) per 128-token tile from a ring of 16 KB K chunks.
+//     36 MMAs (M 128, N 128, K 16) per 128-token tile from a ring of three K slots (latent
+//     chunks 0-3 and 4-7, 64 KB each, then the rope part), filled with 4-D page boxes.
 //     The softmax warpgroup (thread = head) reads S, keeps the running max and sum, and
 //     writes P (bf16) and the rescale factors into a local staging tile, which one thread
 //     hands to rank 1's shared memory with bulk copies (cp.async.bulk over the cluster).
 //     Per-thread remote stores of P (st.shared::cluster) measured 17 % slower per step:
 //     thousands of 16-byte transactions per tile held up the SM's TMA loads.
 //   rank 1 ("O CTA"):  O (128 x 512 fp32) fills its TMEM; O += P V is 16 MMAs (M 128,
-//     N 256, K 16) per tile, V streamed as [4 dim chunks][32 tokens] slots.  A correction
+//     N 256, K 16) per tile, V streamed in 64-token slots of 256 dims through the same 4-D
+//     page view as the keys.  A correction
 //     warpgroup rescales O rows when rank 0 raised a head's running max (lazily, by more
 //     than 2^8), zeroes value rows past the last token of a partial tile, and writes the
 //     normalised output (or a split piece's partial) at the end of a segment.
